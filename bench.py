@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of the Parallax attention layer (forward + backward) on B300.
+
+One step = one pass of the whole layer: forward (pass 1, projection, pass 2)
+and backward (dq, dk, dv, dP) over one batch of the workload
+``c4`` (causal, bf16, B=8, H=16, T=4096, d=64; q, k, v, dO ~ N(0,1),
+P_h ~ N(0, (0.1/sqrt(d))^2), seed 3), inputs resident in HBM.
+
+Metric: algorithmic TFLOP/s of the step (28 d flops per causal pair: 8 d
+forward, 20 d backward) and its fraction of the measured bf16 tensor peak.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs its own independent set of heads (weak scaling, no collective on the
+data path) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import plx_synth  # noqa: E402
+
+METRIC = "Parallax attn fwd/bwd TFLOP/s & % of B300 bf16 tensor peak, T=4096"
+UNIT = "TFLOP/s"
+L2_BYTES = 126 * 1024 * 1024
+
+# Algorithmic flops per causal pair, per kernel role (each MMA-shaped product
+# counted once: S, mu_k | G, o | S, E, R | G, Y, dV, dK (3 terms), dQ).
+FWD_FLOPS_PER_PAIR_D = 8
+BWD_FLOPS_PER_PAIR_D = 20
+KERNEL_FLOPS_PER_PAIR_D = {
+    "tc_pass1": 4, "simt_pass1": 4,
+    "tc_pass2": 4, "simt_pass2": 4,
+    "tc_bwd_b1": 6, "simt_bwd_b1": 6,
+    "tc_bwd_b3": 14, "simt_bwd_b3": 14,
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "sm_max_mhz": p.get("sm_max_mhz", 2032.0), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "sm_max_mhz": 2032.0, "source": "fallback"}
+
+
+def fp32_simt_peak_tflops(sm_mhz: float) -> float:
+    # 148 SMs x 128 FP32 lanes x 2 flops (FFMA) per clock
+    return 148 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ------------------------------------------------------------------ dist
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws an independent set of heads (weak scaling)."""
+    return base + 7919 * rank
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="plx_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+               "-f", self.path]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for r in csv.reader(io.StringIO(f.read())):
+                    if len(r) >= 9:
+                        rows.append([x.strip() for x in r])
+        finally:
+            os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows) -> dict:
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    # samples under load: the upper half of the observed clocks/power
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+            "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+def gpu_query_id(torch, dev) -> str | None:
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", 0)
+        devid = getattr(props, "pci_device_id", 0)
+        if bus is not None:
+            return f"{dom:08X}:{bus:02X}:{devid:02X}.0"
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------- CPU baseline
+def oracle_sample(inp: dict, nheads: int, rows: int, threads: int) -> tuple[float, int]:
+    """Time the oracle's forward + backward on `nheads` heads (batch 0) over
+    the first `rows` queries (and keys).  Returns (seconds, causal pairs)."""
+    import oracle
+    d = inp["d"]
+    sl = (slice(0, 1), slice(0, nheads), slice(0, rows))
+    q = plx_synth.widen(inp["q"][sl])
+    k = plx_synth.widen(inp["k"][sl])
+    v = plx_synth.widen(inp["v"][sl])
+    do = plx_synth.widen(inp["dout"][sl])
+    P = inp["P"][:nheads].astype(np.float64)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, P, nthreads=threads)
+    oracle.backward(q, k, v, P, do, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return dt, plx_synth.causal_pairs(1, nheads, rows)
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def calibrate_rows(inp, nheads, threads, target_s, T) -> int:
+    """Largest row count (multiple of 64, <= T) whose sample takes ~target_s."""
+    r0 = min(T, 512)
+    dt, _ = oracle_sample(inp, nheads, r0, threads)
+    if dt <= 0:
+        return T
+    scale = math.sqrt(target_s / dt)
+    rows = int(min(T, max(64, r0 * scale)) // 64 * 64)
+    return max(64, rows)
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    """The oracle (fp64 C loops) timed on this host's cores: the reference arm."""
+    if rank != 0:
+        return
+    w = plx_synth.WORKLOADS[args.workload]
+    inp = plx_synth.generate_workload(args.workload, B=1, H=w.H, backward=True)
+    threads = cpu_threads()
+    nheads = min(w.H, threads)
+    budget = max(10.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = calibrate_rows(inp, nheads, threads, budget, w.T)
+    for _ in range(args.warmup):
+        oracle_sample(inp, nheads, rows, threads)
+    tot_s, tot_pairs = 0.0, 0
+    for _ in range(args.steps):
+        dt, pairs = oracle_sample(inp, nheads, rows, threads)
+        tot_s += dt
+        tot_pairs += pairs
+    flops = tot_pairs * (FWD_FLOPS_PER_PAIR_D + BWD_FLOPS_PER_PAIR_D) * w.d
+    value = flops / tot_s / 1e12
+    sample = (f"{nheads} heads x first {rows} queries/keys of one batch, fwd+bwd, per step "
+              f"(full step: {w.B * w.H} heads x {w.T})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_s / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, path):
+    return {"workload": w.describe, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "path": path,
+            "pairs_per_step": plx_synth.causal_pairs(w.B, w.H, w.T),
+            "algorithmic_flops_per_pair": f"{FWD_FLOPS_PER_PAIR_D}d fwd + {BWD_FLOPS_PER_PAIR_D}d bwd",
+            "l2": "inputs larger than L2 (q,k,v,dO: 4 x {:.0f} MB bf16 > 126 MB); no flush".format(
+                w.B * w.H * w.T * w.d * 2 / 1e6)}
+
+
+def run_ours(args, world, rank):
+    import torch
+    import parallax_local_linear_fwd_b300 as plx
+
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist_init("nccl")
+    w = plx_synth.WORKLOADS[args.workload]
+    inp = plx_synth.generate_workload(args.workload, seed=rank_seed(w.seed, rank), backward=True)
+    B, H, T, d = w.B, w.H, w.T, w.d
+
+    def host(x):
+        if x.dtype == np.uint16:
+            t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(x)
+        return t.pin_memory()
+
+    h_in = {k: host(inp[k]) for k in ("q", "k", "v", "P", "dout")}
+    d_in = {k: t.to(dev) for k, t in h_in.items()}
+    q, k, v, P, do = (d_in[x] for x in ("q", "k", "v", "P", "dout"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    mu = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dP = torch.empty_like(P)
+    dtc = plx.PLX_BF16 if q.dtype == torch.bfloat16 else plx.PLX_FP32
+    fws = torch.empty(max(256, plx.parallax_fwd_workspace_bytes(B, H, T, d, dtc)), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(256, plx.parallax_bwd_workspace_bytes(B, H, T, d, dtc)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plx.parallax_set_path(plx.PLX_PATH_AUTO)
+    path = "tc" if _tc_ws(plx, B, H, T, d, dtc) > 0 else "simt"
+
+    def step():
+        plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
+        plx.parallax_bwd(q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, detail = plx.parallax_last_device_error(stream)
+    if code != plx.PLX_OK:
+        raise RuntimeError(f"device watchdog: {plx.parallax_strerror(code)} detail={detail:#x}")
+
+    clocks = ClockSampler(gpu_query_id(torch, dev))
+    clocks.start()
+    time.sleep(0.3)
+    plx.parallax_timing_reset()
+    plx.parallax_timing_enable(True)
+    n0 = plx.parallax_launch_count()
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    launches = plx.parallax_launch_count() - n0
+    plx.parallax_timing_enable(False)
+    kt = plx.kernel_times()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    code, detail = plx.parallax_last_device_error(stream)
+    if code != plx.PLX_OK:
+        raise RuntimeError(f"device watchdog: {plx.parallax_strerror(code)} detail={detail:#x}")
+
+    pairs = plx_synth.causal_pairs(B, H, T)
+    flops_step = pairs * (FWD_FLOPS_PER_PAIR_D + BWD_FLOPS_PER_PAIR_D) * d
+    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    peaks = load_peaks()
+
+    # dominant kernel and its live roofline
+    kernels = {}
+    total_k_ms = sum(v_[0] for v_ in kt.values()) or 1.0
+    for name, (tms, cnt) in kt.items():
+        kernels[name] = {"launches": cnt, "avg_ms": tms / cnt, "share": tms / total_k_ms}
+    dom = max(kt, key=lambda n: kt[n][0]) if kt else None
+    roofline = None
+    if dom is not None:
+        avg_s = kt[dom][0] / kt[dom][1] / 1e3
+        fpp = KERNEL_FLOPS_PER_PAIR_D.get(dom)
+        if fpp is not None:
+            achieved = pairs * fpp * d / avg_s / 1e12
+            if dom.startswith("tc_"):
+                peak, bound = peaks["bf16_tflops_sustained"], "tensor"
+                peak_note = f"bf16 dense, {peaks['source']} sustained"
+            else:
+                peak, bound = fp32_simt_peak_tflops(peaks["sm_max_mhz"]), "alu"
+                peak_note = "fp32 FFMA: 148 SMs x 128 lanes x 2 x max SM clock"
+            roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "traffic": None, "peak_source": peak_note,
+                        "flops_per_launch": pairs * fpp * d}
+    # whole-step fraction of the tensor peak
+    pct_peak = value / world / peaks["bf16_tflops_sustained"]
+
+    # forward / backward split (timed separately, same inputs)
+    fwd_ms, bwd_ms = split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream,
+                                   max(3, args.steps // 2))
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, path),
+        "pct_of_bf16_peak": pct_peak,
+        "tokens_per_s": world * B * T * args.steps / (ms / 1e3),
+        "fwd": {"ms": fwd_ms, "tflops": pairs * FWD_FLOPS_PER_PAIR_D * d / (fwd_ms / 1e3) / 1e12},
+        "bwd": {"ms": bwd_ms, "tflops": pairs * BWD_FLOPS_PER_PAIR_D * d / (bwd_ms / 1e3) / 1e12},
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "roofline": roofline,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        nheads = min(H, threads)
+        rows = calibrate_rows(inp, nheads, threads, 15.0, T)
+        dt, sp = oracle_sample(inp, nheads, rows, threads)
+        line["cpu_baseline"] = {"value": sp * (FWD_FLOPS_PER_PAIR_D + BWD_FLOPS_PER_PAIR_D) * d / dt / 1e12,
+                                "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{nheads} heads x first {rows} queries/keys, fwd+bwd, fp64"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _tc_ws(plx, B, H, T, d, dtc):
+    prev = plx.parallax_set_path(plx.PLX_PATH_TC)
+    try:
+        return plx.parallax_fwd_workspace_bytes(B, H, T, d, dtc) or -1
+    finally:
+        plx.parallax_set_path(prev)
+
+
+def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream, n):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for _ in range(n):
+        plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
+    ev[1].record(stream)
+    for _ in range(n):
+        plx.parallax_bwd(q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+    ev[2].record(stream)
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[1]) / n, ev[1].elapsed_time(ev[2]) / n
+
+
+def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
+    """Same step through the public API from pinned host buffers: H2D of the
+    inputs, parallax_fwd + parallax_bwd (library-managed workspace), D2H of the
+    outputs and gradients, all inside the timed region."""
+    dq_ = {k: torch.empty_like(t, device=dev) for k, t in h_in.items()}
+    h_out = {n: torch.empty(s, dtype=dt).pin_memory() for n, s, dt in (
+        ("out", (B, H, T, d), h_in["q"].dtype), ("dq", (B, H, T, d), h_in["q"].dtype),
+        ("dk", (B, H, T, d), h_in["q"].dtype), ("dv", (B, H, T, d), h_in["q"].dtype),
+        ("dP", (H, d, d), torch.float32))}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def step():
+        for name, t in h_in.items():
+            dq_[name].copy_(t, non_blocking=True)
+        o, l_, m_ = plx.parallax_fwd(dq_["q"], dq_["k"], dq_["v"], dq_["P"], stream=stream)
+        g = plx.parallax_bwd(dq_["q"], dq_["k"], dq_["v"], dq_["P"], o, l_, m_, dq_["dout"], stream=stream)
+        h_out["out"].copy_(o, non_blocking=True)
+        for name, t in zip(("dq", "dk", "dv", "dP"), g):
+            h_out[name].copy_(t, non_blocking=True)
+
+    n = max(3, args.steps // 2)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return {"value": world * flops_step * n / (ms / 1e3) / 1e12, "unit": UNIT, "steps": n,
+            "ms_per_step": ms / n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c4", choices=["c4"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
+    world, rank, _ = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank)
+
+
+if __name__ == "__main__":
+    main()

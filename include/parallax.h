@@ -1,0 +1,146 @@
+/*
+ * parallax.h -- C ABI of libparallax.so, the B300 (sm_103a) implementation of
+ * the Parallax attention layer (parameterized Local Linear Attention).
+ *
+ * Operation.  "Parallax: Parameterized Local Linear Attention for Language
+ * Modeling" (gist.science technical summary, "Core mechanism") defines the
+ * layer output as softmax attention plus a correction: the softmax-weighted
+ * KV covariance applied to a per-query probe, with the boundary-amplification
+ * factor set to zero.  This library computes, per batch b and head h, over
+ * causal keys i <= t, with c = 1/sqrt(d):
+ *
+ *     s_ti = c q_t.k_i,   lse_t = log sum_i exp(s_ti),   p_ti = exp(s_ti - lse_t)
+ *     mu_k = sum_i p_ti k_i,   u_t = P_h (q_t - mu_k),   g_ti = k_i.u_t,
+ *     gbar_t = sum_i p_ti g_ti,
+ *     o_t = sum_i p_ti (1 + g_ti - gbar_t) v_i
+ *         = o^SA_t + Sigma_KV u_t,   Sigma_KV = sum_i p_ti (v_i - mu_v)(k_i - mu_k)^T
+ *
+ * A zero projector P gives softmax attention exactly (same page,
+ * "Significance and claims").
+ *
+ * Conventions shared by every entry point.
+ *  - Pointers marked "device" must point to device memory of the current CUDA
+ *    device; the caller allocates and owns every buffer.  The library keeps no
+ *    per-call state (it caches one 16-byte status word per device).
+ *  - q, k, v, out, dout, dq, dk, dv: contiguous row-major [B][H][T][d] in
+ *    `dtype` (PLX_FP32: float, PLX_BF16: bfloat16 bit pattern).  Base pointers
+ *    must be 16-byte aligned.
+ *  - P, dP: [H][d][d] float32, row-major, u = P . delta  (u[a] = sum_b P[a][b] delta[b]).
+ *  - lse: [B][H][T] float32, natural log, scale c included.
+ *  - mu_k: [B][H][T][d] float32.
+ *  - stream: a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on it; the return code covers argument checks and launch
+ *    errors only.  A device-side watchdog (bounded waits inside kernels) is
+ *    read back by parallax_last_device_error().
+ *  - Supported: d in {64, 128}; T >= 1; B, H >= 1; B*H*T*d < 2^31.
+ *  - The library never aborts, never prints and never throws across the ABI.
+ */
+#ifndef PARALLAX_H
+#define PARALLAX_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define PLX_API __attribute__((visibility("default")))
+#else
+#define PLX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    PLX_OK = 0,
+    PLX_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, misaligned base, size overflow */
+    PLX_ERR_UNSUPPORTED = 2, /* d not in {64,128}, unknown dtype, device not sm_103 */
+    PLX_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    PLX_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up (see parallax_last_device_error) */
+};
+
+/* Element types of q, k, v, out, dout, dq, dk, dv. */
+enum { PLX_FP32 = 0, PLX_BF16 = 1 };
+
+/* Kernel families (parallax_set_path). */
+enum {
+    PLX_PATH_AUTO = 0,  /* bf16 -> tensor-core (tcgen05) kernels where built, fp32 -> SIMT */
+    PLX_PATH_SIMT = 1,  /* fp32 FFMA kernels for every dtype (bf16 inputs widened on load) */
+    PLX_PATH_TC = 2     /* tensor-core kernels; PLX_ERR_UNSUPPORTED for fp32 */
+};
+
+/*
+ * Forward.  Writes out [B,H,T,d] (dtype), lse [B,H,T] and mu_k [B,H,T,d]
+ * (float32).  Internally allocates its workspace (the probe u and gbar,
+ * parallax_fwd_workspace_bytes() bytes) stream-ordered with cudaMallocAsync and
+ * frees it before returning; use parallax_fwd_ws() to supply it instead.
+ * Inputs q, k, v (device, dtype), P (device, float32) are read only.
+ * Returns PLX_OK or an error code; on error nothing has been launched.
+ */
+PLX_API int parallax_fwd(const void* q, const void* k, const void* v, const float* P,
+                 void* out, float* lse, float* mu_k,
+                 int B, int H, int T, int d, int dtype, void* stream);
+
+/* Bytes of device workspace the forward needs for these sizes (0 on bad args). */
+PLX_API size_t parallax_fwd_workspace_bytes(int B, int H, int T, int d, int dtype);
+
+/* Forward with a caller-supplied device workspace of at least
+ * parallax_fwd_workspace_bytes() bytes, 256-byte aligned.  No allocation. */
+PLX_API int parallax_fwd_ws(const void* q, const void* k, const void* v, const float* P,
+                    void* out, float* lse, float* mu_k, void* workspace,
+                    int B, int H, int T, int d, int dtype, void* stream);
+
+/* Bytes of device workspace parallax_bwd needs for these sizes (0 on bad args). */
+PLX_API size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtype);
+
+/*
+ * Backward of sum(dout * out) with respect to q, k, v and P.
+ * Reads q, k, v, P, out, lse, mu_k (as written by parallax_fwd on the same
+ * inputs) and dout.  Writes dq, dk, dv ([B,H,T,d], dtype) and dP ([H,d,d]
+ * float32, overwritten, not accumulated; the reduction over b and t runs in a
+ * fixed order, so dP is bitwise reproducible).
+ * workspace: device, >= parallax_bwd_workspace_bytes(), 256-byte aligned, or
+ * NULL to have the library allocate it stream-ordered (cudaMallocAsync) and
+ * free it before returning.
+ */
+PLX_API int parallax_bwd(const void* q, const void* k, const void* v, const float* P,
+                 const void* out, const float* lse, const float* mu_k, const void* dout,
+                 void* dq, void* dk, void* dv, float* dP, void* workspace,
+                 int B, int H, int T, int d, int dtype, void* stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's watchdog
+ * word.  Returns PLX_OK, PLX_ERR_TIMEOUT (a bounded wait inside a kernel gave
+ * up; the kernel skipped its remaining work and released its resources) or
+ * PLX_ERR_CUDA (the synchronize itself failed).  If `detail` is not NULL it
+ * receives the raw word (kernel id << 16 | wait site) of the first timeout.
+ */
+PLX_API int parallax_last_device_error(void* stream, unsigned* detail);
+
+/* Selects the kernel family for later calls in this process; returns the
+ * previous setting, or -1 if `path` is not a PLX_PATH_* value. */
+PLX_API int parallax_set_path(int path);
+
+/*
+ * Launch accounting and per-kernel device timing (tracing).
+ * Every kernel launch the library makes is counted.  While timing is enabled,
+ * a CUDA event is recorded on the launching stream before and after each
+ * launch; parallax_timing_collect() waits for the recorded events and folds
+ * their elapsed times into per-kernel totals, which parallax_timing_get()
+ * returns by index (name is a static string owned by the library).  Timing
+ * assumes one device per process.  Not thread-safe against concurrent calls.
+ */
+PLX_API unsigned long long parallax_launch_count(void);
+PLX_API int parallax_timing_enable(int on);          /* returns the previous setting */
+PLX_API int parallax_timing_collect(void);           /* number of kernel names, or -PLX_ERR_CUDA */
+PLX_API int parallax_timing_get(int i, const char** name, double* total_ms, long long* launches);
+PLX_API void parallax_timing_reset(void);
+
+/* Static description of a status code (never NULL). */
+PLX_API const char* parallax_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PARALLAX_H */

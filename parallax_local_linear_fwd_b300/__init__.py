@@ -1,0 +1,224 @@
+"""Python binding of libparallax.so (Parallax attention on B300, sm_103a).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  The C entry points and
+their contracts are declared in ``include/parallax.h``; the functions here have
+the same names and take torch tensors instead of raw pointers.
+
+If the shared library has not been built, importing succeeds but every call
+raises ``PlxLibraryMissing``; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "PLX_OK", "PLX_ERR_INVALID_ARG", "PLX_ERR_UNSUPPORTED", "PLX_ERR_CUDA", "PLX_ERR_TIMEOUT",
+    "PLX_FP32", "PLX_BF16", "PLX_PATH_AUTO", "PLX_PATH_SIMT", "PLX_PATH_TC",
+    "PlxError", "PlxLibraryMissing", "lib", "lib_path", "exported_symbols",
+    "parallax_fwd", "parallax_fwd_ws", "parallax_bwd", "parallax_fwd_workspace_bytes",
+    "parallax_bwd_workspace_bytes", "parallax_last_device_error", "parallax_set_path",
+    "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
+    "parallax_timing_get", "parallax_timing_reset", "kernel_times",
+]
+
+PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
+PLX_FP32, PLX_BF16 = 0, 1
+PLX_PATH_AUTO, PLX_PATH_SIMT, PLX_PATH_TC = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libparallax.so")
+_lib = None
+
+# Every symbol include/parallax.h declares, with its ctypes signature.
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "parallax_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "parallax_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "parallax_bwd": (_i, [_vp] * 13 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_last_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
+    "parallax_set_path": (_i, [_i]),
+    "parallax_strerror": (ctypes.c_char_p, [_i]),
+    "parallax_launch_count": (ctypes.c_ulonglong, []),
+    "parallax_timing_enable": (_i, [_i]),
+    "parallax_timing_collect": (_i, []),
+    "parallax_timing_get": (_i, [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_longlong)]),
+    "parallax_timing_reset": (None, []),
+}
+
+
+class PlxError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {parallax_strerror(code)} (code {code})")
+
+
+class PlxLibraryMissing(ImportError):
+    pass
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGNATURES)
+
+
+def lib():
+    """Load libparallax.so (once).  Raises PlxLibraryMissing if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise PlxLibraryMissing(
+                f"{_LIB_PATH} is not built; run `python -m parallax_local_linear_fwd_b300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PLX_FP32
+    if t.dtype == torch.bfloat16:
+        return PLX_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != PLX_OK:
+        raise PlxError(code, where)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def parallax_fwd(q, k, v, P, out=None, lse=None, mu_k=None, stream=None):
+    """Forward; returns (out, lse, mu_k).  q, k, v: [B,H,T,d] fp32/bf16 (CUDA)."""
+    B, H, T, d = _shape(q)
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if mu_k is None:
+        mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
+    _check(lib().parallax_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                              B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd")
+    return out, lse, mu_k
+
+
+def parallax_fwd_ws(q, k, v, P, out, lse, mu_k, workspace, stream=None):
+    B, H, T, d = _shape(q)
+    _check(lib().parallax_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                                 _ptr(workspace), B, H, T, d, _dtype_code(q), _stream_ptr(stream)),
+           "parallax_fwd_ws")
+    return out, lse, mu_k
+
+
+def parallax_fwd_workspace_bytes(B, H, T, d, dtype) -> int:
+    return int(lib().parallax_fwd_workspace_bytes(B, H, T, d, dtype))
+
+
+def parallax_bwd_workspace_bytes(B, H, T, d, dtype) -> int:
+    return int(lib().parallax_bwd_workspace_bytes(B, H, T, d, dtype))
+
+
+def parallax_bwd(q, k, v, P, out, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None,
+                 workspace=None, stream=None):
+    """Backward of sum(dout * out); returns (dq, dk, dv, dP)."""
+    B, H, T, d = _shape(q)
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dP = torch.empty_like(P) if dP is None else dP
+    _check(lib().parallax_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
+                              B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
+    return dq, dk, dv, dP
+
+
+def parallax_last_device_error(stream=None):
+    """Synchronize `stream` and return (code, detail) of the device watchdog."""
+    detail = ctypes.c_uint(0)
+    code = lib().parallax_last_device_error(_stream_ptr(stream), ctypes.byref(detail))
+    return int(code), int(detail.value)
+
+
+def parallax_set_path(path: int) -> int:
+    return int(lib().parallax_set_path(path))
+
+
+def parallax_strerror(code: int) -> str:
+    try:
+        return lib().parallax_strerror(code).decode()
+    except PlxLibraryMissing:
+        return f"status {code}"
+
+
+def parallax_launch_count() -> int:
+    """Total kernel launches the library has made in this process."""
+    return int(lib().parallax_launch_count())
+
+
+def parallax_timing_enable(on: bool) -> bool:
+    return bool(lib().parallax_timing_enable(1 if on else 0))
+
+
+def parallax_timing_collect() -> int:
+    n = int(lib().parallax_timing_collect())
+    if n < 0:
+        raise PlxError(-n, "parallax_timing_collect")
+    return n
+
+
+def parallax_timing_get(i: int):
+    name = ctypes.c_char_p()
+    ms = ctypes.c_double()
+    cnt = ctypes.c_longlong()
+    _check(lib().parallax_timing_get(i, ctypes.byref(name), ctypes.byref(ms), ctypes.byref(cnt)),
+           "parallax_timing_get")
+    return name.value.decode(), float(ms.value), int(cnt.value)
+
+
+def parallax_timing_reset() -> None:
+    lib().parallax_timing_reset()
+
+
+def kernel_times() -> dict:
+    """{kernel name: (total ms, launches)} of the timed launches so far."""
+    n = parallax_timing_collect()
+    out = {}
+    for i in range(n):
+        name, ms, cnt = parallax_timing_get(i)
+        if cnt:
+            out[name] = (ms, cnt)
+    return out

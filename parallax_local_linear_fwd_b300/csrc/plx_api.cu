@@ -1,0 +1,294 @@
+// C ABI of libparallax.so: argument checks, workspace handling, kernel-family
+// dispatch and the device watchdog word.  Declarations and contracts are in
+// include/parallax.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "parallax.h"
+#include "plx_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status[kMaxDevices] = {};  // per-device watchdog word (4 x u32)
+int g_arch_ok[kMaxDevices] = {};        // 0 unknown, 1 sm_103, -1 other
+std::atomic<int> g_path{PLX_PATH_AUTO};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Returns PLX_OK and the current device's status word, creating it once.
+int device_state(unsigned** status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PLX_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PLX_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return PLX_ERR_CUDA;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1) return PLX_ERR_UNSUPPORTED;
+    if (!g_status[dev]) {
+        unsigned* p = nullptr;
+        if (cudaMalloc(&p, 4 * sizeof(unsigned)) != cudaSuccess) return PLX_ERR_CUDA;
+        if (cudaMemset(p, 0, 4 * sizeof(unsigned)) != cudaSuccess) {
+            cudaFree(p);
+            return PLX_ERR_CUDA;
+        }
+        g_status[dev] = p;
+    }
+    *status = g_status[dev];
+    return PLX_OK;
+}
+
+int check_sizes(int B, int H, int T, int d, int dtype) {
+    if (B < 1 || H < 1 || T < 1 || d < 1) return PLX_ERR_INVALID_ARG;
+    if (dtype != PLX_FP32 && dtype != PLX_BF16) return PLX_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return PLX_ERR_UNSUPPORTED;
+    const unsigned long long n = (unsigned long long)B * H * T * d;
+    if (n >= (1ull << 31)) return PLX_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return PLX_ERR_UNSUPPORTED;
+    return PLX_OK;
+}
+
+// Which family serves this call: 1 = SIMT, 2 = tensor core, <0 = error code.
+int pick_family(int dtype) {
+    const int path = g_path.load();
+    if (path == PLX_PATH_SIMT) return 1;
+    if (path == PLX_PATH_TC) return dtype == PLX_BF16 && plx::tc_available() ? 2 : -PLX_ERR_UNSUPPORTED;
+    return (dtype == PLX_BF16 && plx::tc_available()) ? 2 : 1;
+}
+
+size_t fwd_ws_for(int fam, int B, int H, int T, int d) {
+    return fam == 2 ? plx::tc_fwd_ws_bytes(B, H, T, d) : plx::simt_fwd_ws_bytes(B, H, T, d);
+}
+size_t bwd_ws_for(int fam, int B, int H, int T, int d) {
+    return fam == 2 ? plx::tc_bwd_ws_bytes(B, H, T, d) : plx::simt_bwd_ws_bytes(B, H, T, d);
+}
+
+int fwd_common(const void* q, const void* k, const void* v, const float* P, void* out, float* lse,
+               float* mu_k, void* ws, bool own_ws, int B, int H, int T, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, T, d, dtype);
+    if (rc) return rc;
+    if (!q || !k || !v || !P || !out || !lse || !mu_k) return PLX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(P) || !aligned16(out) ||
+        !aligned16(lse) || !aligned16(mu_k))
+        return PLX_ERR_INVALID_ARG;
+    if (!own_ws && (!ws || ((uintptr_t)ws & 255u))) return PLX_ERR_INVALID_ARG;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return -fam;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = fwd_ws_for(fam, B, H, T, d);
+    if (own_ws && cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return PLX_ERR_CUDA;
+    plx::FwdArgs a{q, k, v, P, out, lse, mu_k, ws, B, H, T, d, dtype, s, status};
+    cudaError_t e = fam == 2 ? plx::tc_fwd(a) : plx::simt_fwd(a);
+    if (own_ws) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
+// ------------------------------------------------------------- timing
+struct Pending {
+    int kid;
+    cudaEvent_t a, b;
+};
+std::mutex g_tmu;
+std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_timing{0};
+std::vector<const char*> g_names;
+std::vector<double> g_total_ms;
+std::vector<long long> g_count;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+thread_local int t_kid = -1;
+thread_local cudaEvent_t t_ev = nullptr;
+
+int kernel_id(const char* name) {
+    for (size_t i = 0; i < g_names.size(); i++)
+        if (g_names[i] == name || std::strcmp(g_names[i], name) == 0) return (int)i;
+    g_names.push_back(name);
+    g_total_ms.push_back(0.0);
+    g_count.push_back(0);
+    return (int)g_names.size() - 1;
+}
+
+cudaEvent_t get_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+}  // namespace
+
+namespace plx {
+void timing_begin(cudaStream_t s, const char* name) {
+    g_launches.fetch_add(1);
+    t_kid = -1;
+    if (!g_timing.load()) return;
+    std::lock_guard<std::mutex> lock(g_tmu);
+    cudaEvent_t e = get_event();
+    if (!e || cudaEventRecord(e, s) != cudaSuccess) {
+        if (e) g_event_pool.push_back(e);
+        return;
+    }
+    t_kid = kernel_id(name);
+    t_ev = e;
+}
+void timing_end(cudaStream_t s) {
+    if (t_kid < 0) return;
+    std::lock_guard<std::mutex> lock(g_tmu);
+    cudaEvent_t e = get_event();
+    if (!e || cudaEventRecord(e, s) != cudaSuccess) {
+        if (e) g_event_pool.push_back(e);
+        g_event_pool.push_back(t_ev);
+    } else {
+        g_pending.push_back({t_kid, t_ev, e});
+    }
+    t_kid = -1;
+}
+}  // namespace plx
+
+extern "C" {
+
+unsigned long long parallax_launch_count(void) { return g_launches.load(); }
+
+int parallax_timing_enable(int on) { return g_timing.exchange(on ? 1 : 0); }
+
+int parallax_timing_collect(void) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    int rc = 0;
+    for (const Pending& p : g_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
+            rc = -PLX_ERR_CUDA;
+        else {
+            g_total_ms[p.kid] += ms;
+            g_count[p.kid] += 1;
+        }
+        g_event_pool.push_back(p.a);
+        g_event_pool.push_back(p.b);
+    }
+    g_pending.clear();
+    return rc ? rc : (int)g_names.size();
+}
+
+int parallax_timing_get(int i, const char** name, double* total_ms, long long* launches) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    if (i < 0 || (size_t)i >= g_names.size()) return PLX_ERR_INVALID_ARG;
+    if (name) *name = g_names[i];
+    if (total_ms) *total_ms = g_total_ms[i];
+    if (launches) *launches = g_count[i];
+    return PLX_OK;
+}
+
+void parallax_timing_reset(void) {
+    std::lock_guard<std::mutex> lock(g_tmu);
+    for (size_t i = 0; i < g_names.size(); i++) {
+        g_total_ms[i] = 0.0;
+        g_count[i] = 0;
+    }
+}
+
+
+int parallax_fwd(const void* q, const void* k, const void* v, const float* P, void* out, float* lse,
+                 float* mu_k, int B, int H, int T, int d, int dtype, void* stream) {
+    return fwd_common(q, k, v, P, out, lse, mu_k, nullptr, true, B, H, T, d, dtype, stream);
+}
+
+int parallax_fwd_ws(const void* q, const void* k, const void* v, const float* P, void* out, float* lse,
+                    float* mu_k, void* workspace, int B, int H, int T, int d, int dtype, void* stream) {
+    return fwd_common(q, k, v, P, out, lse, mu_k, workspace, false, B, H, T, d, dtype, stream);
+}
+
+size_t parallax_fwd_workspace_bytes(int B, int H, int T, int d, int dtype) {
+    if (check_sizes(B, H, T, d, dtype)) return 0;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return 0;
+    return fwd_ws_for(fam, B, H, T, d);
+}
+
+size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtype) {
+    if (check_sizes(B, H, T, d, dtype)) return 0;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return 0;
+    return bwd_ws_for(fam, B, H, T, d);
+}
+
+int parallax_bwd(const void* q, const void* k, const void* v, const float* P, const void* out, const float* lse,
+                 const float* mu_k, const void* dout, void* dq, void* dk, void* dv, float* dP, void* workspace,
+                 int B, int H, int T, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, T, d, dtype);
+    if (rc) return rc;
+    if (!q || !k || !v || !P || !out || !lse || !mu_k || !dout || !dq || !dk || !dv || !dP)
+        return PLX_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, P, out, lse, mu_k, dout, dq, dk, dv, dP};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
+    if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return -fam;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool own = workspace == nullptr;
+    void* ws = workspace;
+    if (own && cudaMallocAsync(&ws, bwd_ws_for(fam, B, H, T, d), s) != cudaSuccess) return PLX_ERR_CUDA;
+    plx::BwdArgs a{q, k, v, P, out, lse, mu_k, dout, dq, dk, dv, dP, ws, B, H, T, d, dtype, s, status};
+    cudaError_t e = fam == 2 ? plx::tc_bwd(a) : plx::simt_bwd(a);
+    if (own) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
+int parallax_last_device_error(void* stream, unsigned* detail) {
+    if (detail) *detail = 0;
+    unsigned* status = nullptr;
+    int rc = device_state(&status);
+    if (rc) return rc;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return PLX_ERR_CUDA;
+    unsigned word[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return PLX_ERR_CUDA;
+    if (word[0] == 0) return PLX_OK;
+    if (detail) *detail = word[1];
+    if (cudaMemset(status, 0, sizeof(word)) != cudaSuccess) return PLX_ERR_CUDA;
+    return PLX_ERR_TIMEOUT;
+}
+
+int parallax_set_path(int path) {
+    if (path != PLX_PATH_AUTO && path != PLX_PATH_SIMT && path != PLX_PATH_TC) return -1;
+    return g_path.exchange(path);
+}
+
+const char* parallax_strerror(int code) {
+    switch (code) {
+        case PLX_OK: return "success";
+        case PLX_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size)";
+        case PLX_ERR_UNSUPPORTED: return "unsupported configuration (head dim, dtype, path or device)";
+        case PLX_ERR_CUDA: return "CUDA runtime error";
+        case PLX_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status code";
+    }
+}
+
+}  // extern "C"

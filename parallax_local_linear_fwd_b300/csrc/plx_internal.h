@@ -1,0 +1,73 @@
+// Internal interface between the C ABI layer (plx_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace plx {
+
+// Kernel identifiers used in the watchdog word (id << 16 | wait site).
+enum KernelId : unsigned {
+    KID_TC_PASS1 = 1,
+    KID_TC_PASS2 = 2,
+    KID_TC_BWD_B1 = 3,
+    KID_TC_BWD_B3 = 4,
+    KID_TC_PROJ = 5,
+};
+
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* P;
+    void* out;
+    float* lse;
+    float* mu_k;
+    void* ws;  // workspace, 256-byte aligned, fwd_ws_bytes() long
+    int B, H, T, d, dtype;
+    cudaStream_t stream;
+    unsigned* status;  // device watchdog word
+};
+
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* P;
+    const void* out;
+    const float* lse;
+    const float* mu_k;
+    const void* dout;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dP;
+    void* ws;
+    int B, H, T, d, dtype;
+    cudaStream_t stream;
+    unsigned* status;
+};
+
+// Launch accounting / timing hooks (plx_api.cu).  Bracket every launch:
+//   timing_begin(stream, "name"); kernel<<<...>>>(...); timing_end(stream);
+void timing_begin(cudaStream_t s, const char* name);
+void timing_end(cudaStream_t s);
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// SIMT (FFMA) family: any dtype, d in {64,128}.
+size_t simt_fwd_ws_bytes(int B, int H, int T, int d);
+size_t simt_bwd_ws_bytes(int B, int H, int T, int d);
+cudaError_t simt_fwd(const FwdArgs& a);
+cudaError_t simt_bwd(const BwdArgs& a);
+
+// Tensor-core (tcgen05) family: bf16, d in {64,128}.
+bool tc_available();
+size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
+size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
+cudaError_t tc_fwd(const FwdArgs& a);
+cudaError_t tc_bwd(const BwdArgs& a);
+
+}  // namespace plx

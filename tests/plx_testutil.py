@@ -1,0 +1,52 @@
+"""Shared helpers for the parity tests (no layer arithmetic here)."""
+import numpy as np
+import torch
+
+import plx_synth
+
+# Tolerances: max |gpu - oracle| / RMS(oracle), per output tensor.
+TOL_FP32 = 1e-4
+TOL_BF16 = 2e-2
+TOL_BF16_GRAD = 3e-2
+
+
+def rel_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    if rms == 0.0:
+        return float(np.abs(got - ref).max())
+    return float(np.abs(got - ref).max() / rms)
+
+
+def to_device(x: np.ndarray, device="cuda") -> torch.Tensor:
+    if x.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def to_host64(t: torch.Tensor) -> np.ndarray:
+    t = t.detach()
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+def inputs_f64(inp: dict):
+    """Exact float64 views of the stored inputs (bf16 widened exactly)."""
+    out = {k: plx_synth.widen(inp[k]) for k in ("q", "k", "v") if k in inp}
+    out["P"] = inp["P"].astype(np.float64)
+    if "dout" in inp:
+        out["dout"] = plx_synth.widen(inp["dout"])
+    return out
+
+
+def sample_rows(B, H, T, n, seed=0):
+    """Sampled (b, h, t) rows: always the first and last query plus tile edges."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for t in (0, 1, T - 1, min(T - 1, 127), min(T - 1, 128), T // 2):
+        rows.add((int(rng.integers(B)), int(rng.integers(H)), t))
+    while len(rows) < n:
+        rows.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(T))))
+    return sorted(rows)

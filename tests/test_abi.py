@@ -1,0 +1,72 @@
+"""CPU-only checks of the C ABI: the library builds, loads, and exports every
+symbol include/parallax.h declares; host-side argument checks return the
+documented codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import parallax_local_linear_fwd_b300 as plx
+from parallax_local_linear_fwd_b300 import build as plx_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(parallax_\w+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def L():
+    plx_build.build()
+    return plx.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared_symbols()
+    assert "parallax_fwd" in declared and "parallax_bwd" in declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(declared) == sorted(plx.exported_symbols())
+
+
+def test_hidden_internals(L):
+    # only the C ABI is exported; kernel-side C++ symbols stay hidden
+    with pytest.raises(AttributeError):
+        getattr(L, "_ZN3plx8simt_fwdERKNS_7FwdArgsE")
+
+
+def test_strerror_and_path(L):
+    for code in range(5):
+        assert plx.parallax_strerror(code)
+    assert "unknown" in plx.parallax_strerror(99)
+    prev = plx.parallax_set_path(plx.PLX_PATH_SIMT)
+    assert plx.parallax_set_path(prev) == plx.PLX_PATH_SIMT
+    assert plx.parallax_set_path(7) == -1
+
+
+def test_host_argument_checks_need_no_gpu(L):
+    p = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
+    assert L.parallax_fwd(p, p, p, p, p, p, p, 1, 1, 16, 96, 1, None) == plx.PLX_ERR_UNSUPPORTED
+    assert L.parallax_fwd(p, p, p, p, p, p, p, 1, 1, 16, 64, 5, None) == plx.PLX_ERR_UNSUPPORTED
+    assert L.parallax_fwd(p, p, p, p, p, p, p, 0, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    assert L.parallax_fwd(p, p, p, p, p, p, p, 1, 1, 0, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    assert L.parallax_fwd(None, p, p, p, p, p, p, 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    q = ctypes.c_void_p(258)  # misaligned
+    assert L.parallax_fwd(q, p, p, p, p, p, p, 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    assert L.parallax_fwd_ws(p, p, p, p, p, p, p, ctypes.c_void_p(16), 1, 1, 16, 64, 1, None) \
+        == plx.PLX_ERR_INVALID_ARG
+    args13 = [p] * 12
+    assert L.parallax_bwd(*args13, None, 1, 1, 16, 48, 1, None) == plx.PLX_ERR_UNSUPPORTED
+    assert L.parallax_bwd(*args13, ctypes.c_void_p(272), 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    assert L.parallax_fwd_workspace_bytes(1, 1, 16, 80, 1) == 0
+    assert L.parallax_bwd_workspace_bytes(-1, 1, 16, 64, 1) == 0
+    # 2^31 elements overflow the supported index range
+    assert L.parallax_fwd(p, p, p, p, p, p, p, 1 << 10, 1 << 10, 1 << 10, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
