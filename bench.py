@@ -302,7 +302,7 @@ def run_ours(args, world, rank):
 
     def step():
         plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
-        plx.parallax_bwd(q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+        plx.parallax_bwd(q, k, v, P, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -416,7 +416,7 @@ def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws,
         plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
     ev[1].record(stream)
     for _ in range(n):
-        plx.parallax_bwd(q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+        plx.parallax_bwd(q, k, v, P, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
     ev[2].record(stream)
     torch.cuda.synchronize()
     return ev[0].elapsed_time(ev[1]) / n, ev[1].elapsed_time(ev[2]) / n
@@ -438,7 +438,7 @@ def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
         for name, t in h_in.items():
             dq_[name].copy_(t, non_blocking=True)
         o, l_, m_ = plx.parallax_fwd(dq_["q"], dq_["k"], dq_["v"], dq_["P"], stream=stream)
-        g = plx.parallax_bwd(dq_["q"], dq_["k"], dq_["v"], dq_["P"], o, l_, m_, dq_["dout"], stream=stream)
+        g = plx.parallax_bwd(dq_["q"], dq_["k"], dq_["v"], dq_["P"], l_, m_, dq_["dout"], stream=stream)
         h_out["out"].copy_(o, non_blocking=True)
         for name, t in zip(("dq", "dk", "dv", "dP"), g):
             h_out[name].copy_(t, non_blocking=True)

@@ -95,8 +95,10 @@ PLX_API size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtyp
 
 /*
  * Backward of sum(dout * out) with respect to q, k, v and P.
- * Reads q, k, v, P, out, lse, mu_k (as written by parallax_fwd on the same
- * inputs) and dout.  Writes dq, dk, dv ([B,H,T,d], dtype) and dP ([H,d,d]
+ * Reads q, k, v, P, lse, mu_k (as written by parallax_fwd on the same inputs)
+ * and dout.  The forward output itself is not needed: the row term
+ * dout . out is rebuilt from the backward's own fp32 sums, so the rounding of
+ * a bf16-stored out does not leak into the gradients.  Writes dq, dk, dv ([B,H,T,d], dtype) and dP ([H,d,d]
  * float32, overwritten, not accumulated; the reduction over b and t runs in a
  * fixed order, so dP is bitwise reproducible).
  * workspace: device, >= parallax_bwd_workspace_bytes(), 256-byte aligned, or
@@ -104,7 +106,7 @@ PLX_API size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtyp
  * free it before returning.
  */
 PLX_API int parallax_bwd(const void* q, const void* k, const void* v, const float* P,
-                 const void* out, const float* lse, const float* mu_k, const void* dout,
+                 const float* lse, const float* mu_k, const void* dout,
                  void* dq, void* dk, void* dv, float* dP, void* workspace,
                  int B, int H, int T, int d, int dtype, void* stream);
 

@@ -40,7 +40,7 @@ _SIGNATURES = {
     "parallax_fwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
-    "parallax_bwd": (_i, [_vp] * 13 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_bwd": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_last_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "parallax_set_path": (_i, [_i]),
     "parallax_strerror": (ctypes.c_char_p, [_i]),
@@ -151,7 +151,7 @@ def parallax_bwd_workspace_bytes(B, H, T, d, dtype) -> int:
     return int(lib().parallax_bwd_workspace_bytes(B, H, T, d, dtype))
 
 
-def parallax_bwd(q, k, v, P, out, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None,
+def parallax_bwd(q, k, v, P, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None,
                  workspace=None, stream=None):
     """Backward of sum(dout * out); returns (dq, dk, dv, dP)."""
     B, H, T, d = _shape(q)
@@ -160,7 +160,7 @@ def parallax_bwd(q, k, v, P, out, lse, mu_k, dout, dq=None, dk=None, dv=None, dP
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     dP = torch.empty_like(P) if dP is None else dP
-    _check(lib().parallax_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+    _check(lib().parallax_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(lse), _ptr(mu_k),
                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
                               B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
     return dq, dk, dv, dP

@@ -232,14 +232,14 @@ size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtype) {
     return bwd_ws_for(fam, B, H, T, d);
 }
 
-int parallax_bwd(const void* q, const void* k, const void* v, const float* P, const void* out, const float* lse,
+int parallax_bwd(const void* q, const void* k, const void* v, const float* P, const float* lse,
                  const float* mu_k, const void* dout, void* dq, void* dk, void* dv, float* dP, void* workspace,
                  int B, int H, int T, int d, int dtype, void* stream) {
     int rc = check_sizes(B, H, T, d, dtype);
     if (rc) return rc;
-    if (!q || !k || !v || !P || !out || !lse || !mu_k || !dout || !dq || !dk || !dv || !dP)
+    if (!q || !k || !v || !P || !lse || !mu_k || !dout || !dq || !dk || !dv || !dP)
         return PLX_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, P, out, lse, mu_k, dout, dq, dk, dv, dP};
+    const void* ptrs[] = {q, k, v, P, lse, mu_k, dout, dq, dk, dv, dP};
     for (const void* p : ptrs)
         if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
     if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
@@ -252,7 +252,7 @@ int parallax_bwd(const void* q, const void* k, const void* v, const float* P, co
     const bool own = workspace == nullptr;
     void* ws = workspace;
     if (own && cudaMallocAsync(&ws, bwd_ws_for(fam, B, H, T, d), s) != cudaSuccess) return PLX_ERR_CUDA;
-    plx::BwdArgs a{q, k, v, P, out, lse, mu_k, dout, dq, dk, dv, dP, ws, B, H, T, d, dtype, s, status};
+    plx::BwdArgs a{q, k, v, P, lse, mu_k, dout, dq, dk, dv, dP, ws, B, H, T, d, dtype, s, status};
     cudaError_t e = fam == 2 ? plx::tc_bwd(a) : plx::simt_bwd(a);
     if (own) {
         cudaError_t e2 = cudaFreeAsync(ws, s);

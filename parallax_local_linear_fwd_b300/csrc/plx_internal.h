@@ -36,7 +36,6 @@ struct BwdArgs {
     const void* k;
     const void* v;
     const float* P;
-    const void* out;
     const float* lse;
     const float* mu_k;
     const void* dout;

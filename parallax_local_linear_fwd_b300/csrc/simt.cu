@@ -16,7 +16,9 @@
 // Backward (chain rule of the lines above, e_ti = do_t . v_i):
 //   B1 (query tiles): R_t = sum_i p e k_i,  ebar_t = sum_i p e
 //   B2 (rows)       : du = R - ebar mu_k; ddelta = P^T du; dq = ddelta; dmu = -ddelta;
-//                     D = do.o - gbar ebar + mu_k.dmu
+//                     D = do.o - gbar ebar + mu_k.dmu, with do.o = ebar + R.u - gbar ebar
+//                     rebuilt from the fp32 sums (sum_i p e (1 + g - gbar), g = k.u), so
+//                     the stored (possibly bf16) output is never read
 //   dP (rows)       : dP_h = sum_{b,t} du delta^T   (fixed-order two-stage reduction)
 //   B3 (key tiles)  : a = p(1+g-gbar), dg = p(e-ebar), ds = p(e(1+g-gbar) - g ebar + k.dmu - D)
 //                     dv += a do; dk += c ds q + dg u + p dmu; dq += c ds k (fp32 atomics)
@@ -414,11 +416,10 @@ __global__ void __launch_bounds__(NT) simt_bwd_b1(const Tin* __restrict__ q, con
 
 // ---------------------------------------------------------------- bwd B2
 // Per row: delta, u, gbar, du (overwrites R), ddelta = P^T du, dq_acc = ddelta,
-// dmu = -ddelta, D = do.o - gbar ebar + mu_k.dmu.
+// dmu = -ddelta, D = (ebar + R.u - gbar ebar) - gbar ebar + mu_k.dmu.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(NT) simt_bwd_b2(const Tin* __restrict__ q, const float* __restrict__ mu_k,
-                                                  const float* __restrict__ P, const Tin* __restrict__ out,
-                                                  const Tin* __restrict__ dout, float* __restrict__ R,
+                                                  const float* __restrict__ P, float* __restrict__ R,
                                                   const float* __restrict__ ebar, float* __restrict__ U,
                                                   float* __restrict__ dmu, float* __restrict__ dq_acc,
                                                   float* __restrict__ gbar, float* __restrict__ Dv,
@@ -457,17 +458,22 @@ __global__ void __launch_bounds__(NT) simt_bwd_b2(const Tin* __restrict__ q, con
             for (int j = 0; j < NA; j++) u[j] = fmaf(PT[bb * LD + lane + 32 * j], db, u[j]);
         }
         const float eb = ebar[row];
-        float g = 0.f, du[NA];
+        float g = 0.f, ru = 0.f, du[NA];
 #pragma unroll
         for (int j = 0; j < NA; j++) {
             const int a = lane + 32 * j;
+            const float r = R[row * D + a];
             g = fmaf(mk[j], u[j], g);
-            du[j] = R[row * D + a] - eb * mk[j];
+            ru = fmaf(r, u[j], ru);
+            du[j] = r - eb * mk[j];
             U[row * D + a] = u[j];
             R[row * D + a] = du[j];
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            ru += __shfl_xor_sync(0xffffffffu, ru, o);
+        }
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < NA; j++) w[lane + 32 * j] = du[j];
@@ -487,14 +493,13 @@ __global__ void __launch_bounds__(NT) simt_bwd_b2(const Tin* __restrict__ q, con
             const int a = lane + 32 * j;
             dq_acc[row * D + a] = dd[j];
             dmu[row * D + a] = -dd[j];
-            x = fmaf(ldf(dout + row * D + a), ldf(out + row * D + a), x);
             x = fmaf(mk[j], -dd[j], x);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         if (lane == 0) {
             gbar[row] = g;
-            Dv[row] = x - g * eb;
+            Dv[row] = (eb + ru - g * eb) - g * eb + x;
         }
         __syncwarp();
     }
@@ -834,7 +839,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     const dim3 pgrid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
     timing_begin(a.stream, "simt_bwd_b2");
     simt_bwd_b2<Tin, D><<<pgrid, NT, smem_proj<D>(), a.stream>>>(
-        (const Tin*)a.q, a.mu_k, a.P, (const Tin*)a.out, (const Tin*)a.dout, w.R, w.ebar, w.U, w.dmu, w.dq_acc,
+        (const Tin*)a.q, a.mu_k, a.P, w.R, w.ebar, w.U, w.dmu, w.dq_acc,
         w.gbar, w.Dv, a.B, a.H, a.T, PROJ_ROWS);
     timing_end(a.stream);
     PLX_TRY(cudaGetLastError());

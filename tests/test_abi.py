@@ -63,9 +63,9 @@ def test_host_argument_checks_need_no_gpu(L):
     assert L.parallax_fwd(q, p, p, p, p, p, p, 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
     assert L.parallax_fwd_ws(p, p, p, p, p, p, p, ctypes.c_void_p(16), 1, 1, 16, 64, 1, None) \
         == plx.PLX_ERR_INVALID_ARG
-    args13 = [p] * 12
-    assert L.parallax_bwd(*args13, None, 1, 1, 16, 48, 1, None) == plx.PLX_ERR_UNSUPPORTED
-    assert L.parallax_bwd(*args13, ctypes.c_void_p(272), 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+    args = [p] * 11
+    assert L.parallax_bwd(*args, None, 1, 1, 16, 48, 1, None) == plx.PLX_ERR_UNSUPPORTED
+    assert L.parallax_bwd(*args, ctypes.c_void_p(272), 1, 1, 16, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
     assert L.parallax_fwd_workspace_bytes(1, 1, 16, 80, 1) == 0
     assert L.parallax_bwd_workspace_bytes(-1, 1, 16, 64, 1) == 0
     # 2^31 elements overflow the supported index range

@@ -80,7 +80,7 @@ def test_forward_small_full_compare(path, B, H, T, d, dtype):
     ro, rl, rm = oracle.forward(f["q"], f["k"], f["v"], f["P"])
     go, gl, gm = _run_fwd(inp)
     tol = _tol(dtype)
-    assert rel_err(go, ro) < tol
+    assert rel_err(go, ro, dtype) < tol
     assert rel_err(gm, rm) < tol
     assert np.abs(gl - rl).max() < tol * max(1.0, np.sqrt(np.mean(rl * rl)))
 
@@ -96,14 +96,14 @@ def test_pr1_workload_and_zero_projector(path):
         ro, rl, rm = oracle.forward(f["q"], f["k"], f["v"], f["P"])
         go, gl, gm = _run_fwd(inp)
         tol = _tol(dtype)
-        assert rel_err(go, ro) < tol
+        assert rel_err(go, ro, dtype) < tol
         assert rel_err(gm, rm) < tol
         if zero:
             # P = 0 must give softmax attention (library routine, fp64)
             sd = torch.nn.functional.scaled_dot_product_attention(
                 torch.from_numpy(f["q"]), torch.from_numpy(f["k"]), torch.from_numpy(f["v"]),
                 is_causal=True).numpy()
-            assert rel_err(go, sd) < tol
+            assert rel_err(go, sd, dtype) < tol
 
 
 @pytest.mark.parametrize("name", ["c2", "c3", "c5"])
@@ -116,7 +116,7 @@ def test_forward_full_size_sampled_rows(name):
     f = inputs_f64(inp)
     ro, rl, rm = oracle.forward_rows(f["q"], f["k"], f["v"], f["P"], rows)
     idx = tuple(np.array(rows).T)
-    assert rel_err(go[idx], ro) < TOL_BF16
+    assert rel_err(go[idx], ro, "bf16") < TOL_BF16
     assert rel_err(gm[idx], rm) < TOL_BF16
     assert np.abs(gl[idx] - rl).max() < TOL_BF16 * max(1.0, np.sqrt(np.mean(rl * rl)))
     # properties at every row: finite outputs, lse >= the diagonal score
@@ -126,7 +126,7 @@ def test_forward_full_size_sampled_rows(name):
 def _run_bwd(inp, out_dev=None):
     q, k, v, P, do = (to_device(inp[x]) for x in ("q", "k", "v", "P", "dout"))
     out, lse, mu = plx.parallax_fwd(q, k, v, P)
-    dq, dk, dv, dP = plx.parallax_bwd(q, k, v, P, out, lse, mu, do)
+    dq, dk, dv, dP = plx.parallax_bwd(q, k, v, P, lse, mu, do)
     code, detail = plx.parallax_last_device_error()
     assert code == plx.PLX_OK, (code, hex(detail))
     return [to_host64(x) for x in (dq, dk, dv, dP)]
@@ -151,7 +151,7 @@ def test_backward_small_full_compare(path, B, H, T, d, dtype):
     got = _run_bwd(inp)
     tol = TOL_FP32 if dtype == "fp32" else TOL_BF16_GRAD
     for name, g, r in zip(("dq", "dk", "dv", "dP"), got, ref):
-        assert rel_err(g, r) < tol, name
+        assert rel_err(g, r, dtype if name != "dP" else "fp32") < tol, name
 
 
 def test_backward_full_size_c4_head_subset():
@@ -164,7 +164,7 @@ def test_backward_full_size_c4_head_subset():
     f = inputs_f64(inp)
     ref = oracle.backward(f["q"], f["k"], f["v"], f["P"], f["dout"], heads=heads)
     for name, g, r in zip(("dq", "dk", "dv"), got[:3], ref[:3]):
-        assert rel_err(g[:, h], r[:, h]) < TOL_BF16_GRAD, name
+        assert rel_err(g[:, h], r[:, h], "bf16") < TOL_BF16_GRAD, name
     assert rel_err(got[3][h], ref[3][h]) < TOL_BF16_GRAD, "dP"
     for g in got:
         assert np.isfinite(g).all()
