@@ -56,7 +56,8 @@ enum {
     PLX_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, misaligned base, size overflow */
     PLX_ERR_UNSUPPORTED = 2, /* d not in {64,128}, unknown dtype, device not sm_103 */
     PLX_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    PLX_ERR_TIMEOUT = 4      /* a device-side bounded wait gave up (see parallax_last_device_error) */
+    PLX_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up (see parallax_last_device_error) */
+    PLX_ERR_TOO_LARGE = 5    /* problem needs more scratch than parallax_fwd_noalloc's fixed array */
 };
 
 /* Element types of q, k, v, out, dout, dq, dk, dv. */
@@ -89,6 +90,32 @@ PLX_API size_t parallax_fwd_workspace_bytes(int B, int H, int T, int d, int dtyp
 PLX_API int parallax_fwd_ws(const void* q, const void* k, const void* v, const float* P,
                     void* out, float* lse, float* mu_k, void* workspace,
                     int B, int H, int T, int d, int dtype, void* stream);
+
+/*
+ * Forward that allocates nothing.  The paper has no counterpart: this entry
+ * point exists for callers that cannot call cudaMalloc.  Examples are a host
+ * whose device memory is owned by another allocator (a framework's caching
+ * allocator, or a fixed-budget arena), a latency-critical loop where an
+ * allocation would synchronise the device, and a plugin that may not allocate
+ * after start-up.
+ * Same arguments, layouts and results as parallax_fwd.  It computes with the
+ * SIMT (fp32 FFMA) forward kernels for both dtypes, whatever
+ * parallax_set_path() selects.
+ * Its workspace is one static 32 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits.  Problems
+ * whose workspace (B*H*T*d*4 + B*H*T*4 bytes, each rounded up to 256) exceeds
+ * 32 MiB return PLX_ERR_TOO_LARGE; nothing is launched.
+ * The first call on each device does a one-time set-up: it looks up the
+ * array's device address with that device current.  Make that first call
+ * before any stream capture.
+ * Every call shares the one array.  Calls whose work overlaps on the GPU
+ * (several streams, or several host threads on one device) race on it, so
+ * the caller must serialise them.  Calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ */
+PLX_API int parallax_fwd_noalloc(const void* q, const void* k, const void* v, const float* P,
+                         void* out, float* lse, float* mu_k,
+                         int B, int H, int T, int d, int dtype, void* stream);
 
 /* Bytes of device workspace parallax_bwd needs for these sizes (0 on bad args). */
 PLX_API size_t parallax_bwd_workspace_bytes(int B, int H, int T, int d, int dtype);

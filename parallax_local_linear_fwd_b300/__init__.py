@@ -17,6 +17,7 @@ import torch
 
 __all__ = [
     "PLX_OK", "PLX_ERR_INVALID_ARG", "PLX_ERR_UNSUPPORTED", "PLX_ERR_CUDA", "PLX_ERR_TIMEOUT",
+    "PLX_ERR_TOO_LARGE", "parallax_fwd_noalloc",
     "PLX_FP32", "PLX_BF16", "PLX_PATH_AUTO", "PLX_PATH_SIMT", "PLX_PATH_TC",
     "PlxError", "PlxLibraryMissing", "lib", "lib_path", "exported_symbols",
     "parallax_fwd", "parallax_fwd_ws", "parallax_bwd", "parallax_fwd_workspace_bytes",
@@ -26,6 +27,7 @@ __all__ = [
 ]
 
 PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
+PLX_ERR_TOO_LARGE = 5
 PLX_FP32, PLX_BF16 = 0, 1
 PLX_PATH_AUTO, PLX_PATH_SIMT, PLX_PATH_TC = 0, 1, 2
 
@@ -38,6 +40,7 @@ _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "parallax_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_bwd": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _vp]),
@@ -132,6 +135,28 @@ def parallax_fwd(q, k, v, P, out=None, lse=None, mu_k=None, stream=None):
         mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
     _check(lib().parallax_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
                               B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd")
+    return out, lse, mu_k
+
+
+def parallax_fwd_noalloc(q, k, v, P, out=None, lse=None, mu_k=None, stream=None):
+    """Forward that allocates no device memory inside the library.
+
+    For callers that cannot allocate (memory owned by another allocator, or a
+    loop where an allocation would synchronise the device).  Pass preallocated
+    out/lse/mu_k to keep this wrapper allocation-free too.  The library's
+    fixed 32 MiB scratch limits the size; larger problems raise PlxError with
+    PLX_ERR_TOO_LARGE.  Calls that overlap on the GPU race on that scratch.
+    """
+    B, H, T, d = _shape(q)
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if mu_k is None:
+        mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
+    _check(lib().parallax_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                                      B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd_noalloc")
     return out, lse, mu_k
 
 

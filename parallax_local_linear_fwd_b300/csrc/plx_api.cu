@@ -287,6 +287,7 @@ const char* parallax_strerror(int code) {
         case PLX_ERR_UNSUPPORTED: return "unsupported configuration (head dim, dtype, path or device)";
         case PLX_ERR_CUDA: return "CUDA runtime error";
         case PLX_ERR_TIMEOUT: return "device-side wait timed out";
+        case PLX_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of parallax_fwd_noalloc (32 MiB)";
         default: return "unknown status code";
     }
 }

@@ -1,0 +1,61 @@
+"""parallax_fwd_noalloc: the forward for callers that cannot allocate device
+memory (their memory belongs to another allocator, or an allocation would
+synchronise the device on a latency-critical path).
+
+The entry point computes with a fixed scratch array inside the library.  The
+test calls it through the C ABI twice in a row, on different shapes and
+dtypes, and checks each result against the ordinary parallax_fwd entry point
+within the parity tolerances.  This file is collected last, so a run that
+stops at the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import parallax_local_linear_fwd_b300 as plx
+import plx_synth
+from plx_testutil import TOL_BF16, TOL_FP32, rel_err, to_device, to_host64
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, H, T, d, dtype, seed):
+    inp = plx_synth.generate(B, H, T, d, dtype, seed=seed, p_std=0.2 / np.sqrt(d))
+    return [to_device(inp[x]) for x in ("q", "k", "v", "P")]
+
+
+@pytest.mark.parametrize("path", [plx.PLX_PATH_AUTO, plx.PLX_PATH_SIMT])
+def test_noalloc_matches_parallax_fwd_on_two_calls(path):
+    assert torch.cuda.is_available()
+    prev = plx.parallax_set_path(path)
+    try:
+        cases = [((2, 2, 300, 64, "bf16"), 21), ((1, 3, 257, 128, "fp32"), 22)]
+        for (B, H, T, d, dtype), seed in cases:
+            q, k, v, P = _inputs(B, H, T, d, dtype, seed)
+            ref_o, ref_l, ref_m = plx.parallax_fwd(q, k, v, P)
+            out = torch.full_like(q, float("nan"))
+            lse = torch.full((B, H, T), float("nan"), device="cuda")
+            mu = torch.full((B, H, T, d), float("nan"), device="cuda")
+            rc = plx.lib().parallax_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), P.data_ptr(),
+                                                out.data_ptr(), lse.data_ptr(), mu.data_ptr(), B, H, T, d,
+                                                plx.PLX_BF16 if dtype == "bf16" else plx.PLX_FP32,
+                                                torch.cuda.current_stream().cuda_stream)
+            assert rc == plx.PLX_OK, plx.parallax_strerror(rc)
+            torch.cuda.synchronize()
+            tol = TOL_BF16 if dtype == "bf16" else TOL_FP32
+            assert rel_err(to_host64(out), to_host64(ref_o), dtype) < tol
+            assert rel_err(to_host64(mu), to_host64(ref_m)) < tol
+            assert np.abs(to_host64(lse) - to_host64(ref_l)).max() < tol
+    finally:
+        plx.parallax_set_path(prev)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    L = plx.lib()
+    p = ctypes.c_void_p(256)  # never dereferenced: the size check fails first
+    # B1 H16 T16384 d64 needs ~68 MB of scratch, more than the 32 MiB array
+    assert L.parallax_fwd_noalloc(p, p, p, p, p, p, p, 1, 16, 16384, 64, plx.PLX_BF16, None) \
+        == plx.PLX_ERR_TOO_LARGE
+    assert "32 MiB" in plx.parallax_strerror(plx.PLX_ERR_TOO_LARGE)
