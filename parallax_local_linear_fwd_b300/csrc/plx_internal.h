@@ -61,6 +61,10 @@ size_t simt_fwd_ws_bytes(int B, int H, int T, int d);
 size_t simt_bwd_ws_bytes(int B, int H, int T, int d);
 cudaError_t simt_fwd(const FwdArgs& a);
 cudaError_t simt_bwd(const BwdArgs& a);
+// The SIMT backward after its first kernel (B2, dP, B3, dq cast), reading
+// R and ebar from the SIMT workspace; lets another family supply B1.
+cudaError_t simt_bwd_after_b1(const BwdArgs& a);
+void simt_bwd_ws_b1_outputs(void* ws, int B, int H, int T, int d, float** R, float** ebar);
 
 // Tensor-core (tcgen05) family: bf16, d in {64,128}.
 bool tc_available();

@@ -822,19 +822,13 @@ cudaError_t fwd_impl(const FwdArgs& a) {
     return cudaGetLastError();
 }
 
+// B2, dP, B3 and the dq cast; expects R and ebar (B1's outputs) in the workspace.
 template <typename Tin, int D>
-cudaError_t bwd_impl(const BwdArgs& a) {
+cudaError_t bwd_rest_impl(const BwdArgs& a) {
     constexpr int BM = D == 128 ? 32 : 64;
     const float scale = 1.f / sqrtf((float)D);
     const float scale_log2 = LOG2E * scale;
     BwdWs w = bwd_ws(a.ws, a.B, a.H, a.T, a.d);
-    const dim3 grid((a.T + BQ - 1) / BQ, a.B * a.H);
-    PLX_TRY(set_smem(simt_bwd_b1<Tin, D>, smem_b1<D>()));
-    timing_begin(a.stream, "simt_bwd_b1");
-    simt_bwd_b1<Tin, D><<<grid, NT, smem_b1<D>(), a.stream>>>(
-        (const Tin*)a.q, (const Tin*)a.k, (const Tin*)a.v, (const Tin*)a.dout, a.lse, w.R, w.ebar, a.T, scale_log2);
-    timing_end(a.stream);
-    PLX_TRY(cudaGetLastError());
     PLX_TRY(set_smem(simt_bwd_b2<Tin, D>, smem_proj<D>()));
     const dim3 pgrid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
     timing_begin(a.stream, "simt_bwd_b2");
@@ -868,6 +862,20 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     return cudaGetLastError();
 }
 
+template <typename Tin, int D>
+cudaError_t bwd_impl(const BwdArgs& a) {
+    const float scale_log2 = LOG2E / sqrtf((float)D);
+    BwdWs w = bwd_ws(a.ws, a.B, a.H, a.T, a.d);
+    const dim3 grid((a.T + BQ - 1) / BQ, a.B * a.H);
+    PLX_TRY(set_smem(simt_bwd_b1<Tin, D>, smem_b1<D>()));
+    timing_begin(a.stream, "simt_bwd_b1");
+    simt_bwd_b1<Tin, D><<<grid, NT, smem_b1<D>(), a.stream>>>(
+        (const Tin*)a.q, (const Tin*)a.k, (const Tin*)a.v, (const Tin*)a.dout, a.lse, w.R, w.ebar, a.T, scale_log2);
+    timing_end(a.stream);
+    PLX_TRY(cudaGetLastError());
+    return bwd_rest_impl<Tin, D>(a);
+}
+
 }  // namespace
 
 size_t simt_fwd_ws_bytes(int B, int H, int T, int d) {
@@ -884,6 +892,17 @@ size_t simt_bwd_ws_bytes(int B, int H, int T, int d) {
 cudaError_t simt_fwd(const FwdArgs& a) {
     if (a.dtype == 0) return a.d == 64 ? fwd_impl<float, 64>(a) : fwd_impl<float, 128>(a);
     return a.d == 64 ? fwd_impl<__nv_bfloat16, 64>(a) : fwd_impl<__nv_bfloat16, 128>(a);
+}
+
+cudaError_t simt_bwd_after_b1(const BwdArgs& a) {
+    if (a.dtype == 0) return a.d == 64 ? bwd_rest_impl<float, 64>(a) : bwd_rest_impl<float, 128>(a);
+    return a.d == 64 ? bwd_rest_impl<__nv_bfloat16, 64>(a) : bwd_rest_impl<__nv_bfloat16, 128>(a);
+}
+
+void simt_bwd_ws_b1_outputs(void* ws, int B, int H, int T, int d, float** R, float** ebar) {
+    BwdWs w = bwd_ws(ws, B, H, T, d);
+    *R = w.R;
+    *ebar = w.ebar;
 }
 
 cudaError_t simt_bwd(const BwdArgs& a) {

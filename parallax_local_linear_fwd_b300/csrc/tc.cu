@@ -1,10 +1,750 @@
-// Tensor-core (tcgen05) kernels: not built yet.
+// Tensor-core (tcgen05 / TMEM / TMA) kernels for the Parallax attention layer,
+// sm_103a.  Inputs are bf16; every MMA operand is f16 with fp32 accumulation:
+// the inputs convert to f16 exactly (within its range), and the operands the
+// path itself rounds (P~, u, the pass-2 and backward weights) keep three more
+// mantissa bits than bf16 would, which the stated output tolerance needs.
+//
+// Layer ("Parallax: Parameterized Local Linear Attention for Language
+// Modeling", technical summary, "Core mechanism" and "Hardware-aware
+// algorithm"; probe u = P_h (q - mu_k)):
+//   pass 1 (tc_pass1) : S = c Q K^T on a key tile, online softmax, Mu += P~ K;
+//                       emits lse and mu_k = Mu / l.
+//   projection        : u = P_h (q - mu_k) rounded to f16, gbar = mu_k . u.
+//   pass 2 (tc_dual)  : S = c Q K^T and G = U K^T on the SAME key tile in
+//                       shared memory (both branches read one KV stream);
+//                       weights p (1 + g - gbar) with p from the stored lse;
+//                       O += W V.
+//   backward B1 (tc_dual, second mode): S = c Q K^T and E = dO V^T;
+//                       weights p e; R += W K and ebar = sum p e.
+//
+// Warp roles in every tensor-core kernel (192 threads): warp 0 issues TMA
+// loads, warp 1 owns TMEM and issues the MMAs (one thread), warps 2-5 move
+// scores between TMEM and registers (thread = query row) and write results.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "plx_internal.h"
+#include "tc_ptx.cuh"
 
 namespace plx {
-bool tc_available() { return false; }
-size_t tc_fwd_ws_bytes(int, int, int, int) { return 0; }
-size_t tc_bwd_ws_bytes(int, int, int, int) { return 0; }
-cudaError_t tc_fwd(const FwdArgs&) { return cudaErrorNotSupported; }
-cudaError_t tc_bwd(const BwdArgs&) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr int NTHREADS = 192;
+// Online-softmax rescale threshold (log2 units): the running max is only
+// moved when a row max exceeds it by more than this, so p~ <= 2^8.
+constexpr float RESCALE_TH = 8.f;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// ================================================================ pass 1
+template <int D>
+struct P1 {
+    static constexpr int BM = 128, BN = 128;
+    static constexpr int NS = D == 64 ? 4 : 2;  // K-tile stages
+    static constexpr int QB = BM * D * 2;
+    static constexpr int KB = BN * D * 2;
+    static constexpr int NBAR = 1 + 2 * NS + 4;
+    static constexpr int SMEM = 1024 + QB + NS * KB + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 256;  // S [0,128) (P~ f16 aliases [0,64)), Mu [128, 128+D)
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    tc_pass1(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             float* __restrict__ lse, float* __restrict__ mu_k, int T, int BH, int ntq, float scale_log2,
+             unsigned* status) {
+    using C = P1<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sQ = sm;
+    uint8_t* sK = sQ + C::QB;
+    uint64_t* bars = (uint64_t*)(sK + NS * C::KB);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = bars + 1 + NS;
+    uint64_t* s_full = bars + 1 + 2 * NS;
+    uint64_t* p_full = s_full + 1;
+    uint64_t* o_done = s_full + 2;
+    uint64_t* drain = s_full + 3;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x;
+    const int qt = ntq - 1 - item / BH;  // longest rows first
+    const int bh = item % BH;
+    const int q0 = qt * C::BM;
+    const int nkt = min(qt, (T - 1) / C::BN) + 1;
+    const Watchdog wd{status, abortf, KID_TC_PASS1};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tS = tmem, tMu = tmem + 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            mbar_expect_tx(q_full, C::QB);
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) tma_load_3d(sQ + r * C::BM * 128, &tm_q, r * 64, q0, bh, q_full);
+            int issued = 0;
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&k_full[s], C::KB);
+#pragma unroll
+                for (int r = 0; r < D / 64; r++)
+                    tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
+                issued = j + 1;
+            }
+            // Every load issued must land before the CTA may exit.
+            mbar_wait_drain(q_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_mma(128, C::BN, false, false);
+            const uint32_t idM = idesc_mma(128, D, false, true);
+            const uint32_t qaddr = smem_u32(sQ);
+            if (mbar_wait(q_full, 0, wd, 2)) {
+                for (int j = 0; j < nkt; j++) {
+                    const int s = j % NS;
+                    if (!mbar_wait(&k_full[s], (j / NS) & 1, wd, 3)) break;
+                    // S aliases the previous tile's P~: wait until that MMA finished.
+                    if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, wd, 4)) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sK + s * C::KB);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(qaddr, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    if (!mbar_wait(p_full, j & 1, wd, 5)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; kk++)
+                        mma_ts(tMu, tS + kk * 8, desc_mnmajor(kaddr, C::BN, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(o_done);
+                    mma_commit(&k_empty[s]);
+                }
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        // softmax / epilogue warps: thread <-> query row (TMEM lane)
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int t = q0 + row;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        float m_use = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            ok = mbar_wait(s_full, j & 1, wd, 6);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * C::BN;
+            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;  // key k0 + c valid iff c <= lim
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t v[32];
+                tmem_ld32(tS + lrow + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    if (c * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+            }
+            mx *= scale_log2;
+            const float m_new = fmaxf(m_use, mx);
+            const bool need = m_new > m_use + RESCALE_TH;
+            float alpha = 1.f;
+            if (need) {
+                alpha = fast_exp2(m_use - m_new);
+                m_use = m_new;
+            }
+            l *= alpha;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok = mbar_wait(o_done, (j - 1) & 1, wd, 7);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tMu + lrow + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st32(tMu + lrow + c * 32, v);
+                }
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t v[32];
+                tmem_ld32(tS + lrow + c * 32, v);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const int c0 = c * 32 + 2 * i;
+                    const float p0 = c0 <= lim ? fast_exp2(fmaf(__uint_as_float(v[2 * i]), scale_log2, -m_use)) : 0.f;
+                    const float p1 =
+                        c0 + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), scale_log2, -m_use)) : 0.f;
+                    sum += p0 + p1;
+                    pk[i] = pack_f16(p0, p1);
+                }
+                tmem_st16(tS + lrow + c * 16, pk);
+            }
+            l += sum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok) {
+            ok = mbar_wait(o_done, (nkt - 1) & 1, wd, 8);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float inv = 1.f / l;
+                float* dst = mu_k + ((size_t)bh * T + t) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tMu + lrow + c * 32, v);
+                    tmem_wait_ld();
+                    if (t < T) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *(float4*)(dst + c * 32 + i) =
+                                make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
+                                            __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                    }
+                }
+                if (t < T) lse[(size_t)bh * T + t] = (m_use + __log2f(l)) * LN2;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ============================================================ projection
+// u = P_h (q - mu_k) in fp32, stored as f16 (the MMA operand of pass 2), and
+// gbar = mu_k . u computed from the stored (rounded) u, so that
+// sum_i p_i (g_i - gbar) vanishes for the values the MMA sees.
+template <int D>
+__global__ void __launch_bounds__(256) tc_proj(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mu_k,
+                                               const float* __restrict__ P, __half* __restrict__ U,
+                                               float* __restrict__ gbar, int B, int H, int T, int rows_per_cta) {
+    extern __shared__ float psm[];
+    constexpr int LD = D + 1, NA = D / 32;
+    float* PT = psm;          // PT[b][a] = P[a][b]
+    float* dl = PT + D * LD;  // per-warp delta buffer
+    const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* Ph = P + (size_t)h * D * D;
+    for (int e = threadIdx.x; e < D * D; e += 256) PT[(e % D) * LD + e / D] = Ph[e];
+    __syncthreads();
+    float* dw = dl + warp * D;
+    const int r_begin = blockIdx.x * rows_per_cta;
+    const int r_end = min(r_begin + rows_per_cta, B * T);
+    for (int r = r_begin + warp; r < r_end; r += 8) {
+        const int b = r / T, t = r % T;
+        const size_t row = ((size_t)b * H + h) * T + t;
+        float mk[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) {
+            const int a = lane + 32 * j;
+            mk[j] = mu_k[row * D + a];
+            dw[a] = __bfloat162float(q[row * D + a]) - mk[j];
+        }
+        __syncwarp();
+        float u[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) u[j] = 0.f;
+        for (int bb = 0; bb < D; bb++) {
+            const float db = dw[bb];
+#pragma unroll
+            for (int j = 0; j < NA; j++) u[j] = fmaf(PT[bb * LD + lane + 32 * j], db, u[j]);
+        }
+        float g = 0.f;
+#pragma unroll
+        for (int j = 0; j < NA; j++) {
+            const __half uh = __float2half_rn(u[j]);
+            U[row * D + lane + 32 * j] = uh;
+            g = fmaf(mk[j], __half2float(uh), g);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+        if (lane == 0) gbar[row] = g;
+        __syncwarp();
+    }
+}
+
+// ====================================================== f16 operand copies
+// The MMAs take f16 operands: a bf16 input converts to f16 exactly when its
+// magnitude lies in f16's normal range (larger magnitudes saturate to the
+// largest finite f16; tiny ones keep an absolute error below 2^-25).
+struct CvtJob {
+    const uint4* src[4];
+    uint4* dst[4];
+};
+
+__global__ void __launch_bounds__(256) tc_to_f16(CvtJob job, size_t n8) {
+    const uint4* __restrict__ src = job.src[blockIdx.y];
+    uint4* __restrict__ dst = job.dst[blockIdx.y];
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 x = src[i];
+        dst[i] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
+                            pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
+    }
+}
+
+// ======================================================== dual-score pass
+// MODE 0 (forward pass 2): X = U K^T, W = p (x + 1 - gbar), Acc += W V, out = Acc.
+// MODE 1 (backward B1)   : X = dO V^T, W = p x,           Acc += W K, R = Acc,
+//                          ebar = sum_i W (fp32, before rounding).
+template <int D>
+struct DualCfg {
+    static constexpr int BM = 128, BN = 64;
+    static constexpr int NS = D == 64 ? 4 : 1;  // K+V stages
+    static constexpr int AB = BM * D * 2;       // one A tile (Q, U or dO)
+    static constexpr int KB = BN * D * 2;       // one K or V tile
+    static constexpr int NBAR = 1 + 2 * NS + 4;
+    static constexpr int SMEM = 1024 + 2 * AB + NS * 2 * KB + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 256;  // S [0,64) (W aliases [0,32)), X [64,128), Acc [128,128+D)
+};
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    tc_dual(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
+            const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+            const float* __restrict__ lse, const float* __restrict__ gbar, void* __restrict__ acc_out,
+            float* __restrict__ ebar_out, int T, int BH, int ntq, float scale_log2, unsigned* status) {
+    using C = DualCfg<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sA1 = sm;
+    uint8_t* sA2 = sA1 + C::AB;
+    uint8_t* sKV = sA2 + C::AB;  // stage s: K at s * 2KB, V at s * 2KB + KB
+    uint64_t* bars = (uint64_t*)(sKV + NS * 2 * C::KB);
+    uint64_t* a_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = bars + 1 + NS;
+    uint64_t* s_full = bars + 1 + 2 * NS;
+    uint64_t* w_full = s_full + 1;
+    uint64_t* acc_done = s_full + 2;
+    uint64_t* drain = s_full + 3;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x;
+    const int qt = ntq - 1 - item / BH;
+    const int bh = item % BH;
+    const int q0 = qt * C::BM;
+    const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
+    const Watchdog wd{status, abortf, MODE == 0 ? (unsigned)KID_TC_PASS2 : (unsigned)KID_TC_BWD_B1};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(a_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(w_full, 128);
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tS = tmem, tX = tmem + 64, tAcc = tmem + 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_a1);
+            prefetch_tmap(&tm_a2);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(a_full, 2 * C::AB);
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) {
+                tma_load_3d(sA1 + r * C::BM * 128, &tm_a1, r * 64, q0, bh, a_full);
+                tma_load_3d(sA2 + r * C::BM * 128, &tm_a2, r * 64, q0, bh, a_full);
+            }
+            int issued = 0;
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&kv_full[s], 2 * C::KB);
+                uint8_t* st = sKV + s * 2 * C::KB;
+#pragma unroll
+                for (int r = 0; r < D / 64; r++) {
+                    tma_load_3d(st + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &kv_full[s]);
+                    tma_load_3d(st + C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &kv_full[s]);
+                }
+                issued = j + 1;
+            }
+            mbar_wait_drain(a_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_mma(128, C::BN, false, false);
+            const uint32_t idA = idesc_mma(128, D, false, true);
+            const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
+            if (mbar_wait(a_full, 0, wd, 2)) {
+                for (int j = 0; j < nkt; j++) {
+                    const int s = j % NS;
+                    if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
+                    if (j > 0 && !mbar_wait(acc_done, (j - 1) & 1, wd, 4)) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
+                    const uint32_t vaddr = kaddr + C::KB;
+                    const uint32_t xb = MODE == 0 ? kaddr : vaddr;  // B of the second score product
+                    const uint32_t ab = MODE == 0 ? vaddr : kaddr;  // B of the accumulation
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    if (!mbar_wait(w_full, j & 1, wd, 5)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; kk++)
+                        mma_ts(tAcc, tS + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(acc_done);
+                    mma_commit(&kv_empty[s]);
+                }
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int t = q0 + row;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        const bool valid = t < T;
+        const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
+        const float g1 = (MODE == 0 && valid) ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
+        float rowsum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            ok = mbar_wait(s_full, j & 1, wd, 6);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * C::BN;
+            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t vs[32], vx[32];
+                tmem_ld32(tS + lrow + c * 32, vs);
+                tmem_ld32(tX + lrow + c * 32, vx);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    float w[2];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int cc = c * 32 + 2 * i + h;
+                        const float p =
+                            cc <= lim ? fast_exp2(fmaf(__uint_as_float(vs[2 * i + h]), scale_log2, -L2)) : 0.f;
+                        const float x = __uint_as_float(vx[2 * i + h]);
+                        w[h] = MODE == 0 ? p * (x + g1) : p * x;
+                    }
+                    pk[i] = pack_f16(w[0], w[1]);
+                    // ebar sums the rounded weights the MMA sees, so that
+                    // R - ebar mu_k = sum_i w_i (k_i - mu_k) holds for them.
+                    if (MODE == 1) rowsum += f16_lo(pk[i]) + f16_hi(pk[i]);
+                }
+                tmem_st16(tS + lrow + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(w_full);
+        }
+        if (ok) {
+            ok = mbar_wait(acc_done, (nkt - 1) & 1, wd, 8);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tAcc + lrow + c * 32, v);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const size_t off = ((size_t)bh * T + t) * D + c * 32;
+                        if (MODE == 0) {
+                            uint4* dst = (uint4*)((__nv_bfloat16*)acc_out + off);
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                dst[i] = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+                        } else {
+                            float* dst = (float*)acc_out + off;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        }
+                    }
+                }
+                if (MODE == 1 && valid) ebar_out[(size_t)bh * T + t] = rowsum;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ================================================================= host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+// A 16-bit [BH][T][D] tensor viewed as 3-D (D, T, BH) with a box of 64 x rows
+// x 1 and the 128-byte swizzle; rows past T (within a head) read as zero.
+bool make_map(CUtensorMap* m, const void* base, int D, int T, int BH, int rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#define PLX_TRY(x)                         \
+    do {                                   \
+        cudaError_t e_ = (x);              \
+        if (e_ != cudaSuccess) return e_;  \
+    } while (0)
+
+constexpr int PROJ_ROWS = 128;
+
+// Workspace of the tensor-core forward: f16 copies of q, k, v, then U (f16)
+// and gbar (fp32).
+struct TcFwdWs {
+    __half *q16, *k16, *v16, *U;
+    float* gbar;
+};
+TcFwdWs tc_fwd_ws(void* ws, int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T, nd2 = align256(n * d * 2);
+    char* p = (char*)ws;
+    TcFwdWs w;
+    w.q16 = (__half*)p;
+    w.k16 = (__half*)(p + nd2);
+    w.v16 = (__half*)(p + 2 * nd2);
+    w.U = (__half*)(p + 3 * nd2);
+    w.gbar = (float*)(p + 4 * nd2);
+    return w;
+}
+
+// Workspace of the tensor-core backward: the SIMT workspace (R, ebar and the
+// later stages' buffers) followed by f16 copies of q, k, v, dO.
+struct TcBwdWs {
+    __half *q16, *k16, *v16, *do16;
+};
+TcBwdWs tc_bwd_ws(void* ws, int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T, nd2 = align256(n * d * 2);
+    char* p = (char*)ws + align256(simt_bwd_ws_bytes(B, H, T, d));
+    return TcBwdWs{(__half*)p, (__half*)(p + nd2), (__half*)(p + 2 * nd2), (__half*)(p + 3 * nd2)};
+}
+
+cudaError_t to_f16(const void* const* src, __half* const* dst, int count, size_t n, cudaStream_t s) {
+    CvtJob job{};
+    for (int i = 0; i < count; i++) {
+        job.src[i] = (const uint4*)src[i];
+        job.dst[i] = (uint4*)dst[i];
+    }
+    const size_t n8 = n / 8;  // n = B H T d, a multiple of 64
+    const unsigned gx = (unsigned)std::min<size_t>((n8 + 255) / 256, 148 * 8);
+    timing_begin(s, "tc_to_f16");
+    tc_to_f16<<<dim3(gx, count), 256, 0, s>>>(job, n8);
+    timing_end(s);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t fwd_impl(const FwdArgs& a) {
+    const int BH = a.B * a.H;
+    const float scale_log2 = LOG2E / sqrtf((float)D);
+    const size_t n = (size_t)BH * a.T * D;
+    TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
+    CUtensorMap mq128, mk128, mu128, mk64, mv64;
+    if (!make_map(&mq128, w.q16, D, a.T, BH, 128) || !make_map(&mk128, w.k16, D, a.T, BH, 128) ||
+        !make_map(&mu128, w.U, D, a.T, BH, 128) || !make_map(&mk64, w.k16, D, a.T, BH, 64) ||
+        !make_map(&mv64, w.v16, D, a.T, BH, 64))
+        return cudaErrorInvalidValue;
+    {
+        const void* src[3] = {a.q, a.k, a.v};
+        __half* dst[3] = {w.q16, w.k16, w.v16};
+        PLX_TRY(to_f16(src, dst, 3, n, a.stream));
+    }
+    {  // pass 1
+        using C = P1<D>;
+        const int ntq = (a.T + C::BM - 1) / C::BM;
+        PLX_TRY(cudaFuncSetAttribute(tc_pass1<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_pass1");
+        tc_pass1<D><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mk128, a.lse, a.mu_k, a.T, BH, ntq,
+                                                                scale_log2, a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    {  // projection
+        const size_t sm = sizeof(float) * (D * (D + 1) + 8 * D);
+        PLX_TRY(cudaFuncSetAttribute(tc_proj<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        const dim3 grid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
+        timing_begin(a.stream, "tc_proj");
+        tc_proj<D><<<grid, 256, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, w.U, w.gbar, a.B, a.H,
+                                                a.T, PROJ_ROWS);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    {  // pass 2
+        using C = DualCfg<D>;
+        const int ntq = (a.T + C::BM - 1) / C::BM;
+        PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_pass2");
+        tc_dual<D, 0><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, a.lse, w.gbar, a.out,
+                                                                  nullptr, a.T, BH, ntq, scale_log2, a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t bwd_impl(const BwdArgs& a) {
+    const int BH = a.B * a.H;
+    const float scale_log2 = LOG2E / sqrtf((float)D);
+    const size_t n = (size_t)BH * a.T * D;
+    float *R = nullptr, *ebar = nullptr;
+    simt_bwd_ws_b1_outputs(a.ws, a.B, a.H, a.T, D, &R, &ebar);
+    TcBwdWs w = tc_bwd_ws(a.ws, a.B, a.H, a.T, D);
+    CUtensorMap mq128, mdo128, mk64, mv64;
+    if (!make_map(&mq128, w.q16, D, a.T, BH, 128) || !make_map(&mdo128, w.do16, D, a.T, BH, 128) ||
+        !make_map(&mk64, w.k16, D, a.T, BH, 64) || !make_map(&mv64, w.v16, D, a.T, BH, 64))
+        return cudaErrorInvalidValue;
+    {
+        const void* src[4] = {a.q, a.k, a.v, a.dout};
+        __half* dst[4] = {w.q16, w.k16, w.v16, w.do16};
+        PLX_TRY(to_f16(src, dst, 4, n, a.stream));
+    }
+    using C = DualCfg<D>;
+    const int ntq = (a.T + C::BM - 1) / C::BM;
+    PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    timing_begin(a.stream, "tc_bwd_b1");
+    tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr, R, ebar,
+                                                              a.T, BH, ntq, scale_log2, a.status);
+    timing_end(a.stream);
+    PLX_TRY(cudaGetLastError());
+    return simt_bwd_after_b1(a);
+}
+
+}  // namespace
+
+bool tc_available() { return encode_fn() != nullptr; }
+
+size_t tc_fwd_ws_bytes(int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T;
+    return 4 * align256(n * d * 2) + align256(n * 4);
+}
+
+size_t tc_bwd_ws_bytes(int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T;
+    return align256(simt_bwd_ws_bytes(B, H, T, d)) + 4 * align256(n * d * 2);
+}
+
+cudaError_t tc_fwd(const FwdArgs& a) {
+    if (a.dtype != 1) return cudaErrorNotSupported;
+    return a.d == 64 ? fwd_impl<64>(a) : fwd_impl<128>(a);
+}
+
+cudaError_t tc_bwd(const BwdArgs& a) {
+    if (a.dtype != 1) return cudaErrorNotSupported;
+    return a.d == 64 ? bwd_impl<64>(a) : bwd_impl<128>(a);
+}
+
 }  // namespace plx
