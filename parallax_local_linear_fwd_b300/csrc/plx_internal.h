@@ -65,6 +65,11 @@ cudaError_t simt_bwd(const BwdArgs& a);
 // R and ebar from the SIMT workspace; lets another family supply B1.
 cudaError_t simt_bwd_after_b1(const BwdArgs& a);
 void simt_bwd_ws_b1_outputs(void* ws, int B, int H, int T, int d, float** R, float** ebar);
+// dP_h = sum_{b,t} du delta^T (delta = q - mu_k) by the SIMT two-stage
+// fixed-order reduction; `partial` holds simt_dp_partial_bytes() bytes.
+size_t simt_dp_partial_bytes(int B, int H, int T, int d);
+cudaError_t simt_dP(const void* q, const float* mu_k, const float* du, float* partial, float* dP, int B, int H,
+                    int T, int d, int dtype, cudaStream_t stream);
 
 // Tensor-core (tcgen05) family: bf16, d in {64,128}.
 bool tc_available();

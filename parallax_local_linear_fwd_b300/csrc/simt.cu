@@ -26,6 +26,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "plx_internal.h"
 
 namespace plx {
@@ -903,6 +905,34 @@ void simt_bwd_ws_b1_outputs(void* ws, int B, int H, int T, int d, float** R, flo
     BwdWs w = bwd_ws(ws, B, H, T, d);
     *R = w.R;
     *ebar = w.ebar;
+}
+
+size_t simt_dp_partial_bytes(int B, int H, int T, int d) {
+    const size_t nchunks = ((size_t)B * T + DP_ROWS - 1) / DP_ROWS;
+    return align256((size_t)H * nchunks * d * d * 4);
+}
+
+cudaError_t simt_dP(const void* q, const float* mu_k, const float* du, float* partial, float* dP, int B, int H,
+                    int T, int d, int dtype, cudaStream_t stream) {
+    const int nchunks = (B * T + DP_ROWS - 1) / DP_ROWS;
+    auto run = [&](auto tin, auto dd) -> cudaError_t {
+        using Tin = decltype(tin);
+        constexpr int D = decltype(dd)::value;
+        PLX_TRY(set_smem(simt_dp_partial<Tin, D>, smem_dp<D>()));
+        timing_begin(stream, "simt_dp_partial");
+        simt_dp_partial<Tin, D><<<dim3(nchunks, H), NT, smem_dp<D>(), stream>>>((const Tin*)q, mu_k, du, partial,
+                                                                                 B, H, T, DP_ROWS);
+        timing_end(stream);
+        PLX_TRY(cudaGetLastError());
+        timing_begin(stream, "simt_dp_reduce");
+        simt_dp_reduce<<<dim3((D * D + 255) / 256, H), 256, 0, stream>>>(partial, dP, nchunks, D * D);
+        timing_end(stream);
+        return cudaGetLastError();
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    if (dtype == 0) return d == 64 ? run(float{}, I64{}) : run(float{}, I128{});
+    return d == 64 ? run(__nv_bfloat16{}, I64{}) : run(__nv_bfloat16{}, I128{});
 }
 
 cudaError_t simt_bwd(const BwdArgs& a) {

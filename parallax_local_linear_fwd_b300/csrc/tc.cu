@@ -562,6 +562,404 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
+// ============================================================ backward B2
+// Per row: delta = q - mu_k, u = P_h delta (fp32), U = f16(u), du = R - ebar mu_k
+// (overwrites R), ddelta = P_h^T du, dq_acc = ddelta, dmu = -ddelta (f16),
+// and the row scalars B3 needs, packed {lse log2 e, mu_k . U, ebar, D} with
+//   D = do.o - gbar ebar + mu_k . dmu,  do.o = ebar + R.u - gbar ebar
+// (do.o rebuilt from B1's fp32 sums; gbar = mu_k . u in fp32 here, while the
+// packed mu_k . U matches the f16 U that B3's G = K U^T sees).
+template <int D>
+__global__ void __launch_bounds__(256) tc_bwd_b2(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mu_k,
+                                                 const float* __restrict__ P, const float* __restrict__ lse,
+                                                 float* __restrict__ R, const float* __restrict__ ebar,
+                                                 __half* __restrict__ U, __half* __restrict__ dmu,
+                                                 float* __restrict__ dq_acc, float4* __restrict__ rowpack, int B,
+                                                 int H, int T, int rows_per_cta) {
+    extern __shared__ float psm[];
+    constexpr int LD = D + 1, NA = D / 32;
+    float* PT = psm;           // PT[b][a] = P[a][b]
+    float* buf = PT + D * LD;  // per-warp [D]
+    const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* Ph = P + (size_t)h * D * D;
+    for (int e = threadIdx.x; e < D * D; e += 256) PT[(e % D) * LD + e / D] = Ph[e];
+    __syncthreads();
+    float* w = buf + warp * D;
+    const int r_begin = blockIdx.x * rows_per_cta;
+    const int r_end = min(r_begin + rows_per_cta, B * T);
+    for (int r = r_begin + warp; r < r_end; r += 8) {
+        const int b = r / T, t = r % T;
+        const size_t row = ((size_t)b * H + h) * T + t;
+        float mk[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) {
+            const int a = lane + 32 * j;
+            mk[j] = mu_k[row * D + a];
+            w[a] = __bfloat162float(q[row * D + a]) - mk[j];
+        }
+        __syncwarp();
+        float u[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) u[j] = 0.f;
+        for (int bb = 0; bb < D; bb++) {
+            const float db = w[bb];
+#pragma unroll
+            for (int j = 0; j < NA; j++) u[j] = fmaf(PT[bb * LD + lane + 32 * j], db, u[j]);
+        }
+        const float eb = ebar[row];
+        float g = 0.f, gr = 0.f, ru = 0.f, du[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) {
+            const int a = lane + 32 * j;
+            const float rr = R[row * D + a];
+            const __half uh = __float2half_rn(u[j]);
+            g = fmaf(mk[j], u[j], g);
+            gr = fmaf(mk[j], __half2float(uh), gr);
+            ru = fmaf(rr, u[j], ru);
+            du[j] = rr - eb * mk[j];
+            U[row * D + a] = uh;
+            R[row * D + a] = du[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            gr += __shfl_xor_sync(0xffffffffu, gr, o);
+            ru += __shfl_xor_sync(0xffffffffu, ru, o);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NA; j++) w[lane + 32 * j] = du[j];
+        __syncwarp();
+        float dd[NA];
+#pragma unroll
+        for (int j = 0; j < NA; j++) dd[j] = 0.f;
+        for (int a = 0; a < D; a++) {
+            const float da = w[a];
+#pragma unroll
+            for (int j = 0; j < NA; j++) dd[j] = fmaf(PT[(lane + 32 * j) * LD + a], da, dd[j]);
+        }
+        float x = 0.f;
+#pragma unroll
+        for (int j = 0; j < NA; j++) {
+            const int a = lane + 32 * j;
+            dq_acc[row * D + a] = dd[j];
+            dmu[row * D + a] = __float2half_rn(-dd[j]);
+            x = fmaf(mk[j], -dd[j], x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) {
+            const float doo = eb + ru - g * eb;
+            rowpack[row] = make_float4(lse[row] * LOG2E, gr, eb, doo - g * eb + x);
+        }
+        __syncwarp();
+    }
+}
+
+// ============================================================ backward B3
+// CTA = one tile of 128 keys of one head; queries stream in sub-chunks of 64.
+// Per sub-chunk (TMEM lanes = keys i, columns = queries t):
+//   S^T = K Q^T, G^T = K U^T, Y^T = K dmu^T, E^T = V dO^T
+//   p = exp(c s - lse_t), w1 = 1 + g - gbar_t, a = p w1, dg = p (e - ebar_t),
+//   ds = c p (e w1 - g ebar_t + y - D_t)
+//   dV += a dO, dK += dg U + ds Q + p dmu      (A operands f16 in TMEM)
+// and per 128 queries dQ += ds^T K (A = ds from shared memory), added into the
+// fp32 dq accumulator with vector reductions.
+template <int D>
+struct B3Cfg {
+    static constexpr int BK = 128, BQ = 64, QT = 128;
+    static constexpr int NS = D == 64 ? 2 : 1;  // sub-chunk stages
+    static constexpr int KB = BK * D * 2;       // K or V tile
+    static constexpr int SB = BQ * D * 2;       // one 64-row operand sub-tile
+    static constexpr int RB = BQ * 16;          // row scalars of a sub-chunk
+    static constexpr int STAGE = 4 * SB + RB;   // Q, U, dmu, dO, rows
+    static constexpr int DSB = BK * QT * 2;     // ds, f16 [keys][128 queries]
+    static constexpr int NBAR = 1 + 2 * NS + 6;
+    static constexpr int SMEM = 1024 + 2 * KB + DSB + NS * STAGE + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 512;
+    // TMEM columns: S^T [0,64), G^T [64,128), E^T [128,192), Y^T [192,256),
+    // dV [256, 256+D), dK [256+D, 256+2D); dQ reuses [128, 128+D).
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_bwd_b3(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
+              const __grid_constant__ CUtensorMap tm_dmu, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_rows, float* __restrict__ dq_acc,
+              __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T, int BH, int nkt, float scale,
+              float scale_log2, unsigned* status) {
+    using C = B3Cfg<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sK = sm;
+    uint8_t* sV = sK + C::KB;
+    uint8_t* sDS = sV + C::KB;
+    uint8_t* sSt = sDS + C::DSB;  // stage s: Q, U, dmu, dO sub-tiles, then the row scalars
+    uint64_t* bars = (uint64_t*)(sSt + NS * C::STAGE);
+    uint64_t* kv_full = bars;
+    uint64_t* st_full = bars + 1;
+    uint64_t* st_empty = bars + 1 + NS;
+    uint64_t* sc_full = bars + 1 + 2 * NS;
+    uint64_t* op_full = sc_full + 1;
+    uint64_t* acc_done = sc_full + 2;
+    uint64_t* dq_full = sc_full + 3;
+    uint64_t* dq_free = sc_full + 4;
+    uint64_t* drain = sc_full + 5;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x / BH;  // tiles with the most queries first
+    const int bh = blockIdx.x % BH;
+    const int k0 = kt * C::BK;
+    // sub-chunk j covers queries [k0 + 64 j, k0 + 64 j + 64); pairs j = 2m, 2m + 1
+    // form the m-th 128-query tile of the dQ product
+    const int nsub = (T - k0 + C::BQ - 1) / C::BQ;
+    const Watchdog wd{status, abortf, KID_TC_BWD_B3};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&st_full[s], 1);
+            mbar_init(&st_empty[s], 1);
+        }
+        mbar_init(sc_full, 1);
+        mbar_init(op_full, 128);
+        mbar_init(acc_done, 1);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, 128);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    // ds buffer starts at zero: a query tile cut by T leaves its upper half
+    // unwritten, and the dQ MMA must not read stale or uninitialised bits.
+    for (int i = threadIdx.x; i < C::DSB / 16; i += NTHREADS) ((uint4*)sDS)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tS = tmem, tG = tmem + 64, tE = tmem + 128, tY = tmem + 192;
+    const uint32_t tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(kv_full, 2 * C::KB);
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) {
+                tma_load_3d(sK + r * C::BK * 128, &tm_k, r * 64, k0, bh, kv_full);
+                tma_load_3d(sV + r * C::BK * 128, &tm_v, r * 64, k0, bh, kv_full);
+            }
+            int issued = 0;
+            for (int j = 0; j < nsub; j++) {
+                const int s = j % NS;
+                const int t0 = k0 + j * C::BQ;  // sub-chunk j covers queries [t0, t0 + 64)
+                if (j >= NS && !mbar_wait(&st_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&st_full[s], C::STAGE);
+                uint8_t* st = sSt + s * C::STAGE;
+#pragma unroll
+                for (int r = 0; r < D / 64; r++) {
+                    const int o = r * C::BQ * 128;
+                    tma_load_3d(st + o, &tm_q, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(st + C::SB + o, &tm_u, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(st + 2 * C::SB + o, &tm_dmu, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(st + 3 * C::SB + o, &tm_do, r * 64, t0, bh, &st_full[s]);
+                }
+                tma_load_3d(st + 4 * C::SB, &tm_rows, 0, t0, bh, &st_full[s]);
+                issued = j + 1;
+            }
+            mbar_wait_drain(kv_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&st_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_mma(128, C::BQ, false, false);  // scores: M keys, N 64 queries
+            const uint32_t idA = idesc_mma(128, D, false, true);       // dV, dK: A in TMEM, B MN-major
+            const uint32_t idQ = idesc_mma(128, D, true, true);        // dQ: A = ds MN-major, B = K MN-major
+            const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
+            if (mbar_wait(kv_full, 0, wd, 2)) {
+                for (int j = 0; j < nsub; j++) {
+                    const int s = j % NS;
+                    if (!mbar_wait(&st_full[s], (j / NS) & 1, wd, 3)) break;
+                    if (j > 0 && !mbar_wait(acc_done, (j - 1) & 1, wd, 4)) break;
+                    if (j > 0 && (j & 1) == 0 && !mbar_wait(dq_free, ((j >> 1) - 1) & 1, wd, 5)) break;
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(sSt + s * C::STAGE);
+                    const uint32_t aq = st, au = st + C::SB, am = st + 2 * C::SB, ado = st + 3 * C::SB;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) {
+                        const uint64_t dkk = desc_kmajor(kaddr, C::BK, kk);
+                        mma_ss(tS, dkk, desc_kmajor(aq, C::BQ, kk), idS, kk > 0);
+                        mma_ss(tG, dkk, desc_kmajor(au, C::BQ, kk), idS, kk > 0);
+                        mma_ss(tY, dkk, desc_kmajor(am, C::BQ, kk), idS, kk > 0);
+                        mma_ss(tE, desc_kmajor(vaddr, C::BK, kk), desc_kmajor(ado, C::BQ, kk), idS, kk > 0);
+                    }
+                    mma_commit(sc_full);
+                    if (!mbar_wait(op_full, j & 1, wd, 6)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::BQ / 16; kk++) {
+                        const uint32_t first = (j == 0 && kk == 0) ? 0u : 1u;
+                        mma_ts(tDV, tS + 16 * kk, desc_mnmajor(ado, C::BQ, kk), idA, first);
+                        mma_ts(tDK, tS + 16 * kk + 8, desc_mnmajor(au, C::BQ, kk), idA, first);
+                        mma_ts(tDK, tG + 16 * kk, desc_mnmajor(aq, C::BQ, kk), idA, 1u);
+                        mma_ts(tDK, tG + 16 * kk + 8, desc_mnmajor(am, C::BQ, kk), idA, 1u);
+                    }
+                    mma_commit(acc_done);
+                    mma_commit(&st_empty[s]);
+                    if ((j & 1) == 1 || j == nsub - 1) {
+#pragma unroll
+                        for (int kk = 0; kk < C::BK / 16; kk++)
+                            mma_ss(tDQ, desc_mnmajor(dsaddr, C::BK, kk), desc_mnmajor(kaddr, C::BK, kk), idQ, kk > 0);
+                        mma_commit(dq_full);
+                    }
+                }
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        const int qd = warp & 3;
+        const int i = qd * 32 + lane;  // key row (and, for dQ, query row) of this thread
+        const int key = k0 + i;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        bool ok = true;
+        for (int j = 0; j < nsub && ok; j++) {
+            const int s = j % NS;
+            const int t0 = k0 + j * C::BQ;
+            ok = mbar_wait(sc_full, j & 1, wd, 7);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float4* rows = (const float4*)(sSt + s * C::STAGE + 4 * C::SB);
+            uint8_t* dsrow = sDS + (j & 1) * (C::BK * 128) + i * 128;
+#pragma unroll 1
+            for (int c = 0; c < C::BQ / 16; c++) {
+                uint32_t vs[16], vg[16], ve[16], vy[16];
+                tmem_ld16(tS + lrow + 16 * c, vs);
+                tmem_ld16(tG + lrow + 16 * c, vg);
+                tmem_ld16(tE + lrow + 16 * c, ve);
+                tmem_ld16(tY + lrow + 16 * c, vy);
+                tmem_wait_ld();
+                uint32_t o1[16], o2[16];  // o1: a | dg, o2: ds | p (f16 pairs)
+#pragma unroll
+                for (int q2 = 0; q2 < 8; q2++) {
+                    float a[2], dg[2], ds[2], pp[2];
+#pragma unroll
+                    for (int hh = 0; hh < 2; hh++) {
+                        const int qq = 2 * q2 + hh;
+                        const int t = t0 + 16 * c + qq;
+                        const float4 rw = rows[16 * c + qq];  // {lse log2e, gbar, ebar, D}
+                        const float p = (key <= t && t < T)
+                                            ? fast_exp2(fmaf(__uint_as_float(vs[qq]), scale_log2, -rw.x))
+                                            : 0.f;
+                        const float g = __uint_as_float(vg[qq]);
+                        const float e = __uint_as_float(ve[qq]);
+                        const float y = __uint_as_float(vy[qq]);
+                        const float w1 = 1.f + g - rw.y;
+                        a[hh] = p * w1;
+                        dg[hh] = p * (e - rw.z);
+                        ds[hh] = scale * p * (fmaf(e, w1, -g * rw.z) + y - rw.w);
+                        pp[hh] = p;
+                    }
+                    o1[q2] = pack_f16(a[0], a[1]);
+                    o1[8 + q2] = pack_f16(dg[0], dg[1]);
+                    o2[q2] = pack_f16(ds[0], ds[1]);
+                    o2[8 + q2] = pack_f16(pp[0], pp[1]);
+                }
+                tmem_st16(tS + lrow + 16 * c, o1);
+                tmem_st16(tG + lrow + 16 * c, o2);
+                // ds row segment (16 queries = 32 bytes) into the swizzled
+                // [keys][queries] buffer: 16-byte chunks 2c and 2c + 1.
+                *(uint4*)(dsrow + (((2 * c) ^ (i & 7)) << 4)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                *(uint4*)(dsrow + (((2 * c + 1) ^ (i & 7)) << 4)) = make_uint4(o2[4], o2[5], o2[6], o2[7]);
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(op_full);
+            if ((j & 1) == 1 || j == nsub - 1) {
+                // dQ of the 128-query tile m = j / 2: thread = query row i
+                ok = mbar_wait(dq_full, (j >> 1) & 1, wd, 8);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int t = k0 + (j >> 1) * C::QT + i;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tDQ + lrow + 32 * c, v);
+                    tmem_wait_ld();
+                    if (t < T) {
+                        float* dst = dq_acc + ((size_t)bh * T + t) * D + 32 * c;
+#pragma unroll
+                        for (int x = 0; x < 32; x += 4)
+                            red_add_v4(dst + x, __uint_as_float(v[x]), __uint_as_float(v[x + 1]),
+                                       __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(dq_free);
+            }
+        }
+        if (ok) {
+            ok = mbar_wait(acc_done, (nsub - 1) & 1, wd, 9);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32], w[32];
+                    tmem_ld32(tDV + lrow + 32 * c, v);
+                    tmem_ld32(tDK + lrow + 32 * c, w);
+                    tmem_wait_ld();
+                    if (key < T) {
+                        const size_t off = ((size_t)bh * T + key) * D + 32 * c;
+                        uint4* pv = (uint4*)(dv + off);
+                        uint4* pk = (uint4*)(dk + off);
+#pragma unroll
+                        for (int x = 0; x < 4; x++) {
+                            pv[x] = make_uint4(pack_bf16(__uint_as_float(v[8 * x]), __uint_as_float(v[8 * x + 1])),
+                                               pack_bf16(__uint_as_float(v[8 * x + 2]), __uint_as_float(v[8 * x + 3])),
+                                               pack_bf16(__uint_as_float(v[8 * x + 4]), __uint_as_float(v[8 * x + 5])),
+                                               pack_bf16(__uint_as_float(v[8 * x + 6]), __uint_as_float(v[8 * x + 7])));
+                            pk[x] = make_uint4(pack_bf16(__uint_as_float(w[8 * x]), __uint_as_float(w[8 * x + 1])),
+                                               pack_bf16(__uint_as_float(w[8 * x + 2]), __uint_as_float(w[8 * x + 3])),
+                                               pack_bf16(__uint_as_float(w[8 * x + 4]), __uint_as_float(w[8 * x + 5])),
+                                               pack_bf16(__uint_as_float(w[8 * x + 6]), __uint_as_float(w[8 * x + 7])));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+__global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 x = src[i];
+        dst[i] = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    }
+}
+
 // ================================================================= host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -621,15 +1019,46 @@ TcFwdWs tc_fwd_ws(void* ws, int B, int H, int T, int d) {
     return w;
 }
 
-// Workspace of the tensor-core backward: the SIMT workspace (R, ebar and the
-// later stages' buffers) followed by f16 copies of q, k, v, dO.
+// Workspace of the tensor-core backward.
 struct TcBwdWs {
-    __half *q16, *k16, *v16, *do16;
+    float *R, *dq_acc, *ebar, *partial;
+    float4* rows;
+    __half *U, *dmu, *q16, *k16, *v16, *do16;
 };
 TcBwdWs tc_bwd_ws(void* ws, int B, int H, int T, int d) {
-    const size_t n = (size_t)B * H * T, nd2 = align256(n * d * 2);
-    char* p = (char*)ws + align256(simt_bwd_ws_bytes(B, H, T, d));
-    return TcBwdWs{(__half*)p, (__half*)(p + nd2), (__half*)(p + 2 * nd2), (__half*)(p + 3 * nd2)};
+    const size_t n = (size_t)B * H * T, nd4 = align256(n * d * 4), nd2 = align256(n * d * 2);
+    char* p = (char*)ws;
+    TcBwdWs w;
+    w.R = (float*)p; p += nd4;
+    w.dq_acc = (float*)p; p += nd4;
+    w.U = (__half*)p; p += nd2;
+    w.dmu = (__half*)p; p += nd2;
+    w.q16 = (__half*)p; p += nd2;
+    w.k16 = (__half*)p; p += nd2;
+    w.v16 = (__half*)p; p += nd2;
+    w.do16 = (__half*)p; p += nd2;
+    w.ebar = (float*)p; p += align256(n * 4);
+    w.rows = (float4*)p; p += align256(n * 16);
+    w.partial = (float*)p;
+    return w;
+}
+size_t tc_bwd_bytes(int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T;
+    return 2 * align256(n * d * 4) + 6 * align256(n * d * 2) + align256(n * 4) + align256(n * 16) +
+           simt_dp_partial_bytes(B, H, T, d);
+}
+
+// Row scalars [BH][T] float4 viewed as 3-D (4, T, BH), box 4 x 64 x 1.
+bool make_rows_map(CUtensorMap* m, const void* base, int T, int BH) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {4, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {16, (cuuint64_t)T * 16};
+    cuuint32_t box[3] = {4, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t to_f16(const void* const* src, __half* const* dst, int count, size_t n, cudaStream_t s) {
@@ -698,29 +1127,63 @@ cudaError_t fwd_impl(const FwdArgs& a) {
 template <int D>
 cudaError_t bwd_impl(const BwdArgs& a) {
     const int BH = a.B * a.H;
-    const float scale_log2 = LOG2E / sqrtf((float)D);
+    const float scale = 1.f / sqrtf((float)D);
+    const float scale_log2 = LOG2E * scale;
     const size_t n = (size_t)BH * a.T * D;
-    float *R = nullptr, *ebar = nullptr;
-    simt_bwd_ws_b1_outputs(a.ws, a.B, a.H, a.T, D, &R, &ebar);
     TcBwdWs w = tc_bwd_ws(a.ws, a.B, a.H, a.T, D);
-    CUtensorMap mq128, mdo128, mk64, mv64;
+    CUtensorMap mq128, mdo128, mk64, mv64, mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows;
     if (!make_map(&mq128, w.q16, D, a.T, BH, 128) || !make_map(&mdo128, w.do16, D, a.T, BH, 128) ||
-        !make_map(&mk64, w.k16, D, a.T, BH, 64) || !make_map(&mv64, w.v16, D, a.T, BH, 64))
+        !make_map(&mk64, w.k16, D, a.T, BH, 64) || !make_map(&mv64, w.v16, D, a.T, BH, 64) ||
+        !make_map(&mk128, w.k16, D, a.T, BH, 128) || !make_map(&mv128, w.v16, D, a.T, BH, 128) ||
+        !make_map(&mq64, w.q16, D, a.T, BH, 64) || !make_map(&mu64, w.U, D, a.T, BH, 64) ||
+        !make_map(&mdmu64, w.dmu, D, a.T, BH, 64) || !make_map(&mdo64, w.do16, D, a.T, BH, 64) ||
+        !make_rows_map(&mrows, w.rows, a.T, BH))
         return cudaErrorInvalidValue;
     {
         const void* src[4] = {a.q, a.k, a.v, a.dout};
         __half* dst[4] = {w.q16, w.k16, w.v16, w.do16};
         PLX_TRY(to_f16(src, dst, 4, n, a.stream));
     }
-    using C = DualCfg<D>;
-    const int ntq = (a.T + C::BM - 1) / C::BM;
-    PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-    timing_begin(a.stream, "tc_bwd_b1");
-    tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr, R, ebar,
-                                                              a.T, BH, ntq, scale_log2, a.status);
-    timing_end(a.stream);
-    PLX_TRY(cudaGetLastError());
-    return simt_bwd_after_b1(a);
+    {  // B1: R = sum p e k, ebar = sum p e
+        using C = DualCfg<D>;
+        const int ntq = (a.T + C::BM - 1) / C::BM;
+        PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_bwd_b1");
+        tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr, w.R,
+                                                                  w.ebar, a.T, BH, ntq, scale_log2, a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    {  // B2: row math
+        const size_t sm = sizeof(float) * (D * (D + 1) + 8 * D);
+        PLX_TRY(cudaFuncSetAttribute(tc_bwd_b2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        const dim3 grid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
+        timing_begin(a.stream, "tc_bwd_b2");
+        tc_bwd_b2<D><<<grid, 256, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U,
+                                                  w.dmu, w.dq_acc, w.rows, a.B, a.H, a.T, PROJ_ROWS);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    PLX_TRY(simt_dP(a.q, a.mu_k, w.R, w.partial, a.dP, a.B, a.H, a.T, D, a.dtype, a.stream));
+    {  // B3: dK, dV, dQ
+        using C = B3Cfg<D>;
+        const int nkt = (a.T + C::BK - 1) / C::BK;
+        PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_bwd_b3");
+        tc_bwd_b3<D><<<nkt * BH, NTHREADS, C::SMEM, a.stream>>>(
+            mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows, w.dq_acc, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
+            a.T, BH, nkt, scale, scale_log2, a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    }
+    {
+        const size_t n4 = n / 4;
+        const unsigned gx = (unsigned)std::min<size_t>((n4 + 255) / 256, 148 * 8);
+        timing_begin(a.stream, "tc_cast_dq");
+        tc_cast_dq<<<gx, 256, 0, a.stream>>>((const float4*)w.dq_acc, (uint2*)a.dq, n4);
+        timing_end(a.stream);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -732,10 +1195,7 @@ size_t tc_fwd_ws_bytes(int B, int H, int T, int d) {
     return 4 * align256(n * d * 2) + align256(n * 4);
 }
 
-size_t tc_bwd_ws_bytes(int B, int H, int T, int d) {
-    const size_t n = (size_t)B * H * T;
-    return align256(simt_bwd_ws_bytes(B, H, T, d)) + 4 * align256(n * d * 2);
-}
+size_t tc_bwd_ws_bytes(int B, int H, int T, int d) { return tc_bwd_bytes(B, H, T, d); }
 
 cudaError_t tc_fwd(const FwdArgs& a) {
     if (a.dtype != 1) return cudaErrorNotSupported;
