@@ -54,6 +54,20 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
+// Launch order of (tile, head) work items: heads in groups of kHeadGroup, and
+// within a group the longest tiles first (rank 0 = most work).  CTAs that run
+// at the same time then share a few heads' K/V (and dQ rows) in L2 instead of
+// streaming every head's, while the causal triangle still starts heavy-first.
+constexpr int kHeadGroup = 8;
+__device__ __forceinline__ void work_item(int item, int BH, int ntiles, int* rank, int* bh) {
+    const int per_group = kHeadGroup * ntiles;
+    const int g = item / per_group;
+    const int gsize = min(kHeadGroup, BH - g * kHeadGroup);
+    const int r = item - g * per_group;
+    *rank = r / gsize;
+    *bh = g * kHeadGroup + r % gsize;
+}
+
 // ================================================================ pass 1
 template <int D>
 struct P1 {
@@ -89,9 +103,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     volatile int* abortf = (volatile int*)(holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item = blockIdx.x;
-    const int qt = ntq - 1 - item / BH;  // longest rows first
-    const int bh = item % BH;
+    int rank, bh;
+    work_item(blockIdx.x, BH, ntq, &rank, &bh);
+    const int qt = ntq - 1 - rank;  // longest rows first
     const int q0 = qt * C::BM;
     const int nkt = min(qt, (T - 1) / C::BN) + 1;
     const Watchdog wd{status, abortf, KID_TC_PASS1};
@@ -273,58 +287,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
-// ============================================================ projection
-// u = P_h (q - mu_k) in fp32, stored as f16 (the MMA operand of pass 2), and
-// gbar = mu_k . u computed from the stored (rounded) u, so that
-// sum_i p_i (g_i - gbar) vanishes for the values the MMA sees.
-template <int D>
-__global__ void __launch_bounds__(256) tc_proj(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mu_k,
-                                               const float* __restrict__ P, __half* __restrict__ U,
-                                               float* __restrict__ gbar, int B, int H, int T, int rows_per_cta) {
-    extern __shared__ float psm[];
-    constexpr int LD = D + 1, NA = D / 32;
-    float* PT = psm;          // PT[b][a] = P[a][b]
-    float* dl = PT + D * LD;  // per-warp delta buffer
-    const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float* Ph = P + (size_t)h * D * D;
-    for (int e = threadIdx.x; e < D * D; e += 256) PT[(e % D) * LD + e / D] = Ph[e];
-    __syncthreads();
-    float* dw = dl + warp * D;
-    const int r_begin = blockIdx.x * rows_per_cta;
-    const int r_end = min(r_begin + rows_per_cta, B * T);
-    for (int r = r_begin + warp; r < r_end; r += 8) {
-        const int b = r / T, t = r % T;
-        const size_t row = ((size_t)b * H + h) * T + t;
-        float mk[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) {
-            const int a = lane + 32 * j;
-            mk[j] = mu_k[row * D + a];
-            dw[a] = __bfloat162float(q[row * D + a]) - mk[j];
-        }
-        __syncwarp();
-        float u[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) u[j] = 0.f;
-        for (int bb = 0; bb < D; bb++) {
-            const float db = dw[bb];
-#pragma unroll
-            for (int j = 0; j < NA; j++) u[j] = fmaf(PT[bb * LD + lane + 32 * j], db, u[j]);
-        }
-        float g = 0.f;
-#pragma unroll
-        for (int j = 0; j < NA; j++) {
-            const __half uh = __float2half_rn(u[j]);
-            U[row * D + lane + 32 * j] = uh;
-            g = fmaf(mk[j], __half2float(uh), g);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
-        if (lane == 0) gbar[row] = g;
-        __syncwarp();
-    }
-}
-
 // ====================================================== f16 operand copies
 // The MMAs take f16 operands: a bf16 input converts to f16 exactly when its
 // magnitude lies in f16's normal range (larger magnitudes saturate to the
@@ -384,9 +346,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     volatile int* abortf = (volatile int*)(holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item = blockIdx.x;
-    const int qt = ntq - 1 - item / BH;
-    const int bh = item % BH;
+    int rank, bh;
+    work_item(blockIdx.x, BH, ntq, &rank, &bh);
+    const int qt = ntq - 1 - rank;
     const int q0 = qt * C::BM;
     const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
     const Watchdog wd{status, abortf, MODE == 0 ? (unsigned)KID_TC_PASS2 : (unsigned)KID_TC_BWD_B1};
@@ -562,122 +524,292 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
-// ============================================================ backward B2
-// Per row: delta = q - mu_k, u = P_h delta (fp32), U = f16(u), du = R - ebar mu_k
-// (overwrites R), ddelta = P_h^T du, dq_acc = ddelta, dmu = -ddelta (f16),
-// and the row scalars B3 needs, packed {lse log2 e, mu_k . U, ebar, D} with
-//   D = do.o - gbar ebar + mu_k . dmu,  do.o = ebar + R.u - gbar ebar
-// (do.o rebuilt from B1's fp32 sums; gbar = mu_k . u in fp32 here, while the
-// packed mu_k . U matches the f16 U that B3's G = K U^T sees).
+// ============================================================= row math
+// Per-row work around the attention passes, as register-tiled fp32 products
+// over blocks of 64 rows of one head (rows = the B*T queries of head h):
+//   MODE 0 (forward projection): u = P_h (q - mu_k), U = f16(u),
+//          gbar = mu_k . U (from the rounded U, so that sum_i p_i (g_i - gbar)
+//          vanishes for the values pass 2's MMA sees).
+//   MODE 1 (backward B2): the same u, du = R - ebar mu_k, ddelta = P_h^T du,
+//          dq_acc = ddelta, dmu = f16(-ddelta), the row scalars B3 needs
+//          {lse log2 e, 1 - mu_k . U, ebar, D} with
+//          D = do.o - gbar ebar + mu_k . dmu and do.o = ebar + R.u - gbar ebar
+//          (rebuilt from B1's fp32 sums, gbar = mu_k . u in fp32), and this
+//          CTA's partial dP_h = sum_rows du delta^T.
+// Thread (ty, tx) of 16 x 16 owns rows 4ty..4ty+3 and columns NC tx..NC tx+NC-1.
 template <int D>
-__global__ void __launch_bounds__(256) tc_bwd_b2(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mu_k,
-                                                 const float* __restrict__ P, const float* __restrict__ lse,
-                                                 float* __restrict__ R, const float* __restrict__ ebar,
-                                                 __half* __restrict__ U, __half* __restrict__ dmu,
-                                                 float* __restrict__ dq_acc, float4* __restrict__ rowpack, int B,
-                                                 int H, int T, int rows_per_cta) {
-    extern __shared__ float psm[];
-    constexpr int LD = D + 1, NA = D / 32;
-    float* PT = psm;           // PT[b][a] = P[a][b]
-    float* buf = PT + D * LD;  // per-warp [D]
-    const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float* Ph = P + (size_t)h * D * D;
-    for (int e = threadIdx.x; e < D * D; e += 256) PT[(e % D) * LD + e / D] = Ph[e];
-    __syncthreads();
-    float* w = buf + warp * D;
-    const int r_begin = blockIdx.x * rows_per_cta;
-    const int r_end = min(r_begin + rows_per_cta, B * T);
-    for (int r = r_begin + warp; r < r_end; r += 8) {
-        const int b = r / T, t = r % T;
-        const size_t row = ((size_t)b * H + h) * T + t;
-        float mk[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) {
-            const int a = lane + 32 * j;
-            mk[j] = mu_k[row * D + a];
-            w[a] = __bfloat162float(q[row * D + a]) - mk[j];
-        }
-        __syncwarp();
-        float u[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) u[j] = 0.f;
-        for (int bb = 0; bb < D; bb++) {
-            const float db = w[bb];
-#pragma unroll
-            for (int j = 0; j < NA; j++) u[j] = fmaf(PT[bb * LD + lane + 32 * j], db, u[j]);
-        }
-        const float eb = ebar[row];
-        float g = 0.f, gr = 0.f, ru = 0.f, du[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) {
-            const int a = lane + 32 * j;
-            const float rr = R[row * D + a];
-            const __half uh = __float2half_rn(u[j]);
-            g = fmaf(mk[j], u[j], g);
-            gr = fmaf(mk[j], __half2float(uh), gr);
-            ru = fmaf(rr, u[j], ru);
-            du[j] = rr - eb * mk[j];
-            U[row * D + a] = uh;
-            R[row * D + a] = du[j];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xffffffffu, g, o);
-            gr += __shfl_xor_sync(0xffffffffu, gr, o);
-            ru += __shfl_xor_sync(0xffffffffu, ru, o);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < NA; j++) w[lane + 32 * j] = du[j];
-        __syncwarp();
-        float dd[NA];
-#pragma unroll
-        for (int j = 0; j < NA; j++) dd[j] = 0.f;
-        for (int a = 0; a < D; a++) {
-            const float da = w[a];
-#pragma unroll
-            for (int j = 0; j < NA; j++) dd[j] = fmaf(PT[(lane + 32 * j) * LD + a], da, dd[j]);
-        }
-        float x = 0.f;
-#pragma unroll
-        for (int j = 0; j < NA; j++) {
-            const int a = lane + 32 * j;
-            dq_acc[row * D + a] = dd[j];
-            dmu[row * D + a] = __float2half_rn(-dd[j]);
-            x = fmaf(mk[j], -dd[j], x);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) {
-            const float doo = eb + ru - g * eb;
-            rowpack[row] = make_float4(lse[row] * LOG2E, gr, eb, doo - g * eb + x);
-        }
-        __syncwarp();
+struct RowCfg {
+    static constexpr int RB = 64, NT = 256;
+    static constexpr int LDT = RB + 4;  // stride of the transposed row tiles
+    static constexpr int LDP = D + 4;   // stride of the P tiles
+    static constexpr int NC = D / 16;   // output columns per thread
+    static constexpr int NA = D / 16;   // dP rows (a) per thread
+    static constexpr int ROWS_PER_CTA = 512;
+    static constexpr int CPT = D / 4;  // columns per thread in the load phase (4 threads per row)
+    // mu_k is kept row-major in shared memory unless that would not fit
+    static constexpr bool mu_in_smem(int mode) { return D == 64 || mode == 0; }
+    static constexpr size_t smem(int mode) {
+        return sizeof(float) * ((mode ? 2 : 1) * (size_t)D * LDP + (mode ? 2 : 1) * (size_t)D * LDT +
+                                (mu_in_smem(mode) ? (size_t)RB * LDP : 0));
     }
+};
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mu_k,
+                                               const float* __restrict__ P, const float* __restrict__ lse,
+                                               const float* __restrict__ R, const float* __restrict__ ebar,
+                                               __half* __restrict__ U, float* __restrict__ gbar,
+                                               __half* __restrict__ dmu, float* __restrict__ dq_acc,
+                                               float4* __restrict__ rowpack, float* __restrict__ dp_partial,
+                                               int B, int H, int T) {
+    using C = RowCfg<D>;
+    constexpr int NC = C::NC, NA = C::NA, LDT = C::LDT, LDP = C::LDP, RB = C::RB;
+    extern __shared__ float rsm[];
+    float* PT = rsm;                                    // PT[b][a] = P[a][b]
+    float* PM = PT + D * LDP;                           // PM[a][b] = P[a][b]      (MODE 1)
+    float* XT = MODE ? PM + D * LDP : PT + D * LDP;     // XT[b][r] = delta[r][b]
+    float* YT = XT + D * LDT;                           // YT[a][r] = du[r][a]     (MODE 1)
+    float* MS = MODE ? YT + D * LDT : YT;               // MS[r][c] = mu_k (when it fits)
+    constexpr bool kMu = C::mu_in_smem(MODE);
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int h = blockIdx.y;
+    const float* Ph = P + (size_t)h * D * D;
+    for (int e = tid; e < D * D; e += C::NT) {
+        const float v = Ph[e];
+        PT[(e % D) * LDP + e / D] = v;
+        if (MODE) PM[(e / D) * LDP + e % D] = v;
+    }
+    const int nrows = B * T;
+    const int r_begin = blockIdx.x * C::ROWS_PER_CTA;
+    const int r_end = min(r_begin + C::ROWS_PER_CTA, nrows);
+    float dp[NA][NA];
+#pragma unroll
+    for (int i = 0; i < NA; i++)
+#pragma unroll
+        for (int j = 0; j < NA; j++) dp[i][j] = 0.f;
+
+    for (int r0 = r_begin; r0 < r_end; r0 += RB) {
+        __syncthreads();
+        {
+            // 4 threads per row, CPT consecutive columns each, vector loads
+            constexpr int CPT = C::CPT;
+            const int rr = tid >> 2, c0 = (tid & 3) * CPT, r = r0 + rr;
+            if (r < r_end) {
+                const size_t base = (((size_t)(r / T) * H + h) * T + r % T) * D + c0;
+                const float eb = MODE ? ebar[base / D] : 0.f;
+#pragma unroll
+                for (int k = 0; k < CPT; k += 8) {
+                    const uint4 qv = *(const uint4*)&q[base + k];
+                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                    float m[8], rv[8];
+                    *(float4*)&m[0] = *(const float4*)&mu_k[base + k];
+                    *(float4*)&m[4] = *(const float4*)&mu_k[base + k + 4];
+                    if (MODE) {
+                        *(float4*)&rv[0] = *(const float4*)&R[base + k];
+                        *(float4*)&rv[4] = *(const float4*)&R[base + k + 4];
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; x++) {
+                        const float qf = (x & 1) ? bf16_hi(qw[x >> 1]) : bf16_lo(qw[x >> 1]);
+                        XT[(c0 + k + x) * LDT + rr] = qf - m[x];
+                        if (MODE) YT[(c0 + k + x) * LDT + rr] = rv[x] - eb * m[x];
+                    }
+                    if (kMu) {
+                        *(float4*)&MS[rr * LDP + c0 + k] = *(float4*)&m[0];
+                        *(float4*)&MS[rr * LDP + c0 + k + 4] = *(float4*)&m[4];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < CPT; k++) {
+                    XT[(c0 + k) * LDT + rr] = 0.f;
+                    if (MODE) YT[(c0 + k) * LDT + rr] = 0.f;
+                }
+            }
+        }
+        __syncthreads();
+        // u = P delta for the thread's 4 rows x NC columns
+        float u[4][NC];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < NC; j++) u[i][j] = 0.f;
+#pragma unroll 4
+        for (int b = 0; b < D; b++) {
+            const float4 x = *(const float4*)&XT[b * LDT + 4 * ty];
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+            float pv[NC];
+#pragma unroll
+            for (int j = 0; j < NC; j += 4) *(float4*)&pv[j] = *(const float4*)&PT[b * LDP + NC * tx + j];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < NC; j++) u[i][j] = fmaf(xs[i], pv[j], u[i][j]);
+        }
+        float dd[4][NC];
+        if (MODE) {
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < NC; j++) dd[i][j] = 0.f;
+#pragma unroll 4
+            for (int a = 0; a < D; a++) {
+                const float4 y = *(const float4*)&YT[a * LDT + 4 * ty];
+                const float ys[4] = {y.x, y.y, y.z, y.w};
+                float pv[NC];
+#pragma unroll
+                for (int j = 0; j < NC; j += 4) *(float4*)&pv[j] = *(const float4*)&PM[a * LDP + NC * tx + j];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int j = 0; j < NC; j++) dd[i][j] = fmaf(ys[i], pv[j], dd[i][j]);
+            }
+        }
+        // per-row outputs
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int r = r0 + 4 * ty + i;
+            const bool valid = r < r_end;
+            const size_t row = valid ? ((size_t)(r / T) * H + h) * T + r % T : 0;
+            const size_t off = row * D + NC * tx;
+            float m[NC], rr_[NC];
+            float gr = 0.f, gb = 0.f, ru = 0.f, xx = 0.f;
+            uint32_t uh[NC / 2];
+#pragma unroll
+            for (int j = 0; j < NC; j += 2) uh[j / 2] = pack_f16(u[i][j], u[i][j + 1]);
+            if (valid) {
+#pragma unroll
+                for (int j = 0; j < NC; j += 4)
+                    *(float4*)&m[j] = kMu ? *(const float4*)&MS[(4 * ty + i) * LDP + NC * tx + j]
+                                          : *(const float4*)&mu_k[off + j];
+                if (MODE) {
+#pragma unroll
+                    for (int j = 0; j < NC; j += 4) *(float4*)&rr_[j] = *(const float4*)&R[off + j];
+                }
+#pragma unroll
+                for (int j = 0; j < NC; j += 2) {
+                    gr = fmaf(m[j], f16_lo(uh[j / 2]), gr);
+                    gr = fmaf(m[j + 1], f16_hi(uh[j / 2]), gr);
+                }
+                if (MODE) {
+#pragma unroll
+                    for (int j = 0; j < NC; j++) {
+                        gb = fmaf(m[j], u[i][j], gb);
+                        ru = fmaf(rr_[j], u[i][j], ru);
+                        xx = fmaf(m[j], -dd[i][j], xx);
+                    }
+                }
+                if (NC == 4)
+                    *(uint2*)&U[off] = make_uint2(uh[0], uh[1]);
+                else
+                    *(uint4*)&U[off] = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+                if (MODE) {
+                    uint32_t mh[NC / 2];
+#pragma unroll
+                    for (int j = 0; j < NC; j += 2) mh[j / 2] = pack_f16(-dd[i][j], -dd[i][j + 1]);
+                    if (NC == 4)
+                        *(uint2*)&dmu[off] = make_uint2(mh[0], mh[1]);
+                    else
+                        *(uint4*)&dmu[off] = make_uint4(mh[0], mh[1], mh[2], mh[3]);
+#pragma unroll
+                    for (int j = 0; j < NC; j += 4)
+                        *(float4*)&dq_acc[off + j] = make_float4(dd[i][j], dd[i][j + 1], dd[i][j + 2], dd[i][j + 3]);
+                }
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                gr += __shfl_xor_sync(0xffffffffu, gr, o);
+                if (MODE) {
+                    gb += __shfl_xor_sync(0xffffffffu, gb, o);
+                    ru += __shfl_xor_sync(0xffffffffu, ru, o);
+                    xx += __shfl_xor_sync(0xffffffffu, xx, o);
+                }
+            }
+            if (valid && tx == 0) {
+                if (MODE == 0) {
+                    gbar[row] = gr;
+                } else {
+                    const float eb = ebar[row];
+                    const float doo = eb + ru - gb * eb;
+                    rowpack[row] = make_float4(lse[row] * LOG2E, 1.f - gr, eb, doo - gb * eb + xx);
+                }
+            }
+        }
+        if (MODE) {
+            // dP_h partial: dp[a][b] += sum over the block's rows du[r][a] delta[r][b],
+            // a in NA ty + [0, NA), b in NA tx + [0, NA)
+#pragma unroll 2
+            for (int r = 0; r < RB; r += 4) {
+                float4 ya[NA], xb[NA];
+#pragma unroll
+                for (int ii = 0; ii < NA; ii++) ya[ii] = *(const float4*)&YT[(NA * ty + ii) * LDT + r];
+#pragma unroll
+                for (int jj = 0; jj < NA; jj++) xb[jj] = *(const float4*)&XT[(NA * tx + jj) * LDT + r];
+#pragma unroll
+                for (int ii = 0; ii < NA; ii++)
+#pragma unroll
+                    for (int jj = 0; jj < NA; jj++)
+                        dp[ii][jj] = fmaf(ya[ii].x, xb[jj].x,
+                                          fmaf(ya[ii].y, xb[jj].y,
+                                               fmaf(ya[ii].z, xb[jj].z, fmaf(ya[ii].w, xb[jj].w, dp[ii][jj]))));
+            }
+        }
+    }
+    if (MODE) {
+        float* dst = dp_partial + ((size_t)h * gridDim.x + blockIdx.x) * D * D;
+#pragma unroll
+        for (int ii = 0; ii < NA; ii++)
+#pragma unroll
+            for (int jj = 0; jj < NA; jj += 4)
+                *(float4*)&dst[(NA * ty + ii) * D + NA * tx + jj] =
+                    make_float4(dp[ii][jj], dp[ii][jj + 1], dp[ii][jj + 2], dp[ii][jj + 3]);
+    }
+}
+
+// dP[h] = sum of the CTA partials in chunk order (fixed order: reproducible).
+__global__ void __launch_bounds__(256) tc_dp_reduce(const float4* __restrict__ partial, float4* __restrict__ dP,
+                                                    int nchunks, int dd4) {
+    const int h = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= dd4) return;
+    const float4* src = partial + (size_t)h * nchunks * dd4 + e;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < nchunks; c++) {
+        const float4 v = src[(size_t)c * dd4];
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+    }
+    dP[(size_t)h * dd4 + e] = s;
 }
 
 // ============================================================ backward B3
 // CTA = one tile of 128 keys of one head; queries stream in sub-chunks of 64.
 // Per sub-chunk (TMEM lanes = keys i, columns = queries t):
-//   S^T = K Q^T, G^T = K U^T, Y^T = K dmu^T, E^T = V dO^T
+//   [S^T | G^T | Y^T] = K [Q | U | dmu]^T   (one N = 192 MMA: K is read once)
+//   E^T = V dO^T
 //   p = exp(c s - lse_t), w1 = 1 + g - gbar_t, a = p w1, dg = p (e - ebar_t),
 //   ds = c p (e w1 - g ebar_t + y - D_t)
 //   dV += a dO, dK += dg U + ds Q + p dmu      (A operands f16 in TMEM)
 // and per 128 queries dQ += ds^T K (A = ds from shared memory), added into the
-// fp32 dq accumulator with vector reductions.
+// fp32 dq accumulator with vector reductions.  Two warpgroups split the
+// elementwise work by query columns.
 template <int D>
 struct B3Cfg {
     static constexpr int BK = 128, BQ = 64, QT = 128;
+    static constexpr int NT = 320;              // TMA warp, MMA warp, 2 x 4 elementwise warps
     static constexpr int NS = D == 64 ? 2 : 1;  // sub-chunk stages
     static constexpr int KB = BK * D * 2;       // K or V tile
-    static constexpr int SB = BQ * D * 2;       // one 64-row operand sub-tile
-    static constexpr int RB = BQ * 16;          // row scalars of a sub-chunk
-    static constexpr int STAGE = 4 * SB + RB;   // Q, U, dmu, dO, rows
+    static constexpr int QUM_B = 3 * BQ * 128;  // one 64-column block of the stacked [Q|U|dmu] rows
+    static constexpr int DO_OFF = (D / 64) * QUM_B;
+    static constexpr int ROWS_OFF = DO_OFF + BQ * D * 2;
+    static constexpr int STAGE = ROWS_OFF + BQ * 16;
     static constexpr int DSB = BK * QT * 2;     // ds, f16 [keys][128 queries]
     static constexpr int NBAR = 1 + 2 * NS + 6;
     static constexpr int SMEM = 1024 + 2 * KB + DSB + NS * STAGE + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 512;
-    // TMEM columns: S^T [0,64), G^T [64,128), E^T [128,192), Y^T [192,256),
+    // TMEM columns: S^T [0,64), G^T [64,128), Y^T [128,192), E^T [192,256),
     // dV [256, 256+D), dK [256+D, 256+2D); dQ reuses [128, 128+D).
 };
 
@@ -686,8 +818,44 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
+// MN-major operand descriptor with an explicit leading (N-block) byte offset.
+__device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t lbo) {
+    return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
+}
+
+// The elementwise step for 16 queries (one 16-column chunk) of one key row.
+template <bool MASK>
+__device__ __forceinline__ void b3_chunk(const uint32_t (&vs)[16], const uint32_t (&vg)[16], const uint32_t (&vy)[16],
+                                         const uint32_t (&ve)[16], const float4* rows, int qlo, float scale,
+                                         float scale_log2, uint32_t (&o1)[16], uint32_t (&o2)[16]) {
+    // rows[qq] = {lse_t log2 e, 1 - gbar_t, ebar_t, D_t}; query qq valid iff qq >= qlo (MASK only)
+#pragma unroll
+    for (int q2 = 0; q2 < 8; q2++) {
+        float a[2], dg[2], ds[2], pp[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const int qq = 2 * q2 + hh;
+            const float4 rw = rows[qq];
+            float p = fast_exp2(fmaf(__uint_as_float(vs[qq]), scale_log2, -rw.x));
+            if (MASK && qq < qlo) p = 0.f;
+            const float g = __uint_as_float(vg[qq]);
+            const float e = __uint_as_float(ve[qq]);
+            const float y = __uint_as_float(vy[qq]);
+            const float w1 = g + rw.y;
+            a[hh] = p * w1;
+            dg[hh] = p * (e - rw.z);
+            ds[hh] = (p * scale) * fmaf(e, w1, fmaf(-g, rw.z, y - rw.w));
+            pp[hh] = p;
+        }
+        o1[q2] = pack_f16(a[0], a[1]);
+        o1[8 + q2] = pack_f16(dg[0], dg[1]);
+        o2[q2] = pack_f16(ds[0], ds[1]);
+        o2[8 + q2] = pack_f16(pp[0], pp[1]);
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
     tc_bwd_b3(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
               const __grid_constant__ CUtensorMap tm_dmu, const __grid_constant__ CUtensorMap tm_do,
@@ -701,7 +869,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* sK = sm;
     uint8_t* sV = sK + C::KB;
     uint8_t* sDS = sV + C::KB;
-    uint8_t* sSt = sDS + C::DSB;  // stage s: Q, U, dmu, dO sub-tiles, then the row scalars
+    uint8_t* sSt = sDS + C::DSB;  // stage s: [Q|U|dmu] blocks, dO, row scalars
     uint64_t* bars = (uint64_t*)(sSt + NS * C::STAGE);
     uint64_t* kv_full = bars;
     uint64_t* st_full = bars + 1;
@@ -716,8 +884,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     volatile int* abortf = (volatile int*)(holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt = blockIdx.x / BH;  // tiles with the most queries first
-    const int bh = blockIdx.x % BH;
+    int kt, bh;
+    work_item(blockIdx.x, BH, nkt, &kt, &bh);  // key tiles with the most queries first
     const int k0 = kt * C::BK;
     // sub-chunk j covers queries [k0 + 64 j, k0 + 64 j + 64); pairs j = 2m, 2m + 1
     // form the m-th 128-query tile of the dQ product
@@ -732,23 +900,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&st_empty[s], 1);
         }
         mbar_init(sc_full, 1);
-        mbar_init(op_full, 128);
+        mbar_init(op_full, 256);
         mbar_init(acc_done, 1);
         mbar_init(dq_full, 1);
-        mbar_init(dq_free, 128);
+        mbar_init(dq_free, 256);
         mbar_init(drain, 1);
         fence_barrier_init();
     }
     // ds buffer starts at zero: a query tile cut by T leaves its upper half
-    // unwritten, and the dQ MMA must not read stale or uninitialised bits.
-    for (int i = threadIdx.x; i < C::DSB / 16; i += NTHREADS) ((uint4*)sDS)[i] = make_uint4(0, 0, 0, 0);
+    // unwritten, and the dQ MMA must not read uninitialised bits.
+    for (int i = threadIdx.x; i < C::DSB / 16; i += C::NT) ((uint4*)sDS)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
-    const uint32_t tS = tmem, tG = tmem + 64, tE = tmem + 128, tY = tmem + 192;
+    const uint32_t tS = tmem, tG = tmem + 64, tY = tmem + 128, tE = tmem + 192;
     const uint32_t tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 128;
 
     if (warp == 0) {
@@ -762,19 +930,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int issued = 0;
             for (int j = 0; j < nsub; j++) {
                 const int s = j % NS;
-                const int t0 = k0 + j * C::BQ;  // sub-chunk j covers queries [t0, t0 + 64)
+                const int t0 = k0 + j * C::BQ;
                 if (j >= NS && !mbar_wait(&st_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
                 mbar_expect_tx(&st_full[s], C::STAGE);
                 uint8_t* st = sSt + s * C::STAGE;
 #pragma unroll
                 for (int r = 0; r < D / 64; r++) {
-                    const int o = r * C::BQ * 128;
-                    tma_load_3d(st + o, &tm_q, r * 64, t0, bh, &st_full[s]);
-                    tma_load_3d(st + C::SB + o, &tm_u, r * 64, t0, bh, &st_full[s]);
-                    tma_load_3d(st + 2 * C::SB + o, &tm_dmu, r * 64, t0, bh, &st_full[s]);
-                    tma_load_3d(st + 3 * C::SB + o, &tm_do, r * 64, t0, bh, &st_full[s]);
+                    uint8_t* blk = st + r * C::QUM_B;
+                    tma_load_3d(blk, &tm_q, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(blk + C::BQ * 128, &tm_u, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(blk + 2 * C::BQ * 128, &tm_dmu, r * 64, t0, bh, &st_full[s]);
+                    tma_load_3d(st + C::DO_OFF + r * C::BQ * 128, &tm_do, r * 64, t0, bh, &st_full[s]);
                 }
-                tma_load_3d(st + 4 * C::SB, &tm_rows, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0, bh, &st_full[s]);
                 issued = j + 1;
             }
             mbar_wait_drain(kv_full, 0);
@@ -782,9 +950,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idS = idesc_mma(128, C::BQ, false, false);  // scores: M keys, N 64 queries
-            const uint32_t idA = idesc_mma(128, D, false, true);       // dV, dK: A in TMEM, B MN-major
-            const uint32_t idQ = idesc_mma(128, D, true, true);        // dQ: A = ds MN-major, B = K MN-major
+            const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T: N = 192 queries x3
+            const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
+            const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK: A in TMEM, B MN-major
+            const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ: A = ds MN-major, B = K MN-major
             const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
             if (mbar_wait(kv_full, 0, wd, 2)) {
                 for (int j = 0; j < nsub; j++) {
@@ -794,13 +963,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (j > 0 && (j & 1) == 0 && !mbar_wait(dq_free, ((j >> 1) - 1) & 1, wd, 5)) break;
                     tc_fence_after();
                     const uint32_t st = smem_u32(sSt + s * C::STAGE);
-                    const uint32_t aq = st, au = st + C::SB, am = st + 2 * C::SB, ado = st + 3 * C::SB;
+                    const uint32_t ado = st + C::DO_OFF;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) {
-                        const uint64_t dkk = desc_kmajor(kaddr, C::BK, kk);
-                        mma_ss(tS, dkk, desc_kmajor(aq, C::BQ, kk), idS, kk > 0);
-                        mma_ss(tG, dkk, desc_kmajor(au, C::BQ, kk), idS, kk > 0);
-                        mma_ss(tY, dkk, desc_kmajor(am, C::BQ, kk), idS, kk > 0);
+                        mma_ss(tS, desc_kmajor(kaddr, C::BK, kk), desc_kmajor(st, 3 * C::BQ, kk), idS3, kk > 0);
                         mma_ss(tE, desc_kmajor(vaddr, C::BK, kk), desc_kmajor(ado, C::BQ, kk), idS, kk > 0);
                     }
                     mma_commit(sc_full);
@@ -809,10 +975,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < C::BQ / 16; kk++) {
                         const uint32_t first = (j == 0 && kk == 0) ? 0u : 1u;
-                        mma_ts(tDV, tS + 16 * kk, desc_mnmajor(ado, C::BQ, kk), idA, first);
-                        mma_ts(tDK, tS + 16 * kk + 8, desc_mnmajor(au, C::BQ, kk), idA, first);
-                        mma_ts(tDK, tG + 16 * kk, desc_mnmajor(aq, C::BQ, kk), idA, 1u);
-                        mma_ts(tDK, tG + 16 * kk + 8, desc_mnmajor(am, C::BQ, kk), idA, 1u);
+                        mma_ts(tDV, tS + 16 * kk, desc_mn_lbo(ado, kk, C::BQ * 128), idA, first);
+                        mma_ts(tDK, tS + 16 * kk + 8, desc_mn_lbo(st + C::BQ * 128, kk, C::QUM_B), idA, first);
+                        mma_ts(tDK, tG + 16 * kk, desc_mn_lbo(st, kk, C::QUM_B), idA, 1u);
+                        mma_ts(tDK, tG + 16 * kk + 8, desc_mn_lbo(st + 2 * C::BQ * 128, kk, C::QUM_B), idA, 1u);
                     }
                     mma_commit(acc_done);
                     mma_commit(&st_empty[s]);
@@ -828,6 +994,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_wait_drain(drain, 0);
         }
     } else {
+        const int wg = (warp - 2) >> 2;  // warpgroup: query columns [32 wg, 32 wg + 32)
         const int qd = warp & 3;
         const int i = qd * 32 + lane;  // key row (and, for dQ, query row) of this thread
         const int key = k0 + i;
@@ -842,41 +1009,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc_fence_after();
-            const float4* rows = (const float4*)(sSt + s * C::STAGE + 4 * C::SB);
+            const float4* rows = (const float4*)(sSt + s * C::STAGE + C::ROWS_OFF);
             uint8_t* dsrow = sDS + (j & 1) * (C::BK * 128) + i * 128;
+            const bool need_mask = t0 < k0 + C::BK || t0 + C::BQ > T;
 #pragma unroll 1
-            for (int c = 0; c < C::BQ / 16; c++) {
-                uint32_t vs[16], vg[16], ve[16], vy[16];
+            for (int c = 2 * wg; c < 2 * wg + 2; c++) {
+                uint32_t vs[16], vg[16], vy[16], ve[16];
                 tmem_ld16(tS + lrow + 16 * c, vs);
                 tmem_ld16(tG + lrow + 16 * c, vg);
-                tmem_ld16(tE + lrow + 16 * c, ve);
                 tmem_ld16(tY + lrow + 16 * c, vy);
+                tmem_ld16(tE + lrow + 16 * c, ve);
                 tmem_wait_ld();
                 uint32_t o1[16], o2[16];  // o1: a | dg, o2: ds | p (f16 pairs)
+                if (need_mask) {
+                    // query t = t0 + 16 c + qq is valid iff key <= t and t < T
+                    const int qlo = max(key - (t0 + 16 * c), 0);
+                    const int qhi = T - (t0 + 16 * c);
+                    b3_chunk<true>(vs, vg, vy, ve, rows + 16 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
+                    if (qhi < 16) {
 #pragma unroll
-                for (int q2 = 0; q2 < 8; q2++) {
-                    float a[2], dg[2], ds[2], pp[2];
-#pragma unroll
-                    for (int hh = 0; hh < 2; hh++) {
-                        const int qq = 2 * q2 + hh;
-                        const int t = t0 + 16 * c + qq;
-                        const float4 rw = rows[16 * c + qq];  // {lse log2e, gbar, ebar, D}
-                        const float p = (key <= t && t < T)
-                                            ? fast_exp2(fmaf(__uint_as_float(vs[qq]), scale_log2, -rw.x))
-                                            : 0.f;
-                        const float g = __uint_as_float(vg[qq]);
-                        const float e = __uint_as_float(ve[qq]);
-                        const float y = __uint_as_float(vy[qq]);
-                        const float w1 = 1.f + g - rw.y;
-                        a[hh] = p * w1;
-                        dg[hh] = p * (e - rw.z);
-                        ds[hh] = scale * p * (fmaf(e, w1, -g * rw.z) + y - rw.w);
-                        pp[hh] = p;
+                        for (int x = 0; x < 8; x++) {
+                            const uint32_t keep = (2 * x + 1 < qhi) ? 0xFFFFFFFFu : (2 * x < qhi ? 0xFFFFu : 0u);
+                            o1[x] &= keep;
+                            o1[8 + x] &= keep;
+                            o2[x] &= keep;
+                            o2[8 + x] &= keep;
+                        }
                     }
-                    o1[q2] = pack_f16(a[0], a[1]);
-                    o1[8 + q2] = pack_f16(dg[0], dg[1]);
-                    o2[q2] = pack_f16(ds[0], ds[1]);
-                    o2[8 + q2] = pack_f16(pp[0], pp[1]);
+                } else {
+                    b3_chunk<false>(vs, vg, vy, ve, rows + 16 * c, 0, scale, scale_log2, o1, o2);
                 }
                 tmem_st16(tS + lrow + 16 * c, o1);
                 tmem_st16(tG + lrow + 16 * c, o2);
@@ -890,7 +1051,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             mbar_arrive(op_full);
             if ((j & 1) == 1 || j == nsub - 1) {
-                // dQ of the 128-query tile m = j / 2: thread = query row i
+                // dQ of the 128-query tile m = j / 2: thread = query row i,
+                // warpgroup wg adds columns [wg D/2, wg D/2 + D/2)
                 ok = mbar_wait(dq_full, (j >> 1) & 1, wd, 8);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
@@ -899,12 +1061,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_after();
                 const int t = k0 + (j >> 1) * C::QT + i;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; c++) {
+                for (int c = 0; c < D / 64; c++) {
+                    const int col = wg * (D / 2) + 32 * c;
                     uint32_t v[32];
-                    tmem_ld32(tDQ + lrow + 32 * c, v);
+                    tmem_ld32(tDQ + lrow + col, v);
                     tmem_wait_ld();
                     if (t < T) {
-                        float* dst = dq_acc + ((size_t)bh * T + t) * D + 32 * c;
+                        float* dst = dq_acc + ((size_t)bh * T + t) * D + col;
 #pragma unroll
                         for (int x = 0; x < 32; x += 4)
                             red_add_v4(dst + x, __uint_as_float(v[x]), __uint_as_float(v[x + 1]),
@@ -919,27 +1082,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = mbar_wait(acc_done, (nsub - 1) & 1, wd, 9);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
+                // warpgroup 0 writes dV, warpgroup 1 writes dK
+                const uint32_t tsrc = wg == 0 ? tDV : tDK;
+                __nv_bfloat16* dst_base = wg == 0 ? dv : dk;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32], w[32];
-                    tmem_ld32(tDV + lrow + 32 * c, v);
-                    tmem_ld32(tDK + lrow + 32 * c, w);
+                    uint32_t v[32];
+                    tmem_ld32(tsrc + lrow + 32 * c, v);
                     tmem_wait_ld();
                     if (key < T) {
-                        const size_t off = ((size_t)bh * T + key) * D + 32 * c;
-                        uint4* pv = (uint4*)(dv + off);
-                        uint4* pk = (uint4*)(dk + off);
+                        uint4* pv = (uint4*)(dst_base + ((size_t)bh * T + key) * D + 32 * c);
 #pragma unroll
-                        for (int x = 0; x < 4; x++) {
+                        for (int x = 0; x < 4; x++)
                             pv[x] = make_uint4(pack_bf16(__uint_as_float(v[8 * x]), __uint_as_float(v[8 * x + 1])),
                                                pack_bf16(__uint_as_float(v[8 * x + 2]), __uint_as_float(v[8 * x + 3])),
                                                pack_bf16(__uint_as_float(v[8 * x + 4]), __uint_as_float(v[8 * x + 5])),
                                                pack_bf16(__uint_as_float(v[8 * x + 6]), __uint_as_float(v[8 * x + 7])));
-                            pk[x] = make_uint4(pack_bf16(__uint_as_float(w[8 * x]), __uint_as_float(w[8 * x + 1])),
-                                               pack_bf16(__uint_as_float(w[8 * x + 2]), __uint_as_float(w[8 * x + 3])),
-                                               pack_bf16(__uint_as_float(w[8 * x + 4]), __uint_as_float(w[8 * x + 5])),
-                                               pack_bf16(__uint_as_float(w[8 * x + 6]), __uint_as_float(w[8 * x + 7])));
-                        }
                     }
                 }
             }
@@ -999,7 +1157,6 @@ bool make_map(CUtensorMap* m, const void* base, int D, int T, int BH, int rows) 
         if (e_ != cudaSuccess) return e_;  \
     } while (0)
 
-constexpr int PROJ_ROWS = 128;
 
 // Workspace of the tensor-core forward: f16 copies of q, k, v, then U (f16)
 // and gbar (fp32).
@@ -1044,8 +1201,9 @@ TcBwdWs tc_bwd_ws(void* ws, int B, int H, int T, int d) {
 }
 size_t tc_bwd_bytes(int B, int H, int T, int d) {
     const size_t n = (size_t)B * H * T;
+    const size_t nchunks = ((size_t)B * T + 511) / 512;  // RowCfg<d>::ROWS_PER_CTA
     return 2 * align256(n * d * 4) + 6 * align256(n * d * 2) + align256(n * 4) + align256(n * 16) +
-           simt_dp_partial_bytes(B, H, T, d);
+           align256((size_t)H * nchunks * d * d * 4);
 }
 
 // Row scalars [BH][T] float4 viewed as 3-D (4, T, BH), box 4 x 64 x 1.
@@ -1102,12 +1260,14 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         PLX_TRY(cudaGetLastError());
     }
     {  // projection
-        const size_t sm = sizeof(float) * (D * (D + 1) + 8 * D);
-        PLX_TRY(cudaFuncSetAttribute(tc_proj<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        const dim3 grid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
+        using R = RowCfg<D>;
+        const size_t sm = R::smem(0);
+        PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+        const dim3 grid((a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA, a.H);
         timing_begin(a.stream, "tc_proj");
-        tc_proj<D><<<grid, 256, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, w.U, w.gbar, a.B, a.H,
-                                                a.T, PROJ_ROWS);
+        tc_rows<D, 0><<<grid, R::NT, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, nullptr, nullptr,
+                                                      nullptr, w.U, w.gbar, nullptr, nullptr, nullptr, nullptr, a.B,
+                                                      a.H, a.T);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
@@ -1154,23 +1314,30 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
-    {  // B2: row math
-        const size_t sm = sizeof(float) * (D * (D + 1) + 8 * D);
-        PLX_TRY(cudaFuncSetAttribute(tc_bwd_b2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        const dim3 grid((a.B * a.T + PROJ_ROWS - 1) / PROJ_ROWS, a.H);
+    {  // B2: row math and the dP_h partials
+        using R = RowCfg<D>;
+        const size_t sm = R::smem(1);
+        const int nchunks = (a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA;
+        PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
         timing_begin(a.stream, "tc_bwd_b2");
-        tc_bwd_b2<D><<<grid, 256, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U,
-                                                  w.dmu, w.dq_acc, w.rows, a.B, a.H, a.T, PROJ_ROWS);
+        tc_rows<D, 1><<<dim3(nchunks, a.H), R::NT, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, a.lse,
+                                                                   w.R, w.ebar, w.U, nullptr, w.dmu, w.dq_acc,
+                                                                   w.rows, w.partial, a.B, a.H, a.T);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+        const int dd4 = D * D / 4;
+        timing_begin(a.stream, "tc_dp_reduce");
+        tc_dp_reduce<<<dim3((dd4 + 255) / 256, a.H), 256, 0, a.stream>>>((const float4*)w.partial, (float4*)a.dP,
+                                                                           nchunks, dd4);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
-    PLX_TRY(simt_dP(a.q, a.mu_k, w.R, w.partial, a.dP, a.B, a.H, a.T, D, a.dtype, a.stream));
     {  // B3: dK, dV, dQ
         using C = B3Cfg<D>;
         const int nkt = (a.T + C::BK - 1) / C::BK;
         PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b3");
-        tc_bwd_b3<D><<<nkt * BH, NTHREADS, C::SMEM, a.stream>>>(
+        tc_bwd_b3<D><<<nkt * BH, C::NT, C::SMEM, a.stream>>>(
             mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows, w.dq_acc, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
             a.T, BH, nkt, scale, scale_log2, a.status);
         timing_end(a.stream);

@@ -18,11 +18,15 @@ TOL_BF16_GRAD = 3e-2
 STORAGE_REL = {"bf16": 2.0 ** -8, "fp32": 2.0 ** -24}
 
 
-def rel_err(got, ref, storage: str = "fp32") -> float:
-    """max_i max(0, |got_i - ref_i| - u |ref_i|) / RMS(ref), u = STORAGE_REL[storage]."""
+def rel_err(got, ref, storage: str = "fp32", roundings: int = 1) -> float:
+    """max_i max(0, |got_i - ref_i| - n u |ref_i|) / RMS(ref), u = STORAGE_REL[storage].
+
+    ``roundings`` (n) is how many of the two sides were rounded to the storage
+    type: 1 against the fp64 oracle, 2 when both sides are stored results.
+    """
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    err = np.maximum(0.0, np.abs(got - ref) - STORAGE_REL[storage] * np.abs(ref))
+    err = np.maximum(0.0, np.abs(got - ref) - roundings * STORAGE_REL[storage] * np.abs(ref))
     rms = float(np.sqrt(np.mean(ref * ref)))
     if rms == 0.0:
         return float(err.max())

@@ -45,7 +45,8 @@ def test_noalloc_matches_parallax_fwd_on_two_calls(path):
             assert rc == plx.PLX_OK, plx.parallax_strerror(rc)
             torch.cuda.synchronize()
             tol = TOL_BF16 if dtype == "bf16" else TOL_FP32
-            assert rel_err(to_host64(out), to_host64(ref_o), dtype) < tol
+            # both outputs are stored in dtype: neither rounding is charged
+            assert rel_err(to_host64(out), to_host64(ref_o), dtype, roundings=2) < tol
             assert rel_err(to_host64(mu), to_host64(ref_m)) < tol
             assert np.abs(to_host64(lse) - to_host64(ref_l)).max() < tol
     finally:
