@@ -136,7 +136,10 @@ BWD_SMALL = [
     (1, 2, 64, 64, "fp32"),
     (2, 2, 100, 128, "fp32"),
     (1, 1, 1, 64, "bf16"),
+    (2, 1, 33, 64, "bf16"),
+    (1, 1, 96, 64, "bf16"),
     (2, 2, 130, 64, "bf16"),
+    (1, 2, 260, 64, "bf16"),
     (1, 2, 257, 128, "bf16"),
 ]
 
