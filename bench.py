@@ -44,6 +44,9 @@ L2_BYTES = 126 * 1024 * 1024
 # counted once: S, mu_k | G, o | S, E, R | G, Y, dV, dK (3 terms), dQ).
 FWD_FLOPS_PER_PAIR_D = 8
 BWD_FLOPS_PER_PAIR_D = 20
+# MMA flops the forward executes per causal pair: pass 1 S and P~K (4d),
+# pass 2 S, G and W V (6d); S is computed twice.
+FWD_EXEC_FLOPS_PER_PAIR_D = 10
 KERNEL_FLOPS_PER_PAIR_D = {
     "tc_pass1": 4, "simt_pass1": 4,
     "tc_pass2": 4, "simt_pass2": 4,
@@ -62,6 +65,23 @@ def load_peaks():
                 "sm_max_mhz": p.get("sm_max_mhz", 2032.0), "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
             "sm_max_mhz": 2032.0, "source": "fallback"}
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, or None
+    when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic_c4.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+        with open(os.path.join(ROOT, doc["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != doc["source_sha256"]:
+                return None
+        k = doc["kernels"][kernel]
+        return k["read"] + k["write"]
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def fp32_simt_peak_tflops(sm_mhz: float) -> float:
@@ -358,7 +378,7 @@ def run_ours(args, world, rank):
                 peak, bound = fp32_simt_peak_tflops(peaks["sm_max_mhz"]), "alu"
                 peak_note = "fp32 FFMA: 148 SMs x 128 lanes x 2 x max SM clock"
             roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak, "traffic": None, "peak_source": peak_note,
+                        "frac": achieved / peak, "traffic": measured_traffic(dom), "peak_source": peak_note,
                         "flops_per_launch": pairs * fpp * d}
     # whole-step fraction of the tensor peak
     pct_peak = value / world / peaks["bf16_tflops_sustained"]
@@ -385,6 +405,8 @@ def run_ours(args, world, rank):
         "clocks": clk,
         "e2e": e2e,
     }
+    if rank == 0 and world == 1 and path == "tc" and not args.no_fwd_c3:
+        line["fwd_c3"] = forward_workload(torch, plx, "c3", dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
         nheads = min(H, threads)
@@ -406,6 +428,61 @@ def _tc_ws(plx, B, H, T, d, dtc):
         return plx.parallax_fwd_workspace_bytes(B, H, T, d, dtc) or -1
     finally:
         plx.parallax_set_path(prev)
+
+
+def forward_workload(torch, plx, name, dev, stream, iters=10, warmup=3):
+    """Forward-only throughput of another workload (c3: B4 H16 T4096 d128, the
+    shape the forward target is stated on), inputs resident in HBM, timed with
+    CUDA events on the launching stream; per-kernel shares from the library's
+    event timing."""
+    w = plx_synth.WORKLOADS[name]
+    inp = plx_synth.generate_workload(name)
+    B, H, T, d = w.B, w.H, w.T, w.d
+
+    def dev_t(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    q, k, v, P = (dev_t(inp[x]) for x in ("q", "k", "v", "P"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    mu = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+    dtc = plx.PLX_BF16
+    fws = torch.empty(max(256, plx.parallax_fwd_workspace_bytes(B, H, T, d, dtc)), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
+    plx.kernel_times()
+    plx.parallax_timing_reset()
+    plx.parallax_timing_enable(True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    plx.parallax_timing_enable(False)
+    kt = plx.kernel_times()
+    ms = e0.elapsed_time(e1) / iters
+    pairs = plx_synth.causal_pairs(B, H, T)
+    peaks = load_peaks()
+    alg = pairs * FWD_FLOPS_PER_PAIR_D * d / (ms / 1e3) / 1e12
+    exe = pairs * FWD_EXEC_FLOPS_PER_PAIR_D * d / (ms / 1e3) / 1e12
+    res = {"workload": w.describe, "ms": ms, "tflops_algorithmic": alg, "tflops_executed_mma": exe,
+           "frac_of_bf16_peak_algorithmic": alg / peaks["bf16_tflops"],
+           "frac_of_bf16_peak_executed": exe / peaks["bf16_tflops"], "peak": peaks["bf16_tflops"],
+           "peak_source": f"bf16 dense, {peaks['source']} burst", "kernels": {}}
+    for kname, (tms, cnt) in kt.items():
+        avg = tms / cnt
+        entry = {"avg_ms": avg}
+        fpp = KERNEL_FLOPS_PER_PAIR_D.get(kname)
+        if fpp is not None:
+            entry["tflops_algorithmic"] = pairs * fpp * d / (avg / 1e3) / 1e12
+        res["kernels"][kname] = entry
+    del q, k, v, P, out, lse, mu, fws
+    torch.cuda.empty_cache()
+    return res
 
 
 def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream, n):
@@ -467,6 +544,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c4", choices=["c4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fwd-c3", action="store_true",
+                    help="skip the extra forward-only measurement of the B4 H16 T4096 d128 workload")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
     world, rank, _ = dist_env()
