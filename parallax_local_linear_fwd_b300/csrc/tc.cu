@@ -75,16 +75,41 @@ struct P1 {
     static constexpr int NS = D == 64 ? 4 : 2;  // K-tile stages
     static constexpr int QB = BM * D * 2;
     static constexpr int KB = BN * D * 2;
-    static constexpr int NBAR = 1 + 2 * NS + 4;
+    static constexpr int NBAR = 1 + 2 * NS + 6;
     static constexpr int SMEM = 1024 + QB + NS * KB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 256;  // S [0,128) (P~ f16 aliases [0,64)), Mu [128, 128+D)
+    static_assert(NS >= 2 && KB == QB, "the projection reuses two K stages for delta_hi / delta_lo");
 };
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier over `count` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Byte offset of the 16-byte chunk holding columns [c, c + 8) of row r in a
+// swizzled 16-bit tile of `rows` rows (column blocks of 64).
+__device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
+    return (uint32_t)((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
+}
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 2)
     tc_pass1(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             float* __restrict__ lse, float* __restrict__ mu_k, int T, int BH, int ntq, float scale_log2,
-             unsigned* status) {
+             const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ mu_k, __half* __restrict__ U,
+             float* __restrict__ gbar, int T, int H, int BH, int ntq, float scale_log2, unsigned* status) {
     using C = P1<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -99,6 +124,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint64_t* p_full = s_full + 1;
     uint64_t* o_done = s_full + 2;
     uint64_t* drain = s_full + 3;
+    uint64_t* proj_ready = s_full + 4;  // delta_hi/lo and P_h (f16) staged for U = delta P_h^T
+    uint64_t* proj_done = s_full + 5;   // U is in TMEM
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
@@ -121,6 +148,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mbar_init(p_full, 128);
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        mbar_init(proj_ready, 128);
+        mbar_init(proj_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
@@ -175,6 +204,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         mma_ts(tMu, tS + kk * 8, desc_mnmajor(kaddr, C::BN, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(o_done);
                     mma_commit(&k_empty[s]);
+                }
+                // projection U = delta P_h^T (delta = delta_hi + delta_lo, P_h in f16):
+                // M = 128 rows, N = D, K = D, into the S columns
+                if (mbar_wait(proj_ready, 0, wd, 9)) {
+                    tc_fence_after();
+                    const uint32_t idP = idesc_mma(128, D, false, false);
+                    const uint32_t dhi = smem_u32(sK), dlo = smem_u32(sK + C::KB), pb = smem_u32(sQ);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(dhi, C::BM, kk), desc_kmajor(pb, D, kk), idP, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(dlo, C::BM, kk), desc_kmajor(pb, D, kk), idP, 1u);
+                    mma_commit(proj_done);
                 }
             }
             mma_commit(drain);
@@ -256,26 +299,89 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             tc_fence_before();
             mbar_arrive(p_full);
         }
+        if (ok) ok = mbar_wait(o_done, (nkt - 1) & 1, wd, 8);
+        // The four epilogue warps agree on ok before the projection (whose
+        // steps synchronise on a named barrier): an abort anywhere skips it.
+        ok = named_bar_and(1, 128, ok);
         if (ok) {
-            ok = mbar_wait(o_done, (nkt - 1) & 1, wd, 8);
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const size_t grow = (size_t)bh * T + t;
+            // mu_k = Mu / l (output), delta = q - mu_k split into f16 hi + lo,
+            // written as the K-major A tile of the projection into K stages 0, 1
+#pragma unroll 1
+            for (int c = 0; c < D / 32; c++) {
+                uint32_t v[32];
+                tmem_ld32(tMu + lrow + c * 32, v);
+                tmem_wait_ld();
+                float mu[32];
+#pragma unroll
+                for (int i = 0; i < 32; i++) mu[i] = __uint_as_float(v[i]) * inv;
+                if (t < T) {
+                    float* dst = mu_k + grow * D + c * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) *(float4*)(dst + i) = make_float4(mu[i], mu[i + 1], mu[i + 2], mu[i + 3]);
+                }
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+                    const uint32_t off = sw_off(row, c * 32 + g * 8, C::BM);
+                    const uint4 qv = *(const uint4*)(sQ + off);
+                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int x = 0; x < 4; x++) {
+                        const float d0 = f16_lo(qw[x]) - mu[g * 8 + 2 * x];
+                        const float d1 = f16_hi(qw[x]) - mu[g * 8 + 2 * x + 1];
+                        hi[x] = pack_f16(d0, d1);
+                        lo[x] = pack_f16(d0 - f16_lo(hi[x]), d1 - f16_hi(hi[x]));
+                    }
+                    *(uint4*)(sK + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *(uint4*)(sK + C::KB + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            // every thread has read its q row: P_h (f16) replaces the Q tile as
+            // the K-major B operand (rows = output index a, K = input index b)
+            named_bar_sync(1, 128);
+            const float* Ph = P + (size_t)(bh % H) * D * D;
+            const int et = (warp - 2) * 32 + lane;  // 0..127
+#pragma unroll 1
+            for (int id = et; id < D * D / 8; id += 128) {
+                const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
+                const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
+                const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
+                *(uint4*)(sQ + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
+                                                                pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(proj_ready);
+            ok = mbar_wait(proj_done, 0, wd, 10);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const float inv = 1.f / l;
-                float* dst = mu_k + ((size_t)bh * T + t) * D;
-#pragma unroll
+                float g = 0.f;
+#pragma unroll 1
                 for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(tMu + lrow + c * 32, v);
+                    uint32_t vu[32], vm[32];
+                    tmem_ld32(tS + lrow + c * 32, vu);
+                    tmem_ld32(tMu + lrow + c * 32, vm);
                     tmem_wait_ld();
-                    if (t < T) {
+                    uint32_t uh[16];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *(float4*)(dst + c * 32 + i) =
-                                make_float4(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv,
-                                            __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+                    for (int i = 0; i < 16; i++) {
+                        uh[i] = pack_f16(__uint_as_float(vu[2 * i]), __uint_as_float(vu[2 * i + 1]));
+                        g = fmaf(__uint_as_float(vm[2 * i]) * inv, f16_lo(uh[i]), g);
+                        g = fmaf(__uint_as_float(vm[2 * i + 1]) * inv, f16_hi(uh[i]), g);
+                    }
+                    if (t < T) {
+                        uint4* dst = (uint4*)(U + grow * D + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; i++) dst[i] = make_uint4(uh[4 * i], uh[4 * i + 1], uh[4 * i + 2], uh[4 * i + 3]);
                     }
                 }
-                if (t < T) lse[(size_t)bh * T + t] = (m_use + __log2f(l)) * LN2;
+                if (t < T) {
+                    lse[grow] = (m_use + __log2f(l)) * LN2;
+                    gbar[grow] = g;
+                }
             }
         }
     }
@@ -1542,25 +1648,13 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         __half* dst[3] = {w.q16, w.k16, w.v16};
         PLX_TRY(to_f16(src, dst, 3, n, a.stream));
     }
-    {  // pass 1
+    {  // pass 1 (with the projection in its epilogue)
         using C = P1<D>;
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_pass1<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass1");
-        tc_pass1<D><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mk128, a.lse, a.mu_k, a.T, BH, ntq,
-                                                                scale_log2, a.status);
-        timing_end(a.stream);
-        PLX_TRY(cudaGetLastError());
-    }
-    {  // projection
-        using R = RowCfg<D>;
-        const size_t sm = R::smem(0);
-        PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        const dim3 grid((a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA, a.H);
-        timing_begin(a.stream, "tc_proj");
-        tc_rows<D, 0><<<grid, R::NT, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, nullptr, nullptr,
-                                                      nullptr, w.U, w.gbar, nullptr, nullptr, nullptr, nullptr, a.B,
-                                                      a.H, a.T);
+        tc_pass1<D><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mk128, a.P, a.lse, a.mu_k, w.U, w.gbar, a.T,
+                                                                a.H, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
