@@ -405,6 +405,8 @@ def run_ours(args, world, rank):
         "clocks": clk,
         "e2e": e2e,
     }
+    if rank == 0 and world == 1 and not args.no_fwd_c3:
+        line["decode"] = decode_workload(torch, plx, k, v, P, stream)
     if rank == 0 and world == 1 and path == "tc" and not args.no_fwd_c3:
         line["fwd_c3"] = forward_workload(torch, plx, "c3", dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -485,6 +487,45 @@ def forward_workload(torch, plx, name, dev, stream, iters=10, warmup=3):
     return res
 
 
+def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3):
+    """Decode step over the step's own keys and values as a KV cache (one new
+    query per head, every sequence at full length).  HBM-bound: the roofline
+    is the measured copy bandwidth; the algorithmic bytes are the cache (K and
+    V read once each), although the kernels read K twice."""
+    B, H, L, d = (int(x) for x in k.shape)
+    gen = torch.Generator(device="cpu").manual_seed(17)
+    q = torch.randn((B, H, d), generator=gen).to(k.dtype).to(k.device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=k.device)
+    dtc = plx.PLX_BF16 if k.dtype == torch.bfloat16 else plx.PLX_FP32
+    ws = torch.empty(max(256, plx.parallax_decode_workspace_bytes(B, H, L, d, dtc)), dtype=torch.uint8,
+                     device=k.device)
+    for _ in range(warmup):
+        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=stream)
+    plx.kernel_times()
+    plx.parallax_timing_reset()
+    plx.parallax_timing_enable(True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    plx.parallax_timing_enable(False)
+    kt = plx.kernel_times()
+    ms = e0.elapsed_time(e1) / iters
+    cache_bytes = 2 * k.numel() * k.element_size()
+    peaks = load_peaks()
+    gbs = cache_bytes / (ms / 1e3) / 1e9
+    return {"workload": f"decode, {str(k.dtype).replace('torch.', '')}, B{B} H{H} cache {L} d{d}, "
+                        "one new query per head", "us": ms * 1e3, "tokens_per_s": B / (ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": cache_bytes,
+                         "peak_source": f"{peaks['source']} copy bandwidth"},
+            "kernels": {n: {"avg_us": 1e3 * t / c} for n, (t, c) in kt.items()}}
+
+
 def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream, n):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     torch.cuda.synchronize()
@@ -545,7 +586,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="c4", choices=["c4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-c3", action="store_true",
-                    help="skip the extra forward-only measurement of the B4 H16 T4096 d128 workload")
+                    help="skip the extra measurements: the B4 H16 T4096 d128 forward and the decode step")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
     world, rank, _ = dist_env()

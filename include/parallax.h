@@ -138,6 +138,36 @@ PLX_API int parallax_bwd(const void* q, const void* k, const void* v, const floa
                  int B, int H, int T, int d, int dtype, void* stream);
 
 /*
+ * Decode step: one new query per (sequence, head) against a KV cache.
+ * The paper's own kernel is a decode kernel ("Parallax: Parameterized Local
+ * Linear Attention for Language Modeling", technical summary,
+ * "Hardware-aware algorithm"); the layer is the same as parallax_fwd's: the
+ * query of sequence b sits at position lens[b] - 1 and attends to keys
+ * 0 .. lens[b] - 1, so out[b,h] equals row lens[b] - 1 of parallax_fwd run
+ * on the cache with that query in that row.
+ *   q:        device, [B][H][d] in dtype, the new queries.
+ *   k_cache,
+ *   v_cache:  device, [B][H][Lmax][d] in dtype; rows past lens[b] are ignored.
+ *   lens:     device, [B] int32, valid keys per sequence (the new token's own
+ *             key and value included); values outside [1, Lmax] are clamped
+ *             to it.  NULL means every sequence has Lmax keys.
+ *   P:        device, [H][d][d] float32.
+ *   out:      device, [B][H][d] in dtype.   lse: device, [B][H] float32.
+ *   workspace: device, >= parallax_decode_workspace_bytes(), 256-byte
+ *             aligned, or NULL to allocate it stream-ordered and free it
+ *             before returning.
+ * Memory-bound split-KV kernels (fp32 arithmetic for both dtypes): keys are
+ * read twice (the softmax statistics, then the weights) and values once.
+ * Returns PLX_OK or an error code; on error nothing has been launched.
+ */
+PLX_API int parallax_decode(const void* q, const void* k_cache, const void* v_cache, const int* lens,
+                    const float* P, void* out, float* lse, void* workspace,
+                    int B, int H, int Lmax, int d, int dtype, void* stream);
+
+/* Bytes of device workspace parallax_decode needs (0 on bad args). */
+PLX_API size_t parallax_decode_workspace_bytes(int B, int H, int Lmax, int d, int dtype);
+
+/*
  * Synchronizes `stream`, then reads and clears the current device's watchdog
  * word.  Returns PLX_OK, PLX_ERR_TIMEOUT (a bounded wait inside a kernel gave
  * up; the kernel skipped its remaining work and released its resources) or

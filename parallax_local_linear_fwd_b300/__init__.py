@@ -24,6 +24,7 @@ __all__ = [
     "parallax_bwd_workspace_bytes", "parallax_last_device_error", "parallax_set_path",
     "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
     "parallax_timing_get", "parallax_timing_reset", "kernel_times",
+    "parallax_decode", "parallax_decode_workspace_bytes",
 ]
 
 PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -53,6 +54,8 @@ _SIGNATURES = {
     "parallax_timing_get": (_i, [_i, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_longlong)]),
     "parallax_timing_reset": (None, []),
+    "parallax_decode": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
 }
 
 
@@ -189,6 +192,27 @@ def parallax_bwd(q, k, v, P, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None
                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
                               B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
     return dq, dk, dv, dP
+
+
+def parallax_decode_workspace_bytes(B, H, Lmax, d, dtype) -> int:
+    return int(lib().parallax_decode_workspace_bytes(B, H, Lmax, d, dtype))
+
+
+def parallax_decode(q, k_cache, v_cache, P, lens=None, out=None, lse=None, workspace=None, stream=None):
+    """Decode step: q [B,H,d] against caches [B,H,Lmax,d] (fp32/bf16, CUDA);
+    lens: int32 [B] valid keys per sequence (None: Lmax).  Returns (out, lse)."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, H, d] and the caches [B, H, Lmax, d]")
+    B, H, Lmax, d = (int(x) for x in k_cache.shape)
+    dt = _dtype_code(q)
+    if lens is not None and (lens.dtype != torch.int32 or lens.numel() != B):
+        raise ValueError("lens must be int32 [B]")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().parallax_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(P), _ptr(out),
+                                 _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
+           "parallax_decode")
+    return out, lse
 
 
 def parallax_last_device_error(stream=None):

@@ -261,6 +261,37 @@ int parallax_bwd(const void* q, const void* k, const void* v, const float* P, co
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
+size_t parallax_decode_workspace_bytes(int B, int H, int Lmax, int d, int dtype) {
+    if (check_sizes(B, H, Lmax, d, dtype)) return 0;
+    return plx::decode_ws_bytes(B, H, Lmax, d);
+}
+
+int parallax_decode(const void* q, const void* k_cache, const void* v_cache, const int* lens, const float* P,
+                    void* out, float* lse, void* workspace, int B, int H, int Lmax, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, Lmax, d, dtype);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !P || !out || !lse) return PLX_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k_cache, v_cache, P, out, lse};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
+    if (lens && ((uintptr_t)lens & 3u)) return PLX_ERR_INVALID_ARG;
+    if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool own = workspace == nullptr;
+    void* ws = workspace;
+    if (own && cudaMallocAsync(&ws, plx::decode_ws_bytes(B, H, Lmax, d), s) != cudaSuccess) return PLX_ERR_CUDA;
+    plx::DecodeArgs a{q, k_cache, v_cache, lens, P, out, lse, ws, B, H, Lmax, d, dtype, s};
+    cudaError_t e = plx::decode(a);
+    if (own) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
 int parallax_last_device_error(void* stream, unsigned* detail) {
     if (detail) *detail = 0;
     unsigned* status = nullptr;

@@ -49,6 +49,19 @@ struct BwdArgs {
     unsigned* status;
 };
 
+struct DecodeArgs {
+    const void* q;     // [B,H,d] one new query per (sequence, head)
+    const void* k;     // [B,H,Lmax,d] key cache
+    const void* v;     // [B,H,Lmax,d] value cache
+    const int* lens;   // [B] valid keys per sequence (device), or nullptr = Lmax
+    const float* P;    // [H,d,d]
+    void* out;         // [B,H,d]
+    float* lse;        // [B,H]
+    void* ws;          // decode_ws_bytes()
+    int B, H, Lmax, d, dtype;
+    cudaStream_t stream;
+};
+
 // Launch accounting / timing hooks (plx_api.cu).  Bracket every launch:
 //   timing_begin(stream, "name"); kernel<<<...>>>(...); timing_end(stream);
 void timing_begin(cudaStream_t s, const char* name);
@@ -70,6 +83,10 @@ void simt_bwd_ws_b1_outputs(void* ws, int B, int H, int T, int d, float** R, flo
 size_t simt_dp_partial_bytes(int B, int H, int T, int d);
 cudaError_t simt_dP(const void* q, const float* mu_k, const float* du, float* partial, float* dP, int B, int H,
                     int T, int d, int dtype, cudaStream_t stream);
+
+// Decode (SIMT, HBM-bound split-KV), any dtype, d in {64,128}.
+size_t decode_ws_bytes(int B, int H, int Lmax, int d);
+cudaError_t decode(const DecodeArgs& a);
 
 // Tensor-core (tcgen05) family: bf16, d in {64,128}.
 bool tc_available();

@@ -1,0 +1,83 @@
+"""GPU parity of the decode step (parallax_decode) against the fp64 oracle.
+
+A decode step for sequence b is the layer's row lens[b] - 1 with the caches
+as keys and values, so the oracle is the (pinned) forward evaluated at exactly
+those rows: the query goes into row lens[b] - 1 of an otherwise unused query
+array, and the oracle computes only the requested rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parallax_local_linear_fwd_b300 as plx
+import plx_synth
+from plx_testutil import TOL_BF16, TOL_FP32, inputs_f64, rel_err, to_device, to_host64
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(B, H, L, d, dtype, lens, seed):
+    inp = plx_synth.generate(B, H, L, d, dtype, seed=seed, p_std=0.3 / np.sqrt(d))
+    rng = np.random.default_rng(seed + 1)
+    # the new queries: one per (b, h), drawn like q and rounded to the storage type
+    qn = rng.standard_normal((B, H, d))
+    if dtype == "bf16":
+        qn_store = plx_synth.to_bf16_bits(qn)
+        qn64 = plx_synth.bf16_bits_to_f32(qn_store).astype(np.float64)
+    else:
+        qn_store = qn.astype(np.float32)
+        qn64 = qn_store.astype(np.float64)
+    eff = np.full(B, L) if lens is None else np.asarray(lens)
+    f = inputs_f64(inp)
+    qfull = np.zeros((B, H, L, d))
+    rows = []
+    for b in range(B):
+        for h in range(H):
+            qfull[b, h, eff[b] - 1] = qn64[b, h]
+            rows.append((b, h, int(eff[b]) - 1))
+    ro, rl, _ = oracle.forward_rows(qfull, f["k"], f["v"], f["P"], rows)
+    q = to_device(qn_store)
+    k, v, P = (to_device(inp[x]) for x in ("k", "v", "P"))
+    lens_t = None if lens is None else torch.tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    out, lse = plx.parallax_decode(q, k, v, P, lens=lens_t)
+    code, detail = plx.parallax_last_device_error()
+    assert code == plx.PLX_OK, (code, hex(detail))
+    return to_host64(out).reshape(-1, d), to_host64(lse).reshape(-1), ro, rl
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_decode_ragged_lengths(d, dtype):
+    B, H, L = 5, 2, 300
+    lens = [1, 128, 129, 300, 257]  # a single key, chunk edges, the full cache, a ragged tail
+    go, gl, ro, rl = _case(B, H, L, d, dtype, lens, seed=40 + d)
+    tol = TOL_FP32 if dtype == "fp32" else TOL_BF16
+    assert rel_err(go, ro, dtype) < tol
+    assert np.abs(gl - rl).max() < tol * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+    # lens[b] = 1: the output is that sequence's first value row
+    assert np.isfinite(go).all()
+
+
+def test_decode_without_lengths_uses_the_whole_cache():
+    go, gl, ro, rl = _case(2, 3, 200, 64, "bf16", None, seed=7)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+
+
+def test_decode_full_size_c4_cache():
+    # one new query per head over the B8 H16 T4096 d64 workload's keys and values
+    w = plx_synth.WORKLOADS["c4"]
+    go, gl, ro, rl = _case(w.B, w.H, w.T, w.d, "bf16", None, seed=w.seed)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+
+
+def test_decode_invalid_arguments():
+    q = torch.zeros(1, 1, 48, device="cuda", dtype=torch.bfloat16)
+    kc = torch.zeros(1, 1, 16, 48, device="cuda", dtype=torch.bfloat16)
+    P = torch.zeros(1, 48, 48, device="cuda")
+    with pytest.raises(plx.PlxError) as e:
+        plx.parallax_decode(q, kc, kc, P)
+    assert e.value.code == plx.PLX_ERR_UNSUPPORTED
+    assert plx.parallax_last_device_error()[0] == plx.PLX_OK
