@@ -42,7 +42,8 @@ def _load():
                                             ctypes.POINTER(ctypes.c_int64), i, dp, dp, dp, i]
         lib.plx_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i,
                                        ctypes.POINTER(ctypes.c_int32), i, dp, dp, dp, dp, i]
-        for f in (lib.plx_oracle_fwd, lib.plx_oracle_fwd_rows, lib.plx_oracle_bwd):
+        lib.plx_oracle_fwd_probe.argtypes = [dp, dp, dp, dp, i, i, i, i, dp, dp, i]
+        for f in (lib.plx_oracle_fwd, lib.plx_oracle_fwd_rows, lib.plx_oracle_bwd, lib.plx_oracle_fwd_probe):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -97,6 +98,22 @@ def forward_rows(q, k, v, P, rows, nthreads: int | None = None):
     if rc:
         raise RuntimeError(f"plx_oracle_fwd_rows failed ({rc})")
     return out, lse, mu_k
+
+
+def forward_probe(q, k, v, rho, nthreads: int | None = None):
+    """One-pass form with a given probe: o = o^SA - Sigma_KV rho.
+
+    q, k, v, rho: [B,H,T,d].  Returns (out [B,H,T,d], lse [B,H,T]) in float64.
+    """
+    q, k, v, rho = _f64(q), _f64(k), _f64(v), _f64(rho)
+    B, H, T, d = q.shape
+    out = np.empty((B, H, T, d))
+    lse = np.empty((B, H, T))
+    rc = _load().plx_oracle_fwd_probe(_p(q), _p(k), _p(v), _p(rho), B, H, T, d, _p(out), _p(lse),
+                                      nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"plx_oracle_fwd_probe failed ({rc})")
+    return out, lse
 
 
 def backward(q, k, v, P, dout, heads=None, nthreads: int | None = None):

@@ -292,6 +292,88 @@ int plx_oracle_fwd_rows(const double *q, const double *k, const double *v, const
     return run_pool(&pool, nthreads) ? 2 : 0;
 }
 
+/* ------------------------------------------------------- given probe (one pass)
+ * The pages' literal form of the layer: the probe rho_t is given (in the paper
+ * it comes from a learned projection of the layer input), not formed from
+ * mu_k, and
+ *   o_t = o^SA_t - Sigma_KV,t rho_t,
+ *   Sigma_KV,t = sum_i p_ti (v_i - mu_v,t)(k_i - mu_k,t)^T   (reading: the
+ *   softmax-weighted cross-covariance, centred at the softmax means).
+ * rho is [B][H][T][d].  Written out term by term: the covariance applied to
+ * rho is sum_i p_i (v_i - mu_v) ((k_i - mu_k) . rho). */
+typedef struct {
+    const plx_in_t *in;
+    const double *rho;
+    double *out, *lse;
+} probe_ctx_t;
+
+static double probe_query(const plx_in_t *in, const double *rho, int b, int h, int t, scratch_t *w) {
+    const int d = in->d;
+    const double c = 1.0 / sqrt((double)d);
+    const double *Q = head_ptr(in->q, in, b, h);
+    const double *K = head_ptr(in->k, in, b, h);
+    const double *V = head_ptr(in->v, in, b, h);
+    const double *qt = Q + (size_t)t * d;
+    const double *rt = head_ptr(rho, in, b, h) + (size_t)t * d;
+
+    double m = -INFINITY;
+    for (int i = 0; i <= t; i++) {
+        double acc = 0.0;
+        for (int j = 0; j < d; j++) acc += qt[j] * K[(size_t)i * d + j];
+        w->s[i] = c * acc;
+        if (w->s[i] > m) m = w->s[i];
+    }
+    double Z = 0.0;
+    for (int i = 0; i <= t; i++) Z += exp(w->s[i] - m);
+    const double L = m + log(Z);
+    for (int i = 0; i <= t; i++) w->p[i] = exp(w->s[i] - L);
+
+    for (int j = 0; j < d; j++) { w->mu_v[j] = 0.0; w->mu_k[j] = 0.0; }
+    for (int i = 0; i <= t; i++)
+        for (int j = 0; j < d; j++) {
+            w->mu_v[j] += w->p[i] * V[(size_t)i * d + j];
+            w->mu_k[j] += w->p[i] * K[(size_t)i * d + j];
+        }
+    /* Sigma_KV rho = sum_i p_i (v_i - mu_v) ((k_i - mu_k) . rho) */
+    for (int j = 0; j < d; j++) w->o[j] = 0.0;
+    for (int i = 0; i <= t; i++) {
+        double kr = 0.0;
+        for (int j = 0; j < d; j++) kr += (K[(size_t)i * d + j] - w->mu_k[j]) * rt[j];
+        for (int j = 0; j < d; j++) w->o[j] += w->p[i] * (V[(size_t)i * d + j] - w->mu_v[j]) * kr;
+    }
+    /* o = o^SA - Sigma_KV rho, with o^SA = mu_v */
+    for (int j = 0; j < d; j++) w->o[j] = w->mu_v[j] - w->o[j];
+    return L;
+}
+
+static void probe_job(void *vctx, int job, scratch_t *w, double *unused) {
+    (void)unused;
+    probe_ctx_t *ctx = (probe_ctx_t *)vctx;
+    const plx_in_t *in = ctx->in;
+    const int b = job / in->H, h = job % in->H, d = in->d;
+    for (int t = 0; t < in->T; t++) {
+        const double L = probe_query(in, ctx->rho, b, h, t, w);
+        const size_t row = ((size_t)b * in->H + h) * in->T + t;
+        if (ctx->lse) ctx->lse[row] = L;
+        for (int j = 0; j < d; j++)
+            if (ctx->out) ctx->out[row * d + j] = w->o[j];
+    }
+}
+
+int plx_oracle_fwd_probe(const double *q, const double *k, const double *v, const double *rho, int B, int H,
+                         int T, int d, double *out, double *lse, int nthreads) {
+    if (B < 1 || H < 1 || T < 1 || d < 1 || !q || !k || !v || !rho) return 1;
+    plx_in_t in = {q, k, v, NULL, NULL, B, H, T, d, 0};
+    probe_ctx_t ctx = {&in, rho, out, lse};
+    pool_t pool;
+    memset(&pool, 0, sizeof(pool));
+    pool.in = &in;
+    pool.njobs = B * H;
+    pool.run = probe_job;
+    pool.ctx = &ctx;
+    return run_pool(&pool, nthreads) ? 2 : 0;
+}
+
 /* ----------------------------------------------------------------- backward */
 
 typedef struct {

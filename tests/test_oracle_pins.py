@@ -214,3 +214,79 @@ def test_synth_recipe_is_deterministic_and_rounded():
     assert plx_synth.to_bf16_bits(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 0x3F82
     c = plx_synth.generate(1, 2, 8, 4, "fp32", seed=0, key_cov=True)
     assert c["P"].dtype == np.float32 and c["q"].dtype == np.float32
+
+
+# ---------------------------------------------------------------- given probe
+# The one-pass form o = o^SA - Sigma_KV rho with a probe supplied as input
+# ("Parallax: Parameterized Local Linear Attention for Language Modeling",
+# "Core mechanism": the probe comes from a learned projection of the layer
+# input instead of a per-query solve).
+
+
+@pytest.mark.parametrize("T,d", [(1, 4), (7, 8), (33, 16)])
+def test_probe_zero_is_softmax_attention(oracle_mod, T, d):
+    rng = np.random.default_rng(300 + T + d)
+    B, H = 2, 2
+    q, k, v = (_rand(rng, B, H, T, d) for _ in range(3))
+    out, lse = oracle_mod.forward_probe(q, k, v, np.zeros((B, H, T, d)), nthreads=2)
+    np.testing.assert_allclose(out, _sdpa(q, k, v), rtol=0, atol=1e-12)
+    for b in range(B):
+        for h in range(H):
+            _, L = _softmax_weights(q[b, h], k[b, h])
+            np.testing.assert_allclose(lse[b, h], L, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,d", [(5, 4), (24, 8)])
+def test_probe_from_the_projector_is_the_two_pass_layer(oracle_mod, T, d):
+    # rho_t = -P_h (q_t - mu_k,t) turns the given-probe form into the layer the
+    # library's two-pass path computes (the sign reading R6: o^SA - Sigma rho
+    # against mu_v + Sigma u with rho = -u)
+    rng = np.random.default_rng(17 + T * d)
+    B, H = 2, 2
+    q, k, v = (_rand(rng, B, H, T, d) for _ in range(3))
+    P = 0.3 * _rand(rng, H, d, d)
+    out2, lse2, mu_k = oracle_mod.forward(q, k, v, P, nthreads=2)
+    rho = -np.einsum("had,bhtd->bhta", P, q - mu_k)
+    out1, lse1 = oracle_mod.forward_probe(q, k, v, rho, nthreads=2)
+    np.testing.assert_allclose(out1, out2, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(lse1, lse2, rtol=0, atol=1e-12)
+    assert np.abs(out1 - _sdpa(q, k, v)).max() > 1e-2  # not vacuous
+
+
+@pytest.mark.parametrize("T,d,lam", [(6, 2, 0.1), (16, 4, 0.1)])
+def test_probe_exact_lla_intercept(oracle_mod, T, d, lam):
+    # rho_t = -(Sigma_kk,t + lambda I)^-1 (q_t - mu_k,t) is the exact-LLA probe:
+    # the output is the intercept of an independently solved ridge WLS fit
+    rng = np.random.default_rng(29 + T + d)
+    B, H = 1, 2
+    q, k, v = (_rand(rng, B, H, T, d) for _ in range(3))
+    rho = np.zeros((B, H, T, d))
+    expect = np.zeros((B, H, T, d))
+    for b in range(B):
+        for h in range(H):
+            W, _ = _softmax_weights(q[b, h], k[b, h])
+            for t in range(T):
+                p = W[t, :t + 1]
+                K, V = k[b, h, :t + 1], v[b, h, :t + 1]
+                mk = p @ K
+                C = (K - mk).T @ (p[:, None] * (K - mk))
+                rho[b, h, t] = -np.linalg.solve(C + lam * np.eye(d), q[b, h, t] - mk)
+                expect[b, h, t] = _wls_intercept(p, K, V, q[b, h, t], lam)
+    out, _ = oracle_mod.forward_probe(q, k, v, rho, nthreads=2)
+    np.testing.assert_allclose(out, expect, rtol=0, atol=1e-10)
+
+
+def test_probe_constant_values_and_linearity(oracle_mod):
+    rng = np.random.default_rng(5)
+    B, H, T, d = 2, 2, 20, 8
+    q, k = _rand(rng, B, H, T, d), _rand(rng, B, H, T, d)
+    rho = _rand(rng, B, H, T, d)
+    c = _rand(rng, B, H, 1, d)
+    vc = np.broadcast_to(c, (B, H, T, d)).copy()
+    out, _ = oracle_mod.forward_probe(q, k, vc, rho, nthreads=2)
+    np.testing.assert_allclose(out, vc, rtol=0, atol=1e-11)  # the covariance of constant values is 0
+    v = _rand(rng, B, H, T, d)
+    o0, _ = oracle_mod.forward_probe(q, k, v, 0 * rho, nthreads=2)
+    o1, _ = oracle_mod.forward_probe(q, k, v, rho, nthreads=2)
+    o3, _ = oracle_mod.forward_probe(q, k, v, 2.5 * rho, nthreads=2)
+    np.testing.assert_allclose(o3 - o0, 2.5 * (o1 - o0), rtol=0, atol=1e-10)
