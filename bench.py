@@ -409,6 +409,7 @@ def run_ours(args, world, rank):
         line["decode"] = decode_workload(torch, plx, k, v, P, stream)
     if rank == 0 and world == 1 and path == "tc" and not args.no_fwd_c3:
         line["fwd_c3"] = forward_workload(torch, plx, "c3", dev, stream)
+        line["fwd_probe_c3"] = probe_workload(torch, plx, "c3", dev, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = cpu_threads()
         nheads = min(H, threads)
@@ -524,6 +525,48 @@ def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3):
                          "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": cache_bytes,
                          "peak_source": f"{peaks['source']} copy bandwidth"},
             "kernels": {n: {"avg_us": 1e3 * t / c} for n, (t, c) in kt.items()}}
+
+
+def probe_workload(torch, plx, name, dev, stream, iters=10, warmup=3):
+    """One-pass given-probe forward on a workload's shape (rho drawn like the
+    projector-formed probe's scale), inputs resident in HBM."""
+    w = plx_synth.WORKLOADS[name]
+    B, H, T, d = w.B, w.H, w.T, w.d
+    gen = torch.Generator(device="cpu").manual_seed(23)
+    mk = lambda s: (s * torch.randn((B, H, T, d), generator=gen)).to(torch.bfloat16).to(dev)  # noqa: E731
+    q, k, v = mk(1.0), mk(1.0), mk(1.0)
+    rho = mk(0.1 / math.sqrt(d))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, plx.parallax_fwd_probe_workspace_bytes(B, H, T, d, plx.PLX_BF16)), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(warmup):
+        plx.parallax_fwd_probe(q, k, v, rho, out=out, lse=lse, workspace=ws, stream=stream)
+    plx.kernel_times()
+    plx.parallax_timing_reset()
+    plx.parallax_timing_enable(True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        plx.parallax_fwd_probe(q, k, v, rho, out=out, lse=lse, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    plx.parallax_timing_enable(False)
+    kt = plx.kernel_times()
+    ms = e0.elapsed_time(e1) / iters
+    pairs = plx_synth.causal_pairs(B, H, T)
+    peaks = load_peaks()
+    tf = pairs * 8 * d / (ms / 1e3) / 1e12  # S, R, O1, O2: 8 d flops per causal pair
+    res = {"workload": f"one-pass given-probe forward, bf16, B{B} H{H} T{T} d{d}", "ms": ms, "tflops": tf,
+           "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "peak_source": f"bf16 dense, {peaks['source']} burst",
+           "kernels": {n: {"avg_ms": t / c} for n, (t, c) in kt.items()}}
+    if "tc_probe" in kt:
+        t_, c_ = kt["tc_probe"]
+        res["kernels"]["tc_probe"]["tflops"] = pairs * 8 * d / (t_ / c_ / 1e3) / 1e12
+    del q, k, v, rho, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream, n):

@@ -138,6 +138,30 @@ PLX_API int parallax_bwd(const void* q, const void* k, const void* v, const floa
                  int B, int H, int T, int d, int dtype, void* stream);
 
 /*
+ * One-pass forward with a given probe: the layer in the form the paper states
+ * it ("Parallax: Parameterized Local Linear Attention for Language Modeling",
+ * technical summary, "Core mechanism"), with the probe rho supplied by the
+ * caller (in the paper it comes from a learned projection of the layer
+ * input) instead of formed from mu_k:
+ *     o_t = o^SA_t - Sigma_KV,t rho_t,
+ *     Sigma_KV,t = sum_i p_ti (v_i - mu_v,t)(k_i - mu_k,t)^T.
+ * With rho_t = -P_h (q_t - mu_k,t) it is parallax_fwd's layer.
+ *   q, k, v, rho: device, [B][H][T][d] bf16 (PLX_BF16 only; PLX_FP32 returns
+ *                 PLX_ERR_UNSUPPORTED).  out: device, [B][H][T][d] bf16.
+ *   lse: device, [B][H][T] float32.
+ *   workspace: device, >= parallax_fwd_probe_workspace_bytes(), 256-byte
+ *              aligned, or NULL to allocate it stream-ordered.
+ * One pass over the keys on the tensor cores: S = Q K^T and R = rho K^T on
+ * the same K tile, online softmax, two value accumulations.
+ */
+PLX_API int parallax_fwd_probe(const void* q, const void* k, const void* v, const void* rho,
+                       void* out, float* lse, void* workspace,
+                       int B, int H, int T, int d, int dtype, void* stream);
+
+/* Bytes of device workspace parallax_fwd_probe needs (0 on bad or unsupported args). */
+PLX_API size_t parallax_fwd_probe_workspace_bytes(int B, int H, int T, int d, int dtype);
+
+/*
  * Decode step: one new query per (sequence, head) against a KV cache.
  * The paper's own kernel is a decode kernel ("Parallax: Parameterized Local
  * Linear Attention for Language Modeling", technical summary,

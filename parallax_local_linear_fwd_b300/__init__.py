@@ -25,6 +25,7 @@ __all__ = [
     "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
     "parallax_timing_get", "parallax_timing_reset", "kernel_times",
     "parallax_decode", "parallax_decode_workspace_bytes",
+    "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes",
 ]
 
 PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -56,6 +57,8 @@ _SIGNATURES = {
     "parallax_timing_reset": (None, []),
     "parallax_decode": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "parallax_fwd_probe": (_i, [_vp] * 7 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
 }
 
 
@@ -192,6 +195,21 @@ def parallax_bwd(q, k, v, P, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None
                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
                               B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
     return dq, dk, dv, dP
+
+
+def parallax_fwd_probe_workspace_bytes(B, H, T, d, dtype) -> int:
+    return int(lib().parallax_fwd_probe_workspace_bytes(B, H, T, d, dtype))
+
+
+def parallax_fwd_probe(q, k, v, rho, out=None, lse=None, workspace=None, stream=None):
+    """One-pass forward with a given probe rho [B,H,T,d] (bf16): o = o^SA - Sigma_KV rho.
+    Returns (out, lse)."""
+    B, H, T, d = _shape(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().parallax_fwd_probe(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    B, H, T, d, _dtype_code(q), _stream_ptr(stream)), "parallax_fwd_probe")
+    return out, lse
 
 
 def parallax_decode_workspace_bytes(B, H, Lmax, d, dtype) -> int:

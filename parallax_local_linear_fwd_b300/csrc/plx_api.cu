@@ -261,6 +261,37 @@ int parallax_bwd(const void* q, const void* k, const void* v, const float* P, co
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
+size_t parallax_fwd_probe_workspace_bytes(int B, int H, int T, int d, int dtype) {
+    if (check_sizes(B, H, T, d, dtype) || dtype != PLX_BF16 || !plx::tc_available()) return 0;
+    return plx::tc_probe_ws_bytes(B, H, T, d);
+}
+
+int parallax_fwd_probe(const void* q, const void* k, const void* v, const void* rho, void* out, float* lse,
+                       void* workspace, int B, int H, int T, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, T, d, dtype);
+    if (rc) return rc;
+    if (dtype != PLX_BF16 || !plx::tc_available()) return PLX_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !rho || !out || !lse) return PLX_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, rho, out, lse};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
+    if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool own = workspace == nullptr;
+    void* ws = workspace;
+    if (own && cudaMallocAsync(&ws, plx::tc_probe_ws_bytes(B, H, T, d), s) != cudaSuccess) return PLX_ERR_CUDA;
+    plx::ProbeArgs a{q, k, v, rho, out, lse, ws, B, H, T, d, dtype, s, status};
+    cudaError_t e = plx::tc_probe(a);
+    if (own) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
 size_t parallax_decode_workspace_bytes(int B, int H, int Lmax, int d, int dtype) {
     if (check_sizes(B, H, Lmax, d, dtype)) return 0;
     return plx::decode_ws_bytes(B, H, Lmax, d);

@@ -15,6 +15,7 @@ enum KernelId : unsigned {
     KID_TC_BWD_B1 = 3,
     KID_TC_BWD_B3 = 4,
     KID_TC_PROJ = 5,
+    KID_TC_PROBE = 6,
 };
 
 struct FwdArgs {
@@ -62,6 +63,19 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+struct ProbeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* rho;  // [B,H,T,d] the given probe
+    void* out;
+    float* lse;
+    void* ws;
+    int B, H, T, d, dtype;
+    cudaStream_t stream;
+    unsigned* status;
+};
+
 // Launch accounting / timing hooks (plx_api.cu).  Bracket every launch:
 //   timing_begin(stream, "name"); kernel<<<...>>>(...); timing_end(stream);
 void timing_begin(cudaStream_t s, const char* name);
@@ -94,5 +108,8 @@ size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
 cudaError_t tc_fwd(const FwdArgs& a);
 cudaError_t tc_bwd(const BwdArgs& a);
+// One-pass forward with a given probe (o = o^SA - Sigma_KV rho), bf16.
+size_t tc_probe_ws_bytes(int B, int H, int T, int d);
+cudaError_t tc_probe(const ProbeArgs& a);
 
 }  // namespace plx

@@ -630,6 +630,261 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
+// ============================================================ given probe
+// The one-pass form with a probe rho supplied as input ("Parallax: Parameterized
+// Local Linear Attention for Language Modeling", technical summary, "Core
+// mechanism": o = o^SA - Sigma_KV rho, the probe from a learned projection of
+// the layer input; "Hardware-aware algorithm": both branches on one KV stream).
+// With r_i = k_i . rho and the softmax p:
+//   Sigma_KV rho = sum_i p_i r_i v_i - rbar mu_v,   rbar = sum_i p_i r_i,
+//   o = mu_v (1 + rbar) - sum_i p_i r_i v_i.
+// Per key tile: S = Q K^T and R = rho K^T on the same K tile, online softmax,
+// O1 += P~ V and O2 += (P~ o R) V with both weight tiles in TMEM; l and rbar
+// sum the rounded weights the MMAs see, so constant values give that value
+// exactly.  8 d MMA flops per causal pair, one pass.
+template <int D>
+struct ProbeCfg {
+    static constexpr int BM = 128, BN = 64, NT = 192;
+    static constexpr int NS = D == 64 ? 4 : 3;  // K+V stages
+    static constexpr int AB = BM * D * 2;
+    static constexpr int KB = BN * D * 2;
+    static constexpr int NBAR = 1 + 2 * NS + 4;
+    static constexpr int SMEM = 1024 + 2 * AB + NS * 2 * KB + NBAR * 8 + 16;
+    // S [0,64) (P~ aliases [0,32)), R [64,128) (P~ o R aliases [64,96)), O1 [128,128+D), O2 [128+D, 128+2D)
+    static constexpr unsigned TMEM_COLS = D == 64 ? 256 : 512;
+    static constexpr int MIN_BLOCKS = D == 64 ? 2 : 1;
+};
+
+template <int D>
+__global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
+    tc_probe_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int T, int BH, int ntq,
+                    float scale_log2, unsigned* status) {
+    using C = ProbeCfg<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sQ = sm;
+    uint8_t* sR = sQ + C::AB;
+    uint8_t* sKV = sR + C::AB;
+    uint64_t* bars = (uint64_t*)(sKV + NS * 2 * C::KB);
+    uint64_t* a_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + NS;
+    uint64_t* s_full = kv_empty + NS;
+    uint64_t* p_full = s_full + 1;
+    uint64_t* o_done = s_full + 2;
+    uint64_t* drain = s_full + 3;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int rank, bh;
+    work_item(blockIdx.x, BH, ntq, &rank, &bh);
+    const int qt = ntq - 1 - rank;
+    const int q0 = qt * C::BM;
+    const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
+    const Watchdog wd{status, abortf, KID_TC_PROBE};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(a_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tS = tmem, tR = tmem + 64, tO1 = tmem + 128, tO2 = tmem + 128 + D;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(a_full, 2 * C::AB);
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) {
+                tma_load_3d(sQ + r * C::BM * 128, &tm_q, r * 64, q0, bh, a_full);
+                tma_load_3d(sR + r * C::BM * 128, &tm_r, r * 64, q0, bh, a_full);
+            }
+            int issued = 0;
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&kv_full[s], 2 * C::KB);
+                uint8_t* st = sKV + s * 2 * C::KB;
+#pragma unroll
+                for (int r = 0; r < D / 64; r++) {
+                    tma_load_3d(st + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &kv_full[s]);
+                    tma_load_3d(st + C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &kv_full[s]);
+                }
+                issued = j + 1;
+            }
+            mbar_wait_drain(a_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_mma(128, C::BN, false, false);
+            const uint32_t idO = idesc_mma(128, D, false, true);
+            const uint32_t qa = smem_u32(sQ), ra = smem_u32(sR);
+            if (mbar_wait(a_full, 0, wd, 2)) {
+                for (int j = 0; j < nkt; j++) {
+                    const int s = j % NS;
+                    if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
+                    // S and R alias the previous tile's weights: wait until their MMAs finished
+                    if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, wd, 4)) break;
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB), vaddr = kaddr + C::KB;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) {
+                        const uint64_t kd = desc_kmajor(kaddr, C::BN, kk);
+                        mma_ss(tS, desc_kmajor(qa, C::BM, kk), kd, idS, kk > 0);
+                        mma_ss(tR, desc_kmajor(ra, C::BM, kk), kd, idS, kk > 0);
+                    }
+                    mma_commit(s_full);
+                    if (!mbar_wait(p_full, j & 1, wd, 5)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; kk++) {
+                        const uint64_t vd = desc_mnmajor(vaddr, C::BN, kk);
+                        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                        mma_ts(tO1, tS + kk * 8, vd, idO, acc);
+                        mma_ts(tO2, tR + kk * 8, vd, idO, acc);
+                    }
+                    mma_commit(o_done);
+                    mma_commit(&kv_empty[s]);
+                }
+            }
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0);
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int t = q0 + row;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        float m_use = -INFINITY, l = 0.f, rs = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            ok = mbar_wait(s_full, j & 1, wd, 6);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * C::BN;
+            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;  // key k0 + c valid iff c <= lim
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t v[32];
+                tmem_ld32(tS + lrow + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    if (c * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+            }
+            mx *= scale_log2;
+            const float m_new = fmaxf(m_use, mx);
+            const bool need = m_new > m_use + RESCALE_TH;
+            float alpha = 1.f;
+            if (need) {
+                alpha = fast_exp2(m_use - m_new);
+                m_use = m_new;
+            }
+            l *= alpha;
+            rs *= alpha;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok = mbar_wait(o_done, (j - 1) & 1, wd, 7);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 2 * D / 32; c++) {  // O1 and O2 are contiguous
+                    uint32_t v[32];
+                    tmem_ld32(tO1 + lrow + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st32(tO1 + lrow + c * 32, v);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t vs[32], vr[32];
+                tmem_ld32(tS + lrow + c * 32, vs);
+                tmem_ld32(tR + lrow + c * 32, vr);
+                tmem_wait_ld();
+                uint32_t pk[16], wk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    float p[2], w[2];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int cc = c * 32 + 2 * i + h;
+                        p[h] = cc <= lim ? fast_exp2(fmaf(__uint_as_float(vs[2 * i + h]), scale_log2, -m_use)) : 0.f;
+                        w[h] = p[h] * __uint_as_float(vr[2 * i + h]);
+                    }
+                    pk[i] = pack_f16(p[0], p[1]);
+                    wk[i] = pack_f16(w[0], w[1]);
+                    l += f16_lo(pk[i]) + f16_hi(pk[i]);
+                    rs += f16_lo(wk[i]) + f16_hi(wk[i]);
+                }
+                tmem_st16(tS + lrow + c * 16, pk);
+                tmem_st16(tR + lrow + c * 16, wk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok) {
+            ok = mbar_wait(o_done, (nkt - 1) & 1, wd, 8);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const float inv = 1.f / l, g = 1.f + rs * inv;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v1[32], v2[32];
+                    tmem_ld32(tO1 + lrow + c * 32, v1);
+                    tmem_ld32(tO2 + lrow + c * 32, v2);
+                    tmem_wait_ld();
+                    if (t < T) {
+                        uint4* dst = (uint4*)(out + ((size_t)bh * T + t) * D + c * 32);
+                        uint32_t o[16];
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {
+                            const float a0 = (__uint_as_float(v1[2 * i]) * g - __uint_as_float(v2[2 * i])) * inv;
+                            const float a1 =
+                                (__uint_as_float(v1[2 * i + 1]) * g - __uint_as_float(v2[2 * i + 1])) * inv;
+                            o[i] = pack_bf16(a0, a1);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; i++) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+                if (t < T) lse[(size_t)bh * T + t] = (m_use + __log2f(l)) * LN2;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 // ============================================================= row math
 // Per-row work around the attention passes, as register-tiled fp32 products
 // over blocks of 64 rows of one head (rows = the B*T queries of head h):
@@ -1755,6 +2010,34 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t probe_impl(const ProbeArgs& a) {
+    using C = ProbeCfg<D>;
+    const int BH = a.B * a.H;
+    const float scale_log2 = LOG2E / sqrtf((float)D);
+    const size_t n = (size_t)BH * a.T * D, nd2 = align256(n * 2);
+    __half* q16 = (__half*)a.ws;
+    __half* r16 = (__half*)((char*)a.ws + nd2);
+    __half* k16 = (__half*)((char*)a.ws + 2 * nd2);
+    __half* v16 = (__half*)((char*)a.ws + 3 * nd2);
+    CUtensorMap mq, mr, mk, mv;
+    if (!make_map(&mq, q16, D, a.T, BH, 128) || !make_map(&mr, r16, D, a.T, BH, 128) ||
+        !make_map(&mk, k16, D, a.T, BH, 64) || !make_map(&mv, v16, D, a.T, BH, 64))
+        return cudaErrorInvalidValue;
+    {
+        const void* src[4] = {a.q, a.rho, a.k, a.v};
+        __half* dst[4] = {q16, r16, k16, v16};
+        PLX_TRY(to_f16(src, dst, 4, n, a.stream));
+    }
+    const int ntq = (a.T + C::BM - 1) / C::BM;
+    PLX_TRY(cudaFuncSetAttribute(tc_probe_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    timing_begin(a.stream, "tc_probe");
+    tc_probe_kernel<D><<<ntq * BH, C::NT, C::SMEM, a.stream>>>(mq, mr, mk, mv, (__nv_bfloat16*)a.out, a.lse, a.T,
+                                                                BH, ntq, scale_log2, a.status);
+    timing_end(a.stream);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_available() { return encode_fn() != nullptr; }
@@ -1769,6 +2052,16 @@ size_t tc_bwd_ws_bytes(int B, int H, int T, int d) { return tc_bwd_bytes(B, H, T
 cudaError_t tc_fwd(const FwdArgs& a) {
     if (a.dtype != 1) return cudaErrorNotSupported;
     return a.d == 64 ? fwd_impl<64>(a) : fwd_impl<128>(a);
+}
+
+size_t tc_probe_ws_bytes(int B, int H, int T, int d) {
+    const size_t n = (size_t)B * H * T;
+    return 4 * align256(n * d * 2);
+}
+
+cudaError_t tc_probe(const ProbeArgs& a) {
+    if (a.dtype != 1) return cudaErrorNotSupported;
+    return a.d == 64 ? probe_impl<64>(a) : probe_impl<128>(a);
 }
 
 cudaError_t tc_bwd(const BwdArgs& a) {
