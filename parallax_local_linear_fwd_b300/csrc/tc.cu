@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
 //          vanishes for the values pass 2's MMA sees).
 //   MODE 1 (backward B2): the same u, du = R - ebar mu_k, ddelta = P_h^T du,
 //          dq_acc = ddelta, dmu = f16(-ddelta), the row scalars B3 needs
-//          {lse log2 e, 1 - mu_k . U, ebar, D} with
+//          {-lse log2 e, 1 - mu_k . U, -ebar, -D} (stored by query pairs) with
 //          D = do.o - gbar ebar + mu_k . dmu and do.o = ebar + R.u - gbar ebar
 //          (rebuilt from B1's fp32 sums, gbar = mu_k . u in fp32), and this
 //          CTA's partial dP_h = sum_rows du delta^T.
@@ -921,7 +921,7 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
                                                const float* __restrict__ R, const float* __restrict__ ebar,
                                                __half* __restrict__ U, float* __restrict__ gbar,
                                                __half* __restrict__ dmu, float* __restrict__ dq_acc,
-                                               float4* __restrict__ rowpack, float* __restrict__ dp_partial,
+                                               float* __restrict__ rowpack, float* __restrict__ dp_partial,
                                                int B, int H, int T) {
     using C = RowCfg<D>;
     constexpr int NC = C::NC, NA = C::NA, LDT = C::LDT, LDP = C::LDP, RB = C::RB;
@@ -1092,7 +1092,14 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
                 } else {
                     const float eb = ebar[row];
                     const float doo = eb + ru - gb * eb;
-                    rowpack[row] = make_float4(lse[row] * LOG2E, 1.f - gr, eb, doo - gb * eb + xx);
+                    // paired layout: pair t / 2 of head bh holds
+                    // {-L_even, -L_odd, g1_even, g1_odd, -ebar_even, -ebar_odd, -D_even, -D_odd}
+                    const int tt = r % T, half = tt & 1;
+                    float* pr = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + half;
+                    pr[0] = -lse[row] * LOG2E;
+                    pr[2] = 1.f - gr;
+                    pr[4] = -eb;
+                    pr[6] = -(doo - gb * eb + xx);
                 }
             }
         }
@@ -1184,34 +1191,70 @@ __device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t 
     return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
 }
 
-// The elementwise step for 16 queries (one 16-column chunk) of one key row.
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes
+// of work.  A pair lives in a 64-bit register; mov.b64 packs and unpacks it.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 uf2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The elementwise step for 16 queries (one 16-column chunk) of one key row,
+// two queries per f32x2 instruction.  rp points at the chunk's first query
+// pair: {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o} per pair, with
+// L = lse log2 e and g1 = 1 - gbar.
 template <bool MASK>
 __device__ __forceinline__ void b3_chunk(const uint32_t (&vs)[16], const uint32_t (&vg)[16], const uint32_t (&vy)[16],
-                                         const uint32_t (&ve)[16], const float4* rows, int qlo, float scale,
+                                         const uint32_t (&ve)[16], const float* rp, int qlo, float scale,
                                          float scale_log2, uint32_t (&o1)[16], uint32_t (&o2)[16]) {
-    // rows[qq] = {lse_t log2 e, 1 - gbar_t, ebar_t, D_t}; query qq valid iff qq >= qlo (MASK only)
+    const uint64_t SL2 = f2(scale_log2, scale_log2), SC = f2(scale, scale);
 #pragma unroll
     for (int q2 = 0; q2 < 8; q2++) {
-        float a[2], dg[2], ds[2], pp[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-            const int qq = 2 * q2 + hh;
-            const float4 rw = rows[qq];
-            float p = fast_exp2(fmaf(__uint_as_float(vs[qq]), scale_log2, -rw.x));
-            if (MASK && qq < qlo) p = 0.f;
-            const float g = __uint_as_float(vg[qq]);
-            const float e = __uint_as_float(ve[qq]);
-            const float y = __uint_as_float(vy[qq]);
-            const float w1 = g + rw.y;
-            a[hh] = p * w1;
-            dg[hh] = p * (e - rw.z);
-            ds[hh] = (p * scale) * fmaf(e, w1, fmaf(-g, rw.z, y - rw.w));
-            pp[hh] = p;
+        const float4 ra = *(const float4*)(rp + 8 * q2);
+        const float4 rb = *(const float4*)(rp + 8 * q2 + 4);
+        const uint64_t nL = f2(ra.x, ra.y), g1 = f2(ra.z, ra.w), nE = f2(rb.x, rb.y), nD = f2(rb.z, rb.w);
+        const uint64_t sv = f2(__uint_as_float(vs[2 * q2]), __uint_as_float(vs[2 * q2 + 1]));
+        const uint64_t g = f2(__uint_as_float(vg[2 * q2]), __uint_as_float(vg[2 * q2 + 1]));
+        const uint64_t y = f2(__uint_as_float(vy[2 * q2]), __uint_as_float(vy[2 * q2 + 1]));
+        const uint64_t e = f2(__uint_as_float(ve[2 * q2]), __uint_as_float(ve[2 * q2 + 1]));
+        const float2 x = uf2(ffma2(sv, SL2, nL));  // c s - L (log2 units)
+        float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+        if (MASK) {
+            if (2 * q2 < qlo) p0 = 0.f;
+            if (2 * q2 + 1 < qlo) p1 = 0.f;
         }
-        o1[q2] = pack_f16(a[0], a[1]);
-        o1[8 + q2] = pack_f16(dg[0], dg[1]);
-        o2[q2] = pack_f16(ds[0], ds[1]);
-        o2[8 + q2] = pack_f16(pp[0], pp[1]);
+        const uint64_t p = f2(p0, p1);
+        const uint64_t w1 = fadd2(g, g1);                    // 1 + g - gbar
+        const float2 a = uf2(fmul2(p, w1));                  // p w1
+        const float2 dg = uf2(fmul2(p, fadd2(e, nE)));       // p (e - ebar)
+        uint64_t tt = fadd2(y, nD);                          // y - D
+        tt = ffma2(g, nE, tt);                               // - g ebar
+        tt = ffma2(e, w1, tt);                               // + e w1
+        const float2 ds = uf2(fmul2(fmul2(p, SC), tt));      // c p (...)
+        o1[q2] = pack_f16(a.x, a.y);
+        o1[8 + q2] = pack_f16(dg.x, dg.y);
+        o2[q2] = pack_f16(ds.x, ds.y);
+        o2[8 + q2] = pack_f16(p0, p1);
     }
 }
 
@@ -1303,7 +1346,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                     tma_load_3d(blk + 2 * C::BQ * 128, &tm_dmu, r * 64, t0, bh, &st_full[s]);
                     tma_load_3d(st + C::DO_OFF + r * C::BQ * 128, &tm_do, r * 64, t0, bh, &st_full[s]);
                 }
-                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, &st_full[s]);
                 issued = j + 1;
             }
             mbar_wait_drain(kv_full, 0);
@@ -1370,7 +1413,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                 break;
             }
             tc_fence_after();
-            const float4* rows = (const float4*)(sSt + s * C::STAGE + C::ROWS_OFF);
+            const float* rows = (const float*)(sSt + s * C::STAGE + C::ROWS_OFF);  // 8 floats per query pair
             uint8_t* dsrow = sDS + (j & 1) * (C::BK * 128) + i * 128;
             const bool need_mask = t0 < k0 + C::BK || t0 + C::BQ > T;
 #pragma unroll 1
@@ -1386,7 +1429,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                     // query t = t0 + 16 c + qq is valid iff key <= t and t < T
                     const int qlo = max(key - (t0 + 16 * c), 0);
                     const int qhi = T - (t0 + 16 * c);
-                    b3_chunk<true>(vs, vg, vy, ve, rows + 16 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
+                    b3_chunk<true>(vs, vg, vy, ve, rows + 64 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
                     if (qhi < 16) {
 #pragma unroll
                         for (int x = 0; x < 8; x++) {
@@ -1398,7 +1441,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                         }
                     }
                 } else {
-                    b3_chunk<false>(vs, vg, vy, ve, rows + 16 * c, 0, scale, scale_log2, o1, o2);
+                    b3_chunk<false>(vs, vg, vy, ve, rows + 64 * c, 0, scale, scale_log2, o1, o2);
                 }
                 tmem_st16(tS + lrow + 16 * c, o1);
                 tmem_st16(tG + lrow + 16 * c, o2);
@@ -1577,7 +1620,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                 tma_load_3d(st + C::SUB, &tm_u, 0, t0, bh, &st_full[s]);
                 tma_load_3d(st + 2 * C::SUB, &tm_dmu, 0, t0, bh, &st_full[s]);
                 tma_load_3d(st + C::DO_OFF, &tm_do, 0, t0, bh, &st_full[s]);
-                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, &st_full[s]);
                 issued = j + 1;
             }
             mbar_wait_drain(kv_full, 0);
@@ -1688,7 +1731,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                 break;
             }
             tc_fence_after();
-            const float4* rows = (const float4*)(sSt + s * C::STAGE + C::ROWS_OFF);
+            const float* rows = (const float*)(sSt + s * C::STAGE + C::ROWS_OFF);  // 8 floats per query pair
             // ds row segment of this sub-chunk: column block (j & 3) >> 1, 16-byte
             // chunks 4 (j & 1) + 2 c + {0, 1} of the 128-byte row
             uint8_t* dsrow = sDS + x * C::DSB + ((j & 3) >> 1) * (C::BK * 128) + i * 128;
@@ -1705,7 +1748,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                 if (need_mask) {
                     const int qlo = max(key - (t0 + 16 * c), 0);
                     const int qhi = T - (t0 + 16 * c);
-                    b3_chunk<true>(vs, vg, vy, ve, rows + 16 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
+                    b3_chunk<true>(vs, vg, vy, ve, rows + 64 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
                     if (qhi < 16) {
 #pragma unroll
                         for (int y = 0; y < 8; y++) {
@@ -1717,7 +1760,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                         }
                     }
                 } else {
-                    b3_chunk<false>(vs, vg, vy, ve, rows + 16 * c, 0, scale, scale_log2, o1, o2);
+                    b3_chunk<false>(vs, vg, vy, ve, rows + 64 * c, 0, scale, scale_log2, o1, o2);
                 }
                 tmem_st16(tb + lrow + 16 * c, o1);
                 tmem_st16(tb + lrow + 32 + 16 * c, o2);
@@ -1833,7 +1876,7 @@ TcFwdWs tc_fwd_ws(void* ws, int B, int H, int T, int d) {
 // Workspace of the tensor-core backward.
 struct TcBwdWs {
     float *R, *dq_acc, *ebar, *partial;
-    float4* rows;
+    float* rows;  // per head ceil(T/2) query pairs x 8 floats
     __half *U, *dmu, *q16, *k16, *v16, *do16;
 };
 TcBwdWs tc_bwd_ws(void* ws, int B, int H, int T, int d) {
@@ -1849,24 +1892,27 @@ TcBwdWs tc_bwd_ws(void* ws, int B, int H, int T, int d) {
     w.v16 = (__half*)p; p += nd2;
     w.do16 = (__half*)p; p += nd2;
     w.ebar = (float*)p; p += align256(n * 4);
-    w.rows = (float4*)p; p += align256(n * 16);
+    w.rows = (float*)p; p += align256((size_t)B * H * ((T + 1) / 2) * 32);
     w.partial = (float*)p;
     return w;
 }
 size_t tc_bwd_bytes(int B, int H, int T, int d) {
     const size_t n = (size_t)B * H * T;
     const size_t nchunks = ((size_t)B * T + 511) / 512;  // RowCfg<d>::ROWS_PER_CTA
-    return 2 * align256(n * d * 4) + 6 * align256(n * d * 2) + align256(n * 4) + align256(n * 16) +
+    return 2 * align256(n * d * 4) + 6 * align256(n * d * 2) + align256(n * 4) +
+           align256((size_t)B * H * ((T + 1) / 2) * 32) +
            align256((size_t)H * nchunks * d * d * 4);
 }
 
-// Row scalars [BH][T] float4 viewed as 3-D (4, T, BH), box 4 x rows x 1.
-bool make_rows_map(CUtensorMap* m, const void* base, int T, int BH, int rows) {
+// Row scalars: per head ceil(T/2) query pairs of 8 floats, viewed as 3-D
+// (8, pairs, BH) with a box of 8 x pairs_box x 1 (no swizzle).
+bool make_rows_map(CUtensorMap* m, const void* base, int T, int BH, int pairs_box) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {4, (cuuint64_t)T, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {16, (cuuint64_t)T * 16};
-    cuuint32_t box[3] = {4, (cuuint32_t)rows, 1};
+    const cuuint64_t np = (cuuint64_t)(T + 1) / 2;
+    cuuint64_t dims[3] = {8, np, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {32, np * 32};
+    cuuint32_t box[3] = {8, (cuuint32_t)pairs_box, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -1939,7 +1985,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         !make_map(&mk128, w.k16, D, a.T, BH, 128) || !make_map(&mv128, w.v16, D, a.T, BH, 128) ||
         !make_map(&mq64, w.q16, D, a.T, BH, 64) || !make_map(&mu64, w.U, D, a.T, BH, 64) ||
         !make_map(&mdmu64, w.dmu, D, a.T, BH, 64) || !make_map(&mdo64, w.do16, D, a.T, BH, 64) ||
-        !make_rows_map(&mrows, w.rows, a.T, BH, 64))
+        !make_rows_map(&mrows, w.rows, a.T, BH, 32))
         return cudaErrorInvalidValue;
     {
         const void* src[4] = {a.q, a.k, a.v, a.dout};
@@ -1979,7 +2025,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         CUtensorMap mq32, mu32, mdmu32, mdo32, mrows32;
         if (!make_map(&mq32, w.q16, D, a.T, BH, 32) || !make_map(&mu32, w.U, D, a.T, BH, 32) ||
             !make_map(&mdmu32, w.dmu, D, a.T, BH, 32) || !make_map(&mdo32, w.do16, D, a.T, BH, 32) ||
-            !make_rows_map(&mrows32, w.rows, a.T, BH, 32))
+            !make_rows_map(&mrows32, w.rows, a.T, BH, 16))
             return cudaErrorInvalidValue;
         const int nkt = (a.T + C::BK - 1) / C::BK;
         PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3_pp, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
