@@ -174,11 +174,14 @@ __global__ void __launch_bounds__(D) dec_merge(const Tin* __restrict__ q, const 
     }
     const float mu = a / l;
     dl[j] = ldf(q + (size_t)bh * D + j) - mu;
+    // P_h staged with coalesced loads, row stride D + 1 (conflict-free row walks)
+    extern __shared__ float ps[];
+    const float* Ph = P + (size_t)h * D * D;
+    for (int e = j; e < D * D; e += D) ps[(e / D) * (D + 1) + e % D] = Ph[e];
     __syncthreads();
-    const float* Ph = P + (size_t)h * D * D + (size_t)j * D;  // row j: u_j = sum_b P[j][b] delta_b
-    float u = 0.f;
+    float u = 0.f;  // u_j = sum_b P[j][b] delta_b
 #pragma unroll 8
-    for (int k = 0; k < D; k++) u = fmaf(Ph[k], dl[k], u);
+    for (int k = 0; k < D; k++) u = fmaf(ps[j * (D + 1) + k], dl[k], u);
     float g = mu * u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
@@ -285,8 +288,11 @@ cudaError_t decode_impl(const DecodeArgs& a) {
                                                                  a.Lmax, nsplit, scale_log2, part);
     timing_end(a.stream);
     PLX_TRY(cudaGetLastError());
+    const size_t smm = sizeof(float) * D * (D + 1);
+    PLX_TRY(cudaFuncSetAttribute(dec_merge<Tin, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smm));
     timing_begin(a.stream, "dec_merge");
-    dec_merge<Tin, D><<<BH, D, 0, a.stream>>>((const Tin*)a.q, a.P, part, a.lens, a.H, a.Lmax, nsplit, a.lse, state);
+    dec_merge<Tin, D><<<BH, D, smm, a.stream>>>((const Tin*)a.q, a.P, part, a.lens, a.H, a.Lmax, nsplit, a.lse,
+                                                 state);
     timing_end(a.stream);
     PLX_TRY(cudaGetLastError());
     timing_begin(a.stream, "dec_pass2");

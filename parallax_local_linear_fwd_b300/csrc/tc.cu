@@ -50,6 +50,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes
+// of work.  A pair lives in a 64-bit register; mov.b64 packs and unpacks it.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 uf2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return (uint8_t*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
@@ -276,7 +304,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     tmem_st32(tMu + lrow + c * 32, v);
                 }
             }
-            float sum = 0.f;
+            const uint64_t SL2 = f2(scale_log2, scale_log2), NM2 = f2(-m_use, -m_use);
+            const bool need_mask = lim < C::BN;
+            uint64_t sum2 = f2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < C::BN / 32; c++) {
                 uint32_t v[32];
@@ -284,17 +314,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1: one f32x2 op each
                     const int c0 = c * 32 + 2 * i;
-                    const float p0 = c0 <= lim ? fast_exp2(fmaf(__uint_as_float(v[2 * i]), scale_log2, -m_use)) : 0.f;
-                    const float p1 =
-                        c0 + 1 <= lim ? fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), scale_log2, -m_use)) : 0.f;
-                    sum += p0 + p1;
+                    const float2 x = uf2(ffma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), SL2, NM2));
+                    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    if (need_mask) {
+                        if (c0 > lim) p0 = 0.f;
+                        if (c0 + 1 > lim) p1 = 0.f;
+                    }
+                    const uint64_t p2 = f2(p0, p1);
+                    sum2 = fadd2(sum2, p2);
                     pk[i] = pack_f16(p0, p1);
                 }
                 tmem_st16(tS + lrow + c * 16, pk);
             }
-            l += sum;
+            const float2 sp = uf2(sum2);
+            l += sp.x + sp.y;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_full);
@@ -549,7 +584,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const bool valid = t < T;
         const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
         const float g1 = (MODE == 0 && valid) ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
-        float rowsum = 0.f;
+        const uint64_t SL2 = f2(scale_log2, scale_log2), NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+        uint64_t rs2 = f2(0.f, 0.f);  // row sum of the rounded weights, as an (even, odd) pair
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
             ok = mbar_wait(s_full, j & 1, wd, 6);
@@ -560,6 +596,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             tc_fence_after();
             const int k0 = j * C::BN;
             const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+            const bool need_mask = lim < C::BN;
 #pragma unroll
             for (int c = 0; c < C::BN / 32; c++) {
                 uint32_t vs[32], vx[32];
@@ -568,20 +605,21 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float w[2];
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        const int cc = c * 32 + 2 * i + h;
-                        const float p =
-                            cc <= lim ? fast_exp2(fmaf(__uint_as_float(vs[2 * i + h]), scale_log2, -L2)) : 0.f;
-                        const float x = __uint_as_float(vx[2 * i + h]);
-                        w[h] = MODE == 0 ? p * (x + g1) : p * x;
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
+                    const int cc = c * 32 + 2 * i;
+                    const float2 xs = uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])),
+                                                SL2, NL2));
+                    float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
+                    if (need_mask) {
+                        if (cc > lim) p0 = 0.f;
+                        if (cc + 1 > lim) p1 = 0.f;
                     }
-                    pk[i] = pack_f16(w[0], w[1]);
+                    const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
+                    const float2 w = uf2(MODE == 0 ? fmul2(f2(p0, p1), fadd2(xv, G1)) : fmul2(f2(p0, p1), xv));
+                    pk[i] = pack_f16(w.x, w.y);
                     // ebar sums the rounded weights the MMA sees, so that
                     // R - ebar mu_k = sum_i w_i (k_i - mu_k) holds for them.
-                    if (MODE == 1) rowsum += f16_lo(pk[i]) + f16_hi(pk[i]);
+                    if (MODE == 1) rs2 = fadd2(rs2, f2(f16_lo(pk[i]), f16_hi(pk[i])));
                 }
                 tmem_st16(tS + lrow + c * 16, pk);
             }
@@ -618,7 +656,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         }
                     }
                 }
-                if (MODE == 1 && valid) ebar_out[(size_t)bh * T + t] = rowsum;
+                if (MODE == 1 && valid) {
+                    const float2 r2 = uf2(rs2);
+                    ebar_out[(size_t)bh * T + t] = r2.x + r2.y;
+                }
             }
         }
     }
@@ -1105,14 +1146,15 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
         }
         if (MODE) {
             // dP_h partial: dp[a][b] += sum over the block's rows du[r][a] delta[r][b],
-            // a in NA ty + [0, NA), b in NA tx + [0, NA)
+            // a = ty + 16 ii, b = tx + 16 jj (strided ownership: a half-warp reads 16
+            // consecutive transposed rows, which the row stride spreads over all banks)
 #pragma unroll 2
             for (int r = 0; r < RB; r += 4) {
                 float4 ya[NA], xb[NA];
 #pragma unroll
-                for (int ii = 0; ii < NA; ii++) ya[ii] = *(const float4*)&YT[(NA * ty + ii) * LDT + r];
+                for (int ii = 0; ii < NA; ii++) ya[ii] = *(const float4*)&YT[(ty + 16 * ii) * LDT + r];
 #pragma unroll
-                for (int jj = 0; jj < NA; jj++) xb[jj] = *(const float4*)&XT[(NA * tx + jj) * LDT + r];
+                for (int jj = 0; jj < NA; jj++) xb[jj] = *(const float4*)&XT[(tx + 16 * jj) * LDT + r];
 #pragma unroll
                 for (int ii = 0; ii < NA; ii++)
 #pragma unroll
@@ -1128,9 +1170,7 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
 #pragma unroll
         for (int ii = 0; ii < NA; ii++)
 #pragma unroll
-            for (int jj = 0; jj < NA; jj += 4)
-                *(float4*)&dst[(NA * ty + ii) * D + NA * tx + jj] =
-                    make_float4(dp[ii][jj], dp[ii][jj + 1], dp[ii][jj + 2], dp[ii][jj + 3]);
+            for (int jj = 0; jj < NA; jj++) dst[(ty + 16 * ii) * D + tx + 16 * jj] = dp[ii][jj];
     }
 }
 
@@ -1189,34 +1229,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // MN-major operand descriptor with an explicit leading (N-block) byte offset.
 __device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t lbo) {
     return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
-}
-
-// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes
-// of work.  A pair lives in a 64-bit register; mov.b64 packs and unpacks it.
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float2 uf2(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
 }
 
 // The elementwise step for 16 queries (one 16-column chunk) of one key row,
