@@ -1545,15 +1545,16 @@ struct B3P {
     static constexpr int STAGE_BYTES = ROWS_OFF + BQ * 16;
     static constexpr int STAGE = 17 * 1024;        // stage stride (1024-aligned)
     static constexpr int DSB = BK * QT * 2;        // one ds tile, f16 [keys][128 queries]
+    static constexpr int DQB = QT * D * 4;         // dQ staging: two 32-column boxes, 128-byte swizzle
     static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 2 + 2 + 2;
-    static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + NS * STAGE + NBAR * 8 + 16;
+    static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + DQB + NS * STAGE + NBAR * 8 + 16;
 };
 
 __global__ void __launch_bounds__(B3P::NT, 1)
     tc_bwd_b3_pp(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
                  const __grid_constant__ CUtensorMap tm_dmu, const __grid_constant__ CUtensorMap tm_do,
-                 const __grid_constant__ CUtensorMap tm_rows, float* __restrict__ dq_acc,
+                 const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_dq,
                  __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T, int BH, int nkt, float scale,
                  float scale_log2, unsigned* status) {
     using C = B3P;
@@ -1563,7 +1564,8 @@ __global__ void __launch_bounds__(B3P::NT, 1)
     uint8_t* sK = sm;
     uint8_t* sV = sK + C::KB;
     uint8_t* sDS = sV + C::KB;  // two ds tiles
-    uint8_t* sSt = sDS + 2 * C::DSB;
+    uint8_t* sDQ = sDS + 2 * C::DSB;  // dQ staging for the tensor reduce-add
+    uint8_t* sSt = sDQ + C::DQB;
     uint64_t* bars = (uint64_t*)(sSt + NS * C::STAGE);
     uint64_t* kv_full = bars;
     uint64_t* st_full = bars + 1;
@@ -1703,26 +1705,36 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         const uint32_t lrow = (uint32_t)(qd * 32) << 16;
         const uint32_t tb = tmem + 128 * wg;
         // dQ of the 128-query tile m: thread = query row i; reduced into dq_acc
+        // dQ of the 128-query tile m (thread = query row i): staged in shared
+        // memory and added into the fp32 accumulator by one tensor reduce-add
+        // per 32-column box (rows past T are clipped by the tensor map).
         auto read_dq = [&](int m) -> bool {
             const bool got = mbar_wait(dq_full, m & 1, wd, 9);
             if (!__all_sync(0xffffffffu, got)) return false;
             tc_fence_after();
-            const int t = k0 + m * C::QT + i;
+            const bool leader = warp == 6 && lane == 0;
+            if (leader) bulk_wait_read_all();  // the previous tile's reduce has read the staging
+            named_bar_sync(2, 128);
 #pragma unroll 1
             for (int c = 0; c < D / 32; c++) {
                 uint32_t v[32];
                 tmem_ld32(tDQ + lrow + 32 * c, v);
                 tmem_wait_ld();
-                if (t < T) {
-                    float* dst = dq_acc + ((size_t)bh * T + t) * D + 32 * c;
+                uint8_t* box = sDQ + c * (C::QT * 128) + i * 128;
 #pragma unroll
-                    for (int y = 0; y < 32; y += 4)
-                        red_add_v4(dst + y, __uint_as_float(v[y]), __uint_as_float(v[y + 1]),
-                                   __uint_as_float(v[y + 2]), __uint_as_float(v[y + 3]));
-                }
+                for (int y = 0; y < 8; y++)
+                    *(uint4*)(box + ((y ^ (i & 7)) << 4)) = make_uint4(v[4 * y], v[4 * y + 1], v[4 * y + 2], v[4 * y + 3]);
             }
             tc_fence_before();
             mbar_arrive(dq_free);
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            if (leader) {
+#pragma unroll
+                for (int c = 0; c < D / 32; c++)
+                    tma_reduce_add_3d(&tm_dq, 32 * c, k0 + m * C::QT, bh, sDQ + c * (C::QT * 128));
+                bulk_commit();
+            }
             return true;
         };
         bool ok = true;
@@ -1788,6 +1800,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         }
         // warpgroup 1 reads every dQ tile in order; the last one may be partial
         if (ok && wg == 1 && ((nsub - 1) & 3) != 3) ok = read_dq((nsub - 1) >> 2);
+        if (wg == 1 && warp == 6 && lane == 0) bulk_wait_all();  // staging must outlive its reduces
         if (ok) {
             ok = mbar_wait(fin, 0, wd, 10);
             if (__all_sync(0xffffffffu, ok)) {
@@ -2034,7 +2047,18 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     }
     if (D == 64) {  // B3: dK, dV, dQ (ping-pong form)
         using C = B3P;
-        CUtensorMap mq32, mu32, mdmu32, mdo32, mrows32;
+        CUtensorMap mq32, mu32, mdmu32, mdo32, mrows32, mdq;
+        {
+            EncodeTiledFn fn = encode_fn();
+            cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.T, (cuuint64_t)BH};
+            cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)a.T * D * 4};
+            cuuint32_t box[3] = {32, (cuuint32_t)C::QT, 1};
+            cuuint32_t es[3] = {1, 1, 1};
+            if (!fn || fn(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, w.dq_acc, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
         if (!make_map(&mq32, w.q16, D, a.T, BH, 32) || !make_map(&mu32, w.U, D, a.T, BH, 32) ||
             !make_map(&mdmu32, w.dmu, D, a.T, BH, 32) || !make_map(&mdo32, w.do16, D, a.T, BH, 32) ||
             !make_rows_map(&mrows32, w.rows, a.T, BH, 16))
@@ -2043,7 +2067,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3_pp, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b3");
         tc_bwd_b3_pp<<<nkt * BH, C::NT, C::SMEM, a.stream>>>(mk128, mv128, mq32, mu32, mdmu32, mdo32, mrows32,
-                                                              w.dq_acc, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
+                                                              mdq, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
                                                               a.T, BH, nkt, scale, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
