@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 for (int j = 0; j < nkt; j++) {
                     const int s = j % NS;
                     if (!mbar_wait(&k_full[s], (j / NS) & 1, wd, 3)) break;
-                    // S aliases the previous tile's P~: wait until that MMA finished.
-                    if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, wd, 4)) break;
+                    // S aliases the previous tile's P~; tcgen05.mma ops issued by one
+                    // thread execute in issue order, so no wait for that MMA here.
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sK + s * C::KB);
 #pragma unroll
@@ -551,7 +551,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 for (int j = 0; j < nkt; j++) {
                     const int s = j % NS;
                     if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
-                    if (j > 0 && !mbar_wait(acc_done, (j - 1) & 1, wd, 4)) break;
+                    // S aliases the previous tile's weights; tcgen05.mma ops issued by
+                    // one thread execute in issue order, so no wait for that MMA here.
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
                     const uint32_t vaddr = kaddr + C::KB;
@@ -781,8 +782,8 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
                 for (int j = 0; j < nkt; j++) {
                     const int s = j % NS;
                     if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
-                    // S and R alias the previous tile's weights: wait until their MMAs finished
-                    if (j > 0 && !mbar_wait(o_done, (j - 1) & 1, wd, 4)) break;
+                    // S and R alias the previous tile's weights; tcgen05.mma ops issued by
+                    // one thread execute in issue order, so no wait for those MMAs here.
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB), vaddr = kaddr + C::KB;
 #pragma unroll
@@ -861,6 +862,9 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
                     tmem_st32(tO1 + lrow + c * 32, v);
                 }
             }
+            const uint64_t SL2 = f2(scale_log2, scale_log2), NM2 = f2(-m_use, -m_use);
+            const bool need_mask = lim < C::BN;
+            uint64_t l2 = f2(0.f, 0.f), rs2 = f2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < C::BN / 32; c++) {
                 uint32_t vs[32], vr[32];
@@ -869,21 +873,29 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
                 tmem_wait_ld();
                 uint32_t pk[16], wk[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float p[2], w[2];
-#pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        const int cc = c * 32 + 2 * i + h;
-                        p[h] = cc <= lim ? fast_exp2(fmaf(__uint_as_float(vs[2 * i + h]), scale_log2, -m_use)) : 0.f;
-                        w[h] = p[h] * __uint_as_float(vr[2 * i + h]);
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1: one f32x2 op each
+                    const int cc = c * 32 + 2 * i;
+                    const float2 x =
+                        uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NM2));
+                    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    if (need_mask) {
+                        if (cc > lim) p0 = 0.f;
+                        if (cc + 1 > lim) p1 = 0.f;
                     }
-                    pk[i] = pack_f16(p[0], p[1]);
-                    wk[i] = pack_f16(w[0], w[1]);
-                    l += f16_lo(pk[i]) + f16_hi(pk[i]);
-                    rs += f16_lo(wk[i]) + f16_hi(wk[i]);
+                    const uint64_t p2 = f2(p0, p1);
+                    const float2 w = uf2(fmul2(p2, f2(__uint_as_float(vr[2 * i]), __uint_as_float(vr[2 * i + 1]))));
+                    pk[i] = pack_f16(p0, p1);
+                    wk[i] = pack_f16(w.x, w.y);
+                    l2 = fadd2(l2, f2(f16_lo(pk[i]), f16_hi(pk[i])));
+                    rs2 = fadd2(rs2, f2(f16_lo(wk[i]), f16_hi(wk[i])));
                 }
                 tmem_st16(tS + lrow + c * 16, pk);
                 tmem_st16(tR + lrow + c * 16, wk);
+            }
+            {
+                const float2 a2 = uf2(l2), b2 = uf2(rs2);
+                l += a2.x + a2.y;
+                rs += b2.x + b2.y;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -1375,7 +1387,8 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                 for (int j = 0; j < nsub; j++) {
                     const int s = j % NS;
                     if (!mbar_wait(&st_full[s], (j / NS) & 1, wd, 3)) break;
-                    if (j > 0 && !mbar_wait(acc_done, (j - 1) & 1, wd, 4)) break;
+                    // the scores overwrite the previous sub-chunk's weight operands;
+                    // tcgen05.mma ops issued by one thread execute in issue order
                     if (j > 0 && (j & 1) == 0 && !mbar_wait(dq_free, ((j >> 1) - 1) & 1, wd, 5)) break;
                     tc_fence_after();
                     const uint32_t st = smem_u32(sSt + s * C::STAGE);
@@ -1652,7 +1665,8 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                 if (j < nsub) {
                     const int s = j % NS, b = j & 1;
                     if (!mbar_wait(&st_full[s], (j / NS) & 1, wd, 3)) break;
-                    if (j >= 2 && !mbar_wait(&acc_done[b], ((j >> 1) - 1) & 1, wd, 4)) break;
+                    // buffer b's weight operands were read by the accumulation of j - 2,
+                    // issued earlier by this thread: MMAs execute in issue order
                     tc_fence_after();
                     const uint32_t st = smem_u32(sSt + s * C::STAGE);
                     const uint32_t tb = tmem + 128 * b;
