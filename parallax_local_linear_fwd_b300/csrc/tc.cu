@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
                     for (int kk = 0; kk < C::BN / 16; kk++)
                         mma_ts(tAcc, tS + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(acc_done);
+                    if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
                     mma_commit(&kv_empty[s]);
                 }
             }
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             mbar_arrive(w_full);
         }
         if (ok) {
-            ok = mbar_wait(acc_done, (nkt - 1) & 1, wd, 8);
+            ok = mbar_wait(acc_done, 0, wd, 8);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
 #pragma unroll
@@ -1409,7 +1409,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                         mma_ts(tDK, tG + 16 * kk, desc_mn_lbo(st, kk, C::QUM_B), idA, 1u);
                         mma_ts(tDK, tG + 16 * kk + 8, desc_mn_lbo(st + 2 * C::BQ * 128, kk, C::QUM_B), idA, 1u);
                     }
-                    mma_commit(acc_done);
+                    if (j == nsub - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
                     mma_commit(&st_empty[s]);
                     if ((j & 1) == 1 || j == nsub - 1) {
 #pragma unroll
@@ -1508,7 +1508,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
             }
         }
         if (ok) {
-            ok = mbar_wait(acc_done, (nsub - 1) & 1, wd, 9);
+            ok = mbar_wait(acc_done, 0, wd, 9);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 // warpgroup 0 writes dV, warpgroup 1 writes dK
@@ -1559,7 +1559,7 @@ struct B3P {
     static constexpr int STAGE = 17 * 1024;        // stage stride (1024-aligned)
     static constexpr int DSB = BK * QT * 2;        // one ds tile, f16 [keys][128 queries]
     static constexpr int DQB = QT * D * 4;         // dQ staging: two 32-column boxes, 128-byte swizzle
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 2 + 2 + 2;
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 4;
     static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + DQB + NS * STAGE + NBAR * 8 + 16;
 };
 
@@ -1585,8 +1585,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
     uint64_t* st_empty = st_full + NS;
     uint64_t* sc_full = st_empty + NS;   // [2], per score buffer
     uint64_t* op_full = sc_full + 2;     // [2]
-    uint64_t* acc_done = op_full + 2;    // [2]
-    uint64_t* ds_free = acc_done + 2;    // [2], per ds tile
+    uint64_t* ds_free = op_full + 2;     // [2], per ds tile
     uint64_t* dq_full = ds_free + 2;
     uint64_t* dq_free = dq_full + 1;
     uint64_t* drain = dq_free + 1;
@@ -1611,7 +1610,6 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         for (int b = 0; b < 2; b++) {
             mbar_init(&sc_full[b], 1);
             mbar_init(&op_full[b], 128);
-            mbar_init(&acc_done[b], 1);
             mbar_init(&ds_free[b], 1);
         }
         mbar_init(dq_full, 1);
@@ -1692,7 +1690,6 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                         mma_ts(tDK, tb + 32 + 16 * kk, desc_mnmajor(st, C::BQ, kk), idA, 1u);
                         mma_ts(tDK, tb + 32 + 16 * kk + 8, desc_mnmajor(st + 2 * C::SUB, C::BQ, kk), idA, 1u);
                     }
-                    mma_commit(&acc_done[bp]);
                     mma_commit(&st_empty[sp]);
                     if (jp == nsub - 1) mma_commit(fin);
                     if ((jp & 3) == 3 || jp == nsub - 1) {
