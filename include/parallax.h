@@ -192,6 +192,34 @@ PLX_API int parallax_decode(const void* q, const void* k_cache, const void* v_ca
 PLX_API size_t parallax_decode_workspace_bytes(int B, int H, int Lmax, int d, int dtype);
 
 /*
+ * Forward and backward of the layer from HOST buffers, with the copies
+ * overlapped with the compute.  The paper has no counterpart: this entry
+ * serves callers whose tensors live in host memory.  The heads are split into
+ * `chunks` groups (0 = min(H, 8)).  Every group's inputs are copied in on an
+ * internal stream, the group's parallax_fwd + parallax_bwd runs on `stream`
+ * as soon as its inputs have arrived, and its results are copied out on a
+ * second internal stream while later groups compute.  dP_h sums over the
+ * batch only, so each group's dP rows are complete within the group, and
+ * every group runs exactly the arithmetic of parallax_fwd + parallax_bwd on
+ * device copies (dq, whose fp32 accumulation order varies between runs,
+ * agrees to its last bit of rounding).
+ *   q, k, v, dout: host, [B][H][T][d] in dtype.   P: host, [H][d][d] float32.
+ *   out, dq, dk, dv: host, [B][H][T][d] in dtype.   dP: host, [H][d][d] float32.
+ *   lse: host, [B][H][T] float32, or NULL (not returned).
+ *   mu_k: host, [B][H][T][d] float32, or NULL (not returned).
+ * Every pointer must be host memory (PLX_ERR_INVALID_ARG otherwise); use
+ * pinned memory (cudaHostAlloc / cudaHostRegister): copies from or to
+ * pageable memory are correct but do not overlap.  Device memory (the
+ * tensors of all groups plus one workspace for the largest group) is taken
+ * stream-ordered on `stream` and freed before returning.  The call is
+ * asynchronous: the outputs are complete once `stream` has reached the
+ * point where the call was made.  Returns PLX_OK or an error code.
+ */
+PLX_API int parallax_step_host(const void* q, const void* k, const void* v, const float* P, const void* dout,
+                       void* out, float* lse, float* mu_k, void* dq, void* dk, void* dv, float* dP,
+                       int chunks, int B, int H, int T, int d, int dtype, void* stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the current device's watchdog
  * word.  Returns PLX_OK, PLX_ERR_TIMEOUT (a bounded wait inside a kernel gave
  * up; the kernel skipped its remaining work and released its resources) or

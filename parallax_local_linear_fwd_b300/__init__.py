@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "PLX_OK", "PLX_ERR_INVALID_ARG", "PLX_ERR_UNSUPPORTED", "PLX_ERR_CUDA", "PLX_ERR_TIMEOUT",
-    "PLX_ERR_TOO_LARGE", "parallax_fwd_noalloc",
+    "PLX_ERR_TOO_LARGE", "parallax_fwd_noalloc", "parallax_step_host",
     "PLX_FP32", "PLX_BF16", "PLX_PATH_AUTO", "PLX_PATH_SIMT", "PLX_PATH_TC",
     "PlxError", "PlxLibraryMissing", "lib", "lib_path", "exported_symbols",
     "parallax_fwd", "parallax_fwd_ws", "parallax_bwd", "parallax_fwd_workspace_bytes",
@@ -59,6 +59,7 @@ _SIGNATURES = {
     "parallax_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_fwd_probe": (_i, [_vp] * 7 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "parallax_step_host": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _i, _vp]),
 }
 
 
@@ -231,6 +232,34 @@ def parallax_decode(q, k_cache, v_cache, P, lens=None, out=None, lse=None, works
                                  _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
            "parallax_decode")
     return out, lse
+
+
+def parallax_step_host(q, k, v, P, dout, out=None, dq=None, dk=None, dv=None, dP=None, lse=None, mu_k=None,
+                       chunks=0, stream=None):
+    """Forward + backward from host (CPU) tensors, copies overlapped with compute.
+
+    q, k, v, dout: [B,H,T,d] float32/bfloat16 CPU tensors (pinned for overlap); P [H,d,d] float32.
+    Outputs (allocated pinned when None): out, dq, dk, dv like q, dP like P.  lse [B,H,T] and
+    mu_k [B,H,T,d] float32 are returned only when passed in.  The call is asynchronous on
+    `stream`: synchronize it before reading the outputs.  Returns (out, dq, dk, dv, dP, lse, mu_k).
+    """
+    B, H, T, d = _shape(q)
+    for t in (q, k, v, P, dout, out, dq, dk, dv, dP, lse, mu_k):
+        if t is not None and t.device.type != "cpu":
+            raise ValueError("parallax_step_host takes host (CPU) tensors")
+
+    def alloc(like):
+        return torch.empty(like.shape, dtype=like.dtype).pin_memory()
+
+    out = alloc(q) if out is None else out
+    dq = alloc(q) if dq is None else dq
+    dk = alloc(k) if dk is None else dk
+    dv = alloc(v) if dv is None else dv
+    dP = alloc(P) if dP is None else dP
+    _check(lib().parallax_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(dout), _ptr(out), _ptr(lse),
+                                    _ptr(mu_k), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), int(chunks),
+                                    B, H, T, d, _dtype_code(q), _stream_ptr(stream)), "parallax_step_host")
+    return out, dq, dk, dv, dP, lse, mu_k
 
 
 def parallax_last_device_error(stream=None):

@@ -100,6 +100,30 @@ int fwd_common(const void* q, const void* k, const void* v, const float* P, void
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
+
+// ------------------------------------------------------------- host step
+// Heads [h0, h0 + nh) of a [B][H][rows] host tensor (row_bytes per head)
+// against the chunk's own [B][nh][rows] device region.
+cudaError_t copy_heads(void* host, void* dev, bool to_device, size_t row_bytes, int B, int H, int h0, int nh,
+                       cudaStream_t s) {
+    const size_t part = (size_t)nh * row_bytes, full = (size_t)H * row_bytes;
+    char* h = (char*)host + (size_t)h0 * row_bytes;
+    if (to_device) return cudaMemcpy2DAsync(dev, part, h, full, part, (size_t)B, cudaMemcpyHostToDevice, s);
+    return cudaMemcpy2DAsync(h, full, dev, part, part, (size_t)B, cudaMemcpyDeviceToHost, s);
+}
+
+// True for host memory (pinned, registered or pageable), false for device or
+// managed memory.
+bool is_host(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
+
 // ------------------------------------------------------------- timing
 struct Pending {
     int kid;
@@ -320,6 +344,129 @@ int parallax_decode(const void* q, const void* k_cache, const void* v_cache, con
         cudaError_t e2 = cudaFreeAsync(ws, s);
         if (e == cudaSuccess) e = e2;
     }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
+int parallax_step_host(const void* q, const void* k, const void* v, const float* P, const void* dout, void* out,
+                       float* lse, float* mu_k, void* dq, void* dk, void* dv, float* dP, int chunks, int B, int H,
+                       int T, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, T, d, dtype);
+    if (rc) return rc;
+    if (!q || !k || !v || !P || !dout || !out || !dq || !dk || !dv || !dP) return PLX_ERR_INVALID_ARG;
+    if (chunks < 0 || chunks > H) return PLX_ERR_INVALID_ARG;
+    {
+        const void* host_ptrs[] = {q, k, v, P, dout, out, dq, dk, dv, dP, lse, mu_k};
+        for (const void* p : host_ptrs)
+            if (p && !is_host(p)) return PLX_ERR_INVALID_ARG;
+    }
+    const int fam = pick_family(dtype);
+    if (fam < 0) return -fam;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    if (chunks == 0) chunks = H < 8 ? H : 8;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t es = dtype == PLX_BF16 ? 2 : 4;
+    const size_t act_row = (size_t)T * d * es, f32_row = (size_t)T * d * 4, lse_row = (size_t)T * 4;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+
+    // chunk c holds heads [h0[c], h0[c] + nh[c]); every tensor of a chunk starts 256-byte aligned
+    enum { Q, K, V, DO, OUT, DQ, DK, DV, MU, LSE, NT_ };
+    std::vector<int> h0(chunks), nh(chunks);
+    std::vector<size_t> off((size_t)chunks * NT_);
+    size_t total = 0;
+    for (int c = 0, h = 0; c < chunks; c++) {
+        nh[c] = H / chunks + (c < H % chunks ? 1 : 0);
+        h0[c] = h;
+        h += nh[c];
+        for (int t = 0; t < NT_; t++) {
+            const size_t row = t == MU ? f32_row : (t == LSE ? lse_row : act_row);
+            off[(size_t)c * NT_ + t] = total;
+            total += up((size_t)B * nh[c] * row);
+        }
+    }
+    const size_t hmax = (size_t)(H + chunks - 1) / chunks;
+    const size_t pd_bytes = (size_t)H * d * d * 4;
+    const size_t o_P = total, o_dP = o_P + up(pd_bytes), o_ws = o_dP + up(pd_bytes);
+    size_t ws_bytes = fwd_ws_for(fam, B, (int)hmax, T, d);
+    const size_t bw = bwd_ws_for(fam, B, (int)hmax, T, d);
+    if (bw > ws_bytes) ws_bytes = bw;
+    total = o_ws + up(ws_bytes);
+
+    char* base = nullptr;
+    if (cudaMallocAsync((void**)&base, total, s) != cudaSuccess) return PLX_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    auto chk = [&](cudaError_t x) {
+        if (e == cudaSuccess && x != cudaSuccess) e = x;
+        return e == cudaSuccess;
+    };
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    std::vector<cudaEvent_t> ev((size_t)2 * chunks + 2, nullptr);
+    chk(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking));
+    chk(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+    for (auto& x : ev) chk(cudaEventCreateWithFlags(&x, cudaEventDisableTiming));
+    cudaEvent_t e_alloc = ev[0], e_end = ev[1];
+    cudaEvent_t* e_in = ev.data() + 2;
+    cudaEvent_t* e_comp = ev.data() + 2 + chunks;
+    auto dev = [&](int c, int t) { return (void*)(base + off[(size_t)c * NT_ + t]); };
+    float* Pd = (float*)(base + o_P);
+    float* dPd = (float*)(base + o_dP);
+    void* ws = base + o_ws;
+
+    // copy engine in: P, then every chunk's inputs back to back
+    if (chk(cudaEventRecord(e_alloc, s)) && chk(cudaStreamWaitEvent(s_in, e_alloc, 0)) &&
+        chk(cudaMemcpyAsync(Pd, P, pd_bytes, cudaMemcpyHostToDevice, s_in))) {
+        const void* src[4] = {q, k, v, dout};
+        for (int c = 0; c < chunks && e == cudaSuccess; c++) {
+            for (int t = Q; t <= DO; t++)
+                if (!chk(copy_heads((void*)src[t], dev(c, t), true, act_row, B, H, h0[c], nh[c], s_in))) break;
+            chk(cudaEventRecord(e_in[c], s_in));
+        }
+    }
+    // compute on the caller's stream, chunk by chunk; copy engine out behind it
+    for (int c = 0; c < chunks && e == cudaSuccess; c++) {
+        if (!chk(cudaStreamWaitEvent(s, e_in[c], 0))) break;
+        const float* Pc = Pd + (size_t)h0[c] * d * d;
+        plx::FwdArgs fa{dev(c, Q), dev(c, K), dev(c, V), Pc, dev(c, OUT), (float*)dev(c, LSE), (float*)dev(c, MU),
+                        ws, B, nh[c], T, d, dtype, s, status};
+        if (!chk(fam == 2 ? plx::tc_fwd(fa) : plx::simt_fwd(fa))) break;
+        plx::BwdArgs ba{dev(c, Q), dev(c, K), dev(c, V), Pc, (const float*)dev(c, LSE), (const float*)dev(c, MU),
+                        dev(c, DO), dev(c, DQ), dev(c, DK), dev(c, DV), dPd + (size_t)h0[c] * d * d, ws,
+                        B, nh[c], T, d, dtype, s, status};
+        if (!chk(fam == 2 ? plx::tc_bwd(ba) : plx::simt_bwd(ba))) break;
+        if (!chk(cudaEventRecord(e_comp[c], s)) || !chk(cudaStreamWaitEvent(s_out, e_comp[c], 0))) break;
+        void* dst[4] = {out, dq, dk, dv};
+        for (int t = OUT; t <= DV; t++)
+            if (!chk(copy_heads(dst[t - OUT], dev(c, t), false, act_row, B, H, h0[c], nh[c], s_out))) break;
+        if (mu_k) chk(copy_heads(mu_k, dev(c, MU), false, f32_row, B, H, h0[c], nh[c], s_out));
+        if (lse) chk(copy_heads(lse, dev(c, LSE), false, lse_row, B, H, h0[c], nh[c], s_out));
+        chk(cudaMemcpyAsync(dP + (size_t)h0[c] * d * d, dPd + (size_t)h0[c] * d * d, (size_t)nh[c] * d * d * 4,
+                            cudaMemcpyDeviceToHost, s_out));
+    }
+    // the caller's stream orders after both copy streams, then frees the memory
+    cudaError_t e2 = cudaSuccess;
+    if (s_in && s_out && ev[0] && ev[1]) {
+        cudaError_t a = cudaEventRecord(e_alloc, s_in);
+        cudaError_t b = a == cudaSuccess ? cudaStreamWaitEvent(s, e_alloc, 0) : a;
+        cudaError_t c2 = cudaEventRecord(e_end, s_out);
+        cudaError_t d2 = c2 == cudaSuccess ? cudaStreamWaitEvent(s, e_end, 0) : c2;
+        e2 = b != cudaSuccess ? b : d2;
+    }
+    if (e == cudaSuccess) e = e2;
+    if (e2 == cudaSuccess) {
+        cudaError_t f = cudaFreeAsync(base, s);
+        if (e == cudaSuccess) e = f;
+    } else {
+        // the copy streams could not be joined: wait for them before freeing
+        if (s_in) cudaStreamSynchronize(s_in);
+        if (s_out) cudaStreamSynchronize(s_out);
+        cudaStreamSynchronize(s);
+        cudaFree(base);
+    }
+    for (auto& x : ev)
+        if (x) cudaEventDestroy(x);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
