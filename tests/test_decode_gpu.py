@@ -59,6 +59,17 @@ def test_decode_ragged_lengths(d, dtype):
     assert np.isfinite(go).all()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_lengths_across_key_blocks(d):
+    # a cache of 1100 keys spans several key blocks per head, so some blocks
+    # lie wholly past a short sequence and others end one key into a block
+    B, H, L = 5, 2, 1100
+    lens = [1, 513, 1100, 600, 257]
+    go, gl, ro, rl = _case(B, H, L, d, "bf16", lens, seed=60 + d)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+
+
 def test_decode_without_lengths_uses_the_whole_cache():
     go, gl, ro, rl = _case(2, 3, 200, 64, "bf16", None, seed=7)
     assert rel_err(go, ro, "bf16") < TOL_BF16
