@@ -1002,44 +1002,77 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
 #pragma unroll
         for (int j = 0; j < NA; j++) dp[i][j] = 0.f;
 
-    for (int r0 = r_begin; r0 < r_end; r0 += RB) {
-        __syncthreads();
-        {
-            // 4 threads per row, CPT consecutive columns each, vector loads
-            constexpr int CPT = C::CPT;
-            const int rr = tid >> 2, c0 = (tid & 3) * CPT, r = r0 + rr;
-            if (r < r_end) {
-                const size_t base = (((size_t)(r / T) * H + h) * T + r % T) * D + c0;
-                const float eb = MODE ? ebar[base / D] : 0.f;
+    // Block loads: 4 threads per row, CPT consecutive columns each, 16-byte
+    // loads into registers (fetch), then transposed into shared memory (put).
+    // At d = 64 the next block's loads are issued as soon as the current
+    // block is in shared memory, so they complete under this block's math.
+    constexpr int CPT = C::CPT;
+    constexpr bool kPrefetch = D == 64;
+    struct Rows {
+        uint4 qv[CPT / 8];
+        float4 m[CPT / 4];
+        float4 rv[MODE ? CPT / 4 : 1];
+        float eb;
+        bool ok;
+    };
+    const int rr = tid >> 2, c0 = (tid & 3) * CPT;
+    auto fetch = [&](int r0_, Rows& x) {
+        const int r = r0_ + rr;
+        x.ok = r < r_end;
+        if (!x.ok) return;
+        const size_t base = (((size_t)(r / T) * H + h) * T + r % T) * D + c0;
+        x.eb = MODE ? ebar[base / D] : 0.f;
 #pragma unroll
-                for (int k = 0; k < CPT; k += 8) {
-                    const uint4 qv = *(const uint4*)&q[base + k];
-                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                    float m[8], rv[8];
-                    *(float4*)&m[0] = *(const float4*)&mu_k[base + k];
-                    *(float4*)&m[4] = *(const float4*)&mu_k[base + k + 4];
-                    if (MODE) {
-                        *(float4*)&rv[0] = *(const float4*)&R[base + k];
-                        *(float4*)&rv[4] = *(const float4*)&R[base + k + 4];
-                    }
+        for (int k = 0; k < CPT / 8; k++) x.qv[k] = *(const uint4*)&q[base + 8 * k];
 #pragma unroll
-                    for (int x = 0; x < 8; x++) {
-                        const float qf = (x & 1) ? bf16_hi(qw[x >> 1]) : bf16_lo(qw[x >> 1]);
-                        XT[(c0 + k + x) * LDT + rr] = qf - m[x];
-                        if (MODE) YT[(c0 + k + x) * LDT + rr] = rv[x] - eb * m[x];
-                    }
-                    if (kMu) {
-                        *(float4*)&MS[rr * LDP + c0 + k] = *(float4*)&m[0];
-                        *(float4*)&MS[rr * LDP + c0 + k + 4] = *(float4*)&m[4];
-                    }
+        for (int k = 0; k < CPT / 4; k++) x.m[k] = *(const float4*)&mu_k[base + 4 * k];
+        if (MODE) {
+#pragma unroll
+            for (int k = 0; k < CPT / 4; k++) x.rv[k] = *(const float4*)&R[base + 4 * k];
+        }
+    };
+    auto put = [&](const Rows& x) {
+        if (x.ok) {
+#pragma unroll
+            for (int k = 0; k < CPT; k += 8) {
+                const uint32_t qw[4] = {x.qv[k / 8].x, x.qv[k / 8].y, x.qv[k / 8].z, x.qv[k / 8].w};
+                float m[8], rv[8];
+                *(float4*)&m[0] = x.m[k / 4];
+                *(float4*)&m[4] = x.m[k / 4 + 1];
+                if (MODE) {
+                    *(float4*)&rv[0] = x.rv[k / 4];
+                    *(float4*)&rv[4] = x.rv[k / 4 + 1];
                 }
-            } else {
 #pragma unroll
-                for (int k = 0; k < CPT; k++) {
-                    XT[(c0 + k) * LDT + rr] = 0.f;
-                    if (MODE) YT[(c0 + k) * LDT + rr] = 0.f;
+                for (int e = 0; e < 8; e++) {
+                    const float qf = (e & 1) ? bf16_hi(qw[e >> 1]) : bf16_lo(qw[e >> 1]);
+                    XT[(c0 + k + e) * LDT + rr] = qf - m[e];
+                    if (MODE) YT[(c0 + k + e) * LDT + rr] = rv[e] - x.eb * m[e];
+                }
+                if (kMu) {
+                    *(float4*)&MS[rr * LDP + c0 + k] = *(float4*)&m[0];
+                    *(float4*)&MS[rr * LDP + c0 + k + 4] = *(float4*)&m[4];
                 }
             }
+        } else {
+#pragma unroll
+            for (int k = 0; k < CPT; k++) {
+                XT[(c0 + k) * LDT + rr] = 0.f;
+                if (MODE) YT[(c0 + k) * LDT + rr] = 0.f;
+            }
+        }
+    };
+    Rows nxt;
+    if (kPrefetch) fetch(r_begin, nxt);
+    for (int r0 = r_begin; r0 < r_end; r0 += RB) {
+        __syncthreads();
+        if (kPrefetch) {
+            put(nxt);
+            if (r0 + RB < r_end) fetch(r0 + RB, nxt);
+        } else {
+            Rows cur;
+            fetch(r0, cur);
+            put(cur);
         }
         __syncthreads();
         // u = P delta for the thread's 4 rows x NC columns
