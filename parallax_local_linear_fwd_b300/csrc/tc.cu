@@ -1685,22 +1685,25 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&st_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T
-            const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
-            const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK
-            const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ
-            const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
-            bool ok = mbar_wait(kv_full, 0, wd, 2);
-            for (int j = 0; ok && j <= nsub; j++) {
-                if (j < nsub) {
-                    const int s = j % NS, b = j & 1;
-                    if (!mbar_wait(&st_full[s], (j / NS) & 1, wd, 3)) break;
-                    // buffer b's weight operands were read by the accumulation of j - 2,
-                    // issued earlier by this thread: MMAs execute in issue order
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(sSt + s * C::STAGE);
-                    const uint32_t tb = tmem + 128 * b;
+        // The whole warp runs the loop, so the descriptors stay warp-uniform;
+        // the elected lane (lane 0 of the converged warp) issues every tcgen05
+        // instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T
+        const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
+        const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK
+        const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ
+        const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, wd, 2));
+        for (int j = 0; ok && j <= nsub; j++) {
+            if (j < nsub) {
+                const int s = j % NS, b = j & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&st_full[s], (j / NS) & 1, wd, 3))) break;
+                // buffer b's weight operands were read by the accumulation of j - 2,
+                // issued earlier by this thread: MMAs execute in issue order
+                tc_fence_after();
+                const uint32_t st = smem_u32(sSt + s * C::STAGE);
+                const uint32_t tb = tmem + 128 * b;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) {
                         mma_ss(tb, desc_kmajor(kaddr, C::BK, kk), desc_kmajor(st, 3 * C::BQ, kk), idS3, kk > 0);
@@ -1709,12 +1712,15 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                     }
                     mma_commit(&sc_full[b]);
                 }
-                if (j >= 1) {
-                    const int jp = j - 1, bp = jp & 1, sp = jp % NS;
-                    if (!mbar_wait(&op_full[bp], (jp >> 1) & 1, wd, 5)) break;
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(sSt + sp * C::STAGE);
-                    const uint32_t tb = tmem + 128 * bp;
+                __syncwarp();
+            }
+            if (j >= 1) {
+                const int jp = j - 1, bp = jp & 1, sp = jp % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&op_full[bp], (jp >> 1) & 1, wd, 5))) break;
+                tc_fence_after();
+                const uint32_t st = smem_u32(sSt + sp * C::STAGE);
+                const uint32_t tb = tmem + 128 * bp;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < C::BQ / 16; kk++) {
                         const uint32_t first = (jp == 0 && kk == 0) ? 0u : 1u;
@@ -1725,22 +1731,27 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                     }
                     mma_commit(&st_empty[sp]);
                     if (jp == nsub - 1) mma_commit(fin);
-                    if ((jp & 3) == 3 || jp == nsub - 1) {
-                        const int m = jp >> 2, x = m & 1;
-                        if (m >= 1 && !mbar_wait(dq_free, (m - 1) & 1, wd, 6)) break;
-                        tc_fence_after();
-                        const uint32_t dsx = dsaddr + x * C::DSB;
+                }
+                __syncwarp();
+                if ((jp & 3) == 3 || jp == nsub - 1) {
+                    const int m = jp >> 2, x = m & 1;
+                    if (m >= 1 && !__all_sync(0xffffffffu, mbar_wait(dq_free, (m - 1) & 1, wd, 6))) break;
+                    tc_fence_after();
+                    const uint32_t dsx = dsaddr + x * C::DSB;
+                    if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < C::BK / 16; kk++)
                             mma_ss(tDQ, desc_mnmajor(dsx, C::BK, kk), desc_mnmajor(kaddr, C::BK, kk), idQ, kk > 0);
                         mma_commit(dq_full);
                         mma_commit(&ds_free[x]);
                     }
+                    __syncwarp();
                 }
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0);
         }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
     } else {
         const int wg = (warp - 2) >> 2;  // owns score buffer wg and the sub-chunks j = wg (mod 2)
         const int qd = warp & 3;
