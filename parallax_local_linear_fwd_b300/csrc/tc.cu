@@ -209,36 +209,45 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idS = idesc_mma(128, C::BN, false, false);
-            const uint32_t idM = idesc_mma(128, D, false, true);
-            const uint32_t qaddr = smem_u32(sQ);
-            if (mbar_wait(q_full, 0, wd, 2)) {
-                for (int j = 0; j < nkt; j++) {
-                    const int s = j % NS;
-                    if (!mbar_wait(&k_full[s], (j / NS) & 1, wd, 3)) break;
-                    // S aliases the previous tile's P~; tcgen05.mma ops issued by one
-                    // thread execute in issue order, so no wait for that MMA here.
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sK + s * C::KB);
+        // The whole warp runs the issue loop, so the descriptors stay
+        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
+        // every tcgen05 instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        const uint32_t idM = idesc_mma(128, D, false, true);
+        const uint32_t qaddr = smem_u32(sQ);
+        if (__all_sync(0xffffffffu, mbar_wait(q_full, 0, wd, 2))) {
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (j / NS) & 1, wd, 3))) break;
+                // S aliases the previous tile's P~; tcgen05.mma ops issued by one
+                // thread execute in issue order, so no wait for that MMA here.
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sK + s * C::KB);
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tS, desc_kmajor(qaddr, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
                     mma_commit(s_full);
-                    if (!mbar_wait(p_full, j & 1, wd, 5)) break;
-                    tc_fence_after();
+                }
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(p_full, j & 1, wd, 5))) break;
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < C::BN / 16; kk++)
                         mma_ts(tMu, tS + kk * 8, desc_mnmajor(kaddr, C::BN, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(o_done);
                     mma_commit(&k_empty[s]);
                 }
-                // projection U = delta P_h^T (delta = delta_hi + delta_lo, P_h in f16):
-                // M = 128 rows, N = D, K = D, into the S columns
-                if (mbar_wait(proj_ready, 0, wd, 9)) {
-                    tc_fence_after();
-                    const uint32_t idP = idesc_mma(128, D, false, false);
-                    const uint32_t dhi = smem_u32(sK), dlo = smem_u32(sK + C::KB), pb = smem_u32(sQ);
+                __syncwarp();
+            }
+            // projection U = delta P_h^T (delta = delta_hi + delta_lo, P_h in f16):
+            // M = 128 rows, N = D, K = D, into the S columns
+            if (__all_sync(0xffffffffu, mbar_wait(proj_ready, 0, wd, 9))) {
+                tc_fence_after();
+                const uint32_t idP = idesc_mma(128, D, false, false);
+                const uint32_t dhi = smem_u32(sK), dlo = smem_u32(sK + C::KB), pb = smem_u32(sQ);
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tS, desc_kmajor(dhi, C::BM, kk), desc_kmajor(pb, D, kk), idP, kk > 0);
@@ -247,10 +256,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         mma_ss(tS, desc_kmajor(dlo, C::BM, kk), desc_kmajor(pb, D, kk), idP, 1u);
                     mma_commit(proj_done);
                 }
+                __syncwarp();
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0);
         }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
     } else {
         // softmax / epilogue warps: thread <-> query row (TMEM lane)
         const int qd = warp & 3;
@@ -543,21 +554,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idS = idesc_mma(128, C::BN, false, false);
-            const uint32_t idA = idesc_mma(128, D, false, true);
-            const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
-            if (mbar_wait(a_full, 0, wd, 2)) {
-                for (int j = 0; j < nkt; j++) {
-                    const int s = j % NS;
-                    if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
-                    // S aliases the previous tile's weights; tcgen05.mma ops issued by
-                    // one thread execute in issue order, so no wait for that MMA here.
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
-                    const uint32_t vaddr = kaddr + C::KB;
-                    const uint32_t xb = MODE == 0 ? kaddr : vaddr;  // B of the second score product
-                    const uint32_t ab = MODE == 0 ? vaddr : kaddr;  // B of the accumulation
+        // The whole warp runs the issue loop, so the descriptors stay
+        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
+        // every tcgen05 instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        const uint32_t idA = idesc_mma(128, D, false, true);
+        const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
+        if (__all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2))) {
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3))) break;
+                // S aliases the previous tile's weights; tcgen05.mma ops issued by
+                // one thread execute in issue order, so no wait for that MMA here.
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
+                const uint32_t vaddr = kaddr + C::KB;
+                const uint32_t xb = MODE == 0 ? kaddr : vaddr;  // B of the second score product
+                const uint32_t ab = MODE == 0 ? vaddr : kaddr;  // B of the accumulation
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
@@ -565,18 +579,23 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
                     mma_commit(s_full);
-                    if (!mbar_wait(w_full, j & 1, wd, 5)) break;
-                    tc_fence_after();
+                }
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < C::BN / 16; kk++)
                         mma_ts(tAcc, tS + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
                     if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
                     mma_commit(&kv_empty[s]);
                 }
+                __syncwarp();
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0);
         }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
     } else {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
@@ -774,18 +793,21 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idS = idesc_mma(128, C::BN, false, false);
-            const uint32_t idO = idesc_mma(128, D, false, true);
-            const uint32_t qa = smem_u32(sQ), ra = smem_u32(sR);
-            if (mbar_wait(a_full, 0, wd, 2)) {
-                for (int j = 0; j < nkt; j++) {
-                    const int s = j % NS;
-                    if (!mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3)) break;
-                    // S and R alias the previous tile's weights; tcgen05.mma ops issued by
-                    // one thread execute in issue order, so no wait for those MMAs here.
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB), vaddr = kaddr + C::KB;
+        // The whole warp runs the issue loop, so the descriptors stay
+        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
+        // every tcgen05 instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        const uint32_t idO = idesc_mma(128, D, false, true);
+        const uint32_t qa = smem_u32(sQ), ra = smem_u32(sR);
+        if (__all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2))) {
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3))) break;
+                // S and R alias the previous tile's weights; tcgen05.mma ops issued by
+                // one thread execute in issue order, so no wait for those MMAs here.
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB), vaddr = kaddr + C::KB;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) {
                         const uint64_t kd = desc_kmajor(kaddr, C::BN, kk);
@@ -793,8 +815,11 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
                         mma_ss(tR, desc_kmajor(ra, C::BM, kk), kd, idS, kk > 0);
                     }
                     mma_commit(s_full);
-                    if (!mbar_wait(p_full, j & 1, wd, 5)) break;
-                    tc_fence_after();
+                }
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(p_full, j & 1, wd, 5))) break;
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < C::BN / 16; kk++) {
                         const uint64_t vd = desc_mnmajor(vaddr, C::BN, kk);
@@ -805,10 +830,12 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
                     mma_commit(o_done);
                     mma_commit(&kv_empty[s]);
                 }
+                __syncwarp();
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0);
         }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
     } else {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
@@ -1410,30 +1437,36 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&st_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T: N = 192 queries x3
-            const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
-            const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK: A in TMEM, B MN-major
-            const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ: A = ds MN-major, B = K MN-major
-            const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
-            if (mbar_wait(kv_full, 0, wd, 2)) {
-                for (int j = 0; j < nsub; j++) {
-                    const int s = j % NS;
-                    if (!mbar_wait(&st_full[s], (j / NS) & 1, wd, 3)) break;
-                    // the scores overwrite the previous sub-chunk's weight operands;
-                    // tcgen05.mma ops issued by one thread execute in issue order
-                    if (j > 0 && (j & 1) == 0 && !mbar_wait(dq_free, ((j >> 1) - 1) & 1, wd, 5)) break;
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(sSt + s * C::STAGE);
-                    const uint32_t ado = st + C::DO_OFF;
+        // The whole warp runs the issue loop, so the descriptors stay
+        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
+        // every tcgen05 instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T: N = 192 queries x3
+        const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
+        const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK: A in TMEM, B MN-major
+        const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ: A = ds MN-major, B = K MN-major
+        const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
+        if (__all_sync(0xffffffffu, mbar_wait(kv_full, 0, wd, 2))) {
+            for (int j = 0; j < nsub; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&st_full[s], (j / NS) & 1, wd, 3))) break;
+                // the scores overwrite the previous sub-chunk's weight operands;
+                // tcgen05.mma ops issued by one thread execute in issue order
+                if (j > 0 && (j & 1) == 0 && !__all_sync(0xffffffffu, mbar_wait(dq_free, ((j >> 1) - 1) & 1, wd, 5))) break;
+                tc_fence_after();
+                const uint32_t st = smem_u32(sSt + s * C::STAGE);
+                const uint32_t ado = st + C::DO_OFF;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) {
                         mma_ss(tS, desc_kmajor(kaddr, C::BK, kk), desc_kmajor(st, 3 * C::BQ, kk), idS3, kk > 0);
                         mma_ss(tE, desc_kmajor(vaddr, C::BK, kk), desc_kmajor(ado, C::BQ, kk), idS, kk > 0);
                     }
                     mma_commit(sc_full);
-                    if (!mbar_wait(op_full, j & 1, wd, 6)) break;
-                    tc_fence_after();
+                }
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(op_full, j & 1, wd, 6))) break;
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < C::BQ / 16; kk++) {
                         const uint32_t first = (j == 0 && kk == 0) ? 0u : 1u;
@@ -1451,10 +1484,12 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                         mma_commit(dq_full);
                     }
                 }
+                __syncwarp();
             }
-            mma_commit(drain);
-            mbar_wait_drain(drain, 0);
         }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
     } else {
         const int wg = (warp - 2) >> 2;  // warpgroup: query columns [32 wg, 32 wg + 32)
         const int qd = warp & 3;
