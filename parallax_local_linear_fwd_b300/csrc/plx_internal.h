@@ -16,6 +16,7 @@ enum KernelId : unsigned {
     KID_TC_BWD_B3 = 4,
     KID_TC_PROJ = 5,
     KID_TC_PROBE = 6,
+    KID_TC_BWD_B2 = 7,
 };
 
 struct FwdArgs {

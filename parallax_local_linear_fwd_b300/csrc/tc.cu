@@ -1246,6 +1246,236 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
     }
 }
 
+// ============================================================ B2 on the tensor cores (d = 64)
+// The row math of B2 (same outputs as tc_rows<64, 1>) with its three
+// products on the tensor cores, per tile of 128 rows of head h (thread =
+// row = TMEM lane):
+//   U = delta P_h^T and ddelta = du P_h, with delta and du split into f16
+//   hi + lo halves against P_h in f16 (the forward's projection: delta is
+//   formed from the same f16 copy of q, so U and gbar equal the forward's);
+//   dP_h partial += du^T delta over the CTA's 512 rows as one M = 128
+//   product whose A stacks [du | delta] along M (rows 0..63 of the result
+//   are du^T delta), in three passes hi.hi + lo.hi + hi.lo.
+struct B2T {
+    static constexpr int D = 64, BM = 128, NT = 128, TILES = 4;  // 512 rows per CTA
+    static constexpr int TB = BM * D * 2;                         // one f16 [128][64] tile
+    static constexpr int PB = D * D * 2;                          // P_h in f16
+    // tiles in this order: [du_hi | delta_hi] and [du_lo | delta_lo] sit TB
+    // apart, as the two 64-row M blocks of the dP product's A operand
+    static constexpr int SMEM = 1024 + 4 * TB + PB + 64;
+    static constexpr unsigned TMEM_COLS = 256;  // U [0,64), ddelta [64,128), dP [128,192)
+};
+static_assert(B2T::BM * B2T::TILES == RowCfg<64>::ROWS_PER_CTA, "dP partial layout shared with tc_rows");
+
+__global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16, const float* __restrict__ mu_k,
+                                                 const float* __restrict__ P, const float* __restrict__ lse,
+                                                 const float* __restrict__ R, const float* __restrict__ ebar,
+                                                 __half* __restrict__ U, __half* __restrict__ dmu,
+                                                 float* __restrict__ dq_acc, float* __restrict__ rowpack,
+                                                 float* __restrict__ dp_partial, int B, int H, int T,
+                                                 unsigned* status) {
+    using C = B2T;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sUH = sm;
+    uint8_t* sDH = sUH + C::TB;
+    uint8_t* sUL = sDH + C::TB;
+    uint8_t* sDL = sUL + C::TB;
+    uint8_t* sP = sDL + C::TB;
+    uint64_t* bars = (uint64_t*)(sP + C::PB);  // [0] the tile's MMAs are done, [1] teardown drain
+    uint32_t* holder = (uint32_t*)(bars + 2);
+    volatile int* abortf = (volatile int*)(holder + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int h = blockIdx.y;
+    const int nrows = B * T;
+    const int r_begin = blockIdx.x * C::BM * C::TILES, r_end = min(r_begin + C::BM * C::TILES, nrows);
+    const Watchdog wd{status, abortf, KID_TC_BWD_B2};
+    if (tid == 0) {
+        *abortf = 0;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    // P_h in f16 as a K-major [a][b] tile: the B operand of U (N = a, K = b)
+    // and, read MN-major, of ddelta (N = b, K = a)
+    const float* Ph = P + (size_t)h * D * D;
+    for (int id = tid; id < D * D / 8; id += C::NT) {
+        const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
+        const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
+        const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
+        *(uint4*)(sP + sw_off(pa, pb0, D)) =
+            make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w), pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
+    }
+    if (warp == 0) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder, tU = tmem, tDD = tmem + 64, tDP = tmem + 128;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const uint32_t idN = idesc_mma(128, D, false, false);  // U: A and B K-major
+    const uint32_t idNb = idesc_mma(128, D, false, true);  // ddelta: B = P_h read MN-major
+    const uint32_t idPd = idesc_mma(128, D, true, true);   // dP: A = [du | delta], B = delta, both MN-major
+    bool ok = true;
+    int tile = 0;
+    for (int r0 = r_begin; r0 < r_end; r0 += C::BM, tile++) {
+        const int r = r0 + tid;
+        const bool valid = r < r_end;
+        const size_t row = valid ? ((size_t)(r / T) * H + h) * T + r % T : 0;
+        const float eb = valid ? ebar[row] : 0.f;
+        // delta = q - mu_k and du = R - ebar mu_k as f16 hi + lo, K-major rows
+#pragma unroll 2
+        for (int c = 0; c < D / 8; c++) {
+            uint32_t dh[4] = {0, 0, 0, 0}, dl[4] = {0, 0, 0, 0}, uh[4] = {0, 0, 0, 0}, ul[4] = {0, 0, 0, 0};
+            if (valid) {
+                const uint4 qv = *(const uint4*)(q16 + row * D + 8 * c);
+                const float4 m0 = *(const float4*)(mu_k + row * D + 8 * c);
+                const float4 m1 = *(const float4*)(mu_k + row * D + 8 * c + 4);
+                const float4 x0 = *(const float4*)(R + row * D + 8 * c);
+                const float4 x1 = *(const float4*)(R + row * D + 8 * c + 4);
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                const float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                const float rv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int x = 0; x < 4; x++) {
+                    const float d0 = f16_lo(qw[x]) - m[2 * x];
+                    const float d1 = f16_hi(qw[x]) - m[2 * x + 1];
+                    dh[x] = pack_f16(d0, d1);
+                    dl[x] = pack_f16(d0 - f16_lo(dh[x]), d1 - f16_hi(dh[x]));
+                    const float u0 = rv[2 * x] - eb * m[2 * x];
+                    const float u1 = rv[2 * x + 1] - eb * m[2 * x + 1];
+                    uh[x] = pack_f16(u0, u1);
+                    ul[x] = pack_f16(u0 - f16_lo(uh[x]), u1 - f16_hi(uh[x]));
+                }
+            }
+            const uint32_t off = sw_off(tid, 8 * c, C::BM);
+            *(uint4*)(sDH + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
+            *(uint4*)(sDL + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+            *(uint4*)(sUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+            *(uint4*)(sUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();  // the previous tile's TMEM reads come before these MMAs
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t dh = smem_u32(sDH), dl = smem_u32(sDL), uh = smem_u32(sUH), ul = smem_u32(sUL);
+                const uint32_t pb = smem_u32(sP);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tU, desc_kmajor(dh, C::BM, kk), desc_kmajor(pb, D, kk), idN, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tU, desc_kmajor(dl, C::BM, kk), desc_kmajor(pb, D, kk), idN, 1u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tDD, desc_kmajor(uh, C::BM, kk), desc_mnmajor(pb, D, kk), idNb, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tDD, desc_kmajor(ul, C::BM, kk), desc_mnmajor(pb, D, kk), idNb, 1u);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; kk++)
+                    mma_ss(tDP, desc_mn_lbo(uh, kk, C::TB), desc_mnmajor(dh, C::BM, kk), idPd,
+                           (tile > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; kk++)
+                    mma_ss(tDP, desc_mn_lbo(ul, kk, C::TB), desc_mnmajor(dh, C::BM, kk), idPd, 1u);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; kk++)
+                    mma_ss(tDP, desc_mn_lbo(uh, kk, C::TB), desc_mnmajor(dl, C::BM, kk), idPd, 1u);
+                mma_commit(&bars[0]);
+            }
+            __syncwarp();
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[0], tile & 1, wd, 1)) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        // tcgen05.ld is warp-collective: every lane loads, only valid rows compute and store
+        float gr = 0.f, gb = 0.f, ru = 0.f, xx = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; c++) {
+            uint32_t vu[32], vd[32];
+            tmem_ld32(tU + lrow + 32 * c, vu);
+            tmem_ld32(tDD + lrow + 32 * c, vd);
+            tmem_wait_ld();
+            if (!valid) continue;
+            const float* mrow = mu_k + row * D + 32 * c;
+            const float* rrow = R + row * D + 32 * c;
+            uint32_t uhp[16], mh[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float4 m = *(const float4*)(mrow + 2 * i);
+                const float4 x = *(const float4*)(rrow + 2 * i);
+                const float u[4] = {__uint_as_float(vu[2 * i]), __uint_as_float(vu[2 * i + 1]),
+                                    __uint_as_float(vu[2 * i + 2]), __uint_as_float(vu[2 * i + 3])};
+                const float dd[4] = {__uint_as_float(vd[2 * i]), __uint_as_float(vd[2 * i + 1]),
+                                     __uint_as_float(vd[2 * i + 2]), __uint_as_float(vd[2 * i + 3])};
+                const float mm[4] = {m.x, m.y, m.z, m.w}, xr[4] = {x.x, x.y, x.z, x.w};
+                uhp[i] = pack_f16(u[0], u[1]);
+                uhp[i + 1] = pack_f16(u[2], u[3]);
+                gr = fmaf(mm[0], f16_lo(uhp[i]), gr);
+                gr = fmaf(mm[1], f16_hi(uhp[i]), gr);
+                gr = fmaf(mm[2], f16_lo(uhp[i + 1]), gr);
+                gr = fmaf(mm[3], f16_hi(uhp[i + 1]), gr);
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    gb = fmaf(mm[e], u[e], gb);
+                    ru = fmaf(xr[e], u[e], ru);
+                    xx = fmaf(mm[e], -dd[e], xx);
+                }
+                mh[i] = pack_f16(-dd[0], -dd[1]);
+                mh[i + 1] = pack_f16(-dd[2], -dd[3]);
+                *(float4*)(dq_acc + row * D + 32 * c + 2 * i) = make_float4(dd[0], dd[1], dd[2], dd[3]);
+            }
+            uint4* ud = (uint4*)(U + row * D + 32 * c);
+            uint4* md = (uint4*)(dmu + row * D + 32 * c);
+#pragma unroll
+            for (int y = 0; y < 4; y++) {
+                ud[y] = make_uint4(uhp[4 * y], uhp[4 * y + 1], uhp[4 * y + 2], uhp[4 * y + 3]);
+                md[y] = make_uint4(mh[4 * y], mh[4 * y + 1], mh[4 * y + 2], mh[4 * y + 3]);
+            }
+        }
+        if (valid) {
+            // paired row scalars {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o}
+            const float doo = eb + ru - gb * eb;
+            const int tt = r % T, half = tt & 1;
+            float* pr = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + half;
+            pr[0] = -lse[row] * LOG2E;
+            pr[2] = 1.f - gr;
+            pr[4] = -eb;
+            pr[6] = -(doo - gb * eb + xx);
+        }
+    }
+    // this CTA's dP_h partial: rows a = TMEM lanes 0..63 (warps 0 and 1)
+    if (ok && warp < 2) {
+        tc_fence_after();
+        float* dst = dp_partial + ((size_t)h * gridDim.x + blockIdx.x) * D * D + (size_t)tid * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; c++) {
+            uint32_t v[32];
+            tmem_ld32(tDP + lrow + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *(float4*)(dst + 32 * c + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
+    }
+    // teardown: every MMA issued must complete before the CTA releases TMEM
+    if (warp == 0) {
+        if (elect_one()) mma_commit(&bars[1]);
+        __syncwarp();
+        mbar_wait_drain(&bars[1], 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 // dP[h] = sum of the CTA partials in chunk order (fixed order: reproducible).
 __global__ void __launch_bounds__(256) tc_dp_reduce(const float4* __restrict__ partial, float4* __restrict__ dP,
                                                     int nchunks, int dd4) {
@@ -1298,10 +1528,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
-// MN-major operand descriptor with an explicit leading (N-block) byte offset.
-__device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t lbo) {
-    return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
-}
 
 // The elementwise step for 16 queries (one 16-column chunk) of one key row,
 // two queries per f32x2 instruction.  rp points at the chunk's first query
@@ -2119,13 +2345,21 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     }
     {  // B2: row math and the dP_h partials
         using R = RowCfg<D>;
-        const size_t sm = R::smem(1);
         const int nchunks = (a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA;
-        PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-        timing_begin(a.stream, "tc_bwd_b2");
-        tc_rows<D, 1><<<dim3(nchunks, a.H), R::NT, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P, a.lse,
-                                                                   w.R, w.ebar, w.U, nullptr, w.dmu, w.dq_acc,
-                                                                   w.rows, w.partial, a.B, a.H, a.T);
+        if (D == 64) {
+            PLX_TRY(cudaFuncSetAttribute(tc_b2, cudaFuncAttributeMaxDynamicSharedMemorySize, B2T::SMEM));
+            timing_begin(a.stream, "tc_bwd_b2");
+            tc_b2<<<dim3(nchunks, a.H), B2T::NT, B2T::SMEM, a.stream>>>(w.q16, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U,
+                                                                       w.dmu, w.dq_acc, w.rows, w.partial, a.B,
+                                                                       a.H, a.T, a.status);
+        } else {
+            const size_t sm = R::smem(1);
+            PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+            timing_begin(a.stream, "tc_bwd_b2");
+            tc_rows<D, 1><<<dim3(nchunks, a.H), R::NT, sm, a.stream>>>((const __nv_bfloat16*)a.q, a.mu_k, a.P,
+                                                                       a.lse, w.R, w.ebar, w.U, nullptr, w.dmu,
+                                                                       w.dq_acc, w.rows, w.partial, a.B, a.H, a.T);
+        }
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
         const int dd4 = D * D / 4;

@@ -279,6 +279,12 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int rows, int kk
     return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), (uint32_t)(rows * 128), 1024);
 }
 
+// MN-major operand descriptor with an explicit leading byte offset: the
+// distance between the 64-element blocks of the M (or N) dimension.
+__device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t lbo) {
+    return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
+}
+
 // ------------------------------------------------------------ packing
 // Two floats -> one 32-bit word of two 16-bit values, round to nearest even;
 // `lo` lands in the low half (the even element of an MMA operand pair).
