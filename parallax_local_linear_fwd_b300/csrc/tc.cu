@@ -1248,26 +1248,29 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
 
 // ============================================================ B2 on the tensor cores (d = 64)
 // The row math of B2 (same outputs as tc_rows<64, 1>) with its three
-// products on the tensor cores, per tile of 128 rows of head h (thread =
-// row = TMEM lane):
+// products on the tensor cores, per tile of 128 rows of head h:
 //   U = delta P_h^T and ddelta = du P_h, with delta and du split into f16
 //   hi + lo halves against P_h in f16 (the forward's projection: delta is
-//   formed from the same f16 copy of q, so U and gbar equal the forward's);
+//   formed from the same f16 copy of q, so U equals the forward's);
 //   dP_h partial += du^T delta over the CTA's 512 rows as one M = 128
 //   product whose A stacks [du | delta] along M (rows 0..63 of the result
 //   are du^T delta), in three passes hi.hi + lo.hi + hi.lo.
+// Two threads per row: warps w and w + 4 cover rows 32 (w % 4) .. + 31 (their
+// TMEM lane quadrant) and the column halves [0, 32) and [32, 64), so twice as
+// many row loads are in flight; the halves' row sums meet in shared memory.
 struct B2T {
-    static constexpr int D = 64, BM = 128, NT = 128, TILES = 4;  // 512 rows per CTA
+    static constexpr int D = 64, BM = 128, NT = 256, TILES = 4;  // 512 rows per CTA
     static constexpr int TB = BM * D * 2;                         // one f16 [128][64] tile
     static constexpr int PB = D * D * 2;                          // P_h in f16
+    static constexpr int RED = BM * 4 * 4;                        // the upper half's 4 row sums
     // tiles in this order: [du_hi | delta_hi] and [du_lo | delta_lo] sit TB
     // apart, as the two 64-row M blocks of the dP product's A operand
-    static constexpr int SMEM = 1024 + 4 * TB + PB + 64;
+    static constexpr int SMEM = 1024 + 4 * TB + PB + RED + 64;
     static constexpr unsigned TMEM_COLS = 256;  // U [0,64), ddelta [64,128), dP [128,192)
 };
 static_assert(B2T::BM * B2T::TILES == RowCfg<64>::ROWS_PER_CTA, "dP partial layout shared with tc_rows");
 
-__global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16, const float* __restrict__ mu_k,
+__global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q16, const float* __restrict__ mu_k,
                                                  const float* __restrict__ P, const float* __restrict__ lse,
                                                  const float* __restrict__ R, const float* __restrict__ ebar,
                                                  __half* __restrict__ U, __half* __restrict__ dmu,
@@ -1283,10 +1286,13 @@ __global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16,
     uint8_t* sUL = sDH + C::TB;
     uint8_t* sDL = sUL + C::TB;
     uint8_t* sP = sDL + C::TB;
-    uint64_t* bars = (uint64_t*)(sP + C::PB);  // [0] the tile's MMAs are done, [1] teardown drain
+    float4* sRed = (float4*)(sP + C::PB);       // [128] the upper column half's row sums
+    uint64_t* bars = (uint64_t*)(sP + C::PB + C::RED);  // [0] the tile's MMAs are done, [1] teardown drain
     uint32_t* holder = (uint32_t*)(bars + 2);
     volatile int* abortf = (volatile int*)(holder + 1);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+    const int rit = quad * 32 + lane;             // row in the tile = TMEM lane
     const int h = blockIdx.y;
     const int nrows = B * T;
     const int r_begin = blockIdx.x * C::BM * C::TILES, r_end = min(r_begin + C::BM * C::TILES, nrows);
@@ -1312,20 +1318,21 @@ __global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder, tU = tmem, tDD = tmem + 64, tDP = tmem + 128;
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const uint32_t lrow = (uint32_t)(quad * 32) << 16;
+    const int c0 = 32 * half;  // this thread's columns [c0, c0 + 32)
     const uint32_t idN = idesc_mma(128, D, false, false);  // U: A and B K-major
     const uint32_t idNb = idesc_mma(128, D, false, true);  // ddelta: B = P_h read MN-major
     const uint32_t idPd = idesc_mma(128, D, true, true);   // dP: A = [du | delta], B = delta, both MN-major
     bool ok = true;
     int tile = 0;
     for (int r0 = r_begin; r0 < r_end; r0 += C::BM, tile++) {
-        const int r = r0 + tid;
+        const int r = r0 + rit;
         const bool valid = r < r_end;
         const size_t row = valid ? ((size_t)(r / T) * H + h) * T + r % T : 0;
         const float eb = valid ? ebar[row] : 0.f;
         // delta = q - mu_k and du = R - ebar mu_k as f16 hi + lo, K-major rows
 #pragma unroll 2
-        for (int c = 0; c < D / 8; c++) {
+        for (int c = c0 / 8; c < c0 / 8 + 4; c++) {
             uint32_t dh[4] = {0, 0, 0, 0}, dl[4] = {0, 0, 0, 0}, uh[4] = {0, 0, 0, 0}, ul[4] = {0, 0, 0, 0};
             if (valid) {
                 const uint4 qv = *(const uint4*)(q16 + row * D + 8 * c);
@@ -1348,7 +1355,7 @@ __global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16,
                     ul[x] = pack_f16(u0 - f16_lo(uh[x]), u1 - f16_hi(uh[x]));
                 }
             }
-            const uint32_t off = sw_off(tid, 8 * c, C::BM);
+            const uint32_t off = sw_off(rit, 8 * c, C::BM);
             *(uint4*)(sDH + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
             *(uint4*)(sDL + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
             *(uint4*)(sUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
@@ -1393,74 +1400,79 @@ __global__ void __launch_bounds__(B2T::NT) tc_b2(const __half* __restrict__ q16,
         tc_fence_after();
         // tcgen05.ld is warp-collective: every lane loads, only valid rows compute and store
         float gr = 0.f, gb = 0.f, ru = 0.f, xx = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; c++) {
+        {
             uint32_t vu[32], vd[32];
-            tmem_ld32(tU + lrow + 32 * c, vu);
-            tmem_ld32(tDD + lrow + 32 * c, vd);
+            tmem_ld32(tU + lrow + c0, vu);
+            tmem_ld32(tDD + lrow + c0, vd);
             tmem_wait_ld();
-            if (!valid) continue;
-            const float* mrow = mu_k + row * D + 32 * c;
-            const float* rrow = R + row * D + 32 * c;
-            uint32_t uhp[16], mh[16];
+            if (valid) {
+                const float* mrow = mu_k + row * D + c0;
+                const float* rrow = R + row * D + c0;
+                uint32_t uhp[16], mh[16];
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float4 m = *(const float4*)(mrow + 2 * i);
-                const float4 x = *(const float4*)(rrow + 2 * i);
-                const float u[4] = {__uint_as_float(vu[2 * i]), __uint_as_float(vu[2 * i + 1]),
-                                    __uint_as_float(vu[2 * i + 2]), __uint_as_float(vu[2 * i + 3])};
-                const float dd[4] = {__uint_as_float(vd[2 * i]), __uint_as_float(vd[2 * i + 1]),
-                                     __uint_as_float(vd[2 * i + 2]), __uint_as_float(vd[2 * i + 3])};
-                const float mm[4] = {m.x, m.y, m.z, m.w}, xr[4] = {x.x, x.y, x.z, x.w};
-                uhp[i] = pack_f16(u[0], u[1]);
-                uhp[i + 1] = pack_f16(u[2], u[3]);
-                gr = fmaf(mm[0], f16_lo(uhp[i]), gr);
-                gr = fmaf(mm[1], f16_hi(uhp[i]), gr);
-                gr = fmaf(mm[2], f16_lo(uhp[i + 1]), gr);
-                gr = fmaf(mm[3], f16_hi(uhp[i + 1]), gr);
+                for (int i = 0; i < 16; i += 2) {
+                    const float4 m = *(const float4*)(mrow + 2 * i);
+                    const float4 x = *(const float4*)(rrow + 2 * i);
+                    const float u[4] = {__uint_as_float(vu[2 * i]), __uint_as_float(vu[2 * i + 1]),
+                                        __uint_as_float(vu[2 * i + 2]), __uint_as_float(vu[2 * i + 3])};
+                    const float dd[4] = {__uint_as_float(vd[2 * i]), __uint_as_float(vd[2 * i + 1]),
+                                         __uint_as_float(vd[2 * i + 2]), __uint_as_float(vd[2 * i + 3])};
+                    const float mm[4] = {m.x, m.y, m.z, m.w}, xr[4] = {x.x, x.y, x.z, x.w};
+                    uhp[i] = pack_f16(u[0], u[1]);
+                    uhp[i + 1] = pack_f16(u[2], u[3]);
+                    gr = fmaf(mm[0], f16_lo(uhp[i]), gr);
+                    gr = fmaf(mm[1], f16_hi(uhp[i]), gr);
+                    gr = fmaf(mm[2], f16_lo(uhp[i + 1]), gr);
+                    gr = fmaf(mm[3], f16_hi(uhp[i + 1]), gr);
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    gb = fmaf(mm[e], u[e], gb);
-                    ru = fmaf(xr[e], u[e], ru);
-                    xx = fmaf(mm[e], -dd[e], xx);
+                    for (int e = 0; e < 4; e++) {
+                        gb = fmaf(mm[e], u[e], gb);
+                        ru = fmaf(xr[e], u[e], ru);
+                        xx = fmaf(mm[e], -dd[e], xx);
+                    }
+                    mh[i] = pack_f16(-dd[0], -dd[1]);
+                    mh[i + 1] = pack_f16(-dd[2], -dd[3]);
+                    *(float4*)(dq_acc + row * D + c0 + 2 * i) = make_float4(dd[0], dd[1], dd[2], dd[3]);
                 }
-                mh[i] = pack_f16(-dd[0], -dd[1]);
-                mh[i + 1] = pack_f16(-dd[2], -dd[3]);
-                *(float4*)(dq_acc + row * D + 32 * c + 2 * i) = make_float4(dd[0], dd[1], dd[2], dd[3]);
-            }
-            uint4* ud = (uint4*)(U + row * D + 32 * c);
-            uint4* md = (uint4*)(dmu + row * D + 32 * c);
+                uint4* ud = (uint4*)(U + row * D + c0);
+                uint4* md = (uint4*)(dmu + row * D + c0);
 #pragma unroll
-            for (int y = 0; y < 4; y++) {
-                ud[y] = make_uint4(uhp[4 * y], uhp[4 * y + 1], uhp[4 * y + 2], uhp[4 * y + 3]);
-                md[y] = make_uint4(mh[4 * y], mh[4 * y + 1], mh[4 * y + 2], mh[4 * y + 3]);
+                for (int y = 0; y < 4; y++) {
+                    ud[y] = make_uint4(uhp[4 * y], uhp[4 * y + 1], uhp[4 * y + 2], uhp[4 * y + 3]);
+                    md[y] = make_uint4(mh[4 * y], mh[4 * y + 1], mh[4 * y + 2], mh[4 * y + 3]);
+                }
             }
         }
-        if (valid) {
+        if (half == 1) sRed[rit] = make_float4(gr, gb, ru, xx);
+        __syncthreads();
+        if (half == 0 && valid) {
+            const float4 o = sRed[rit];
+            gr += o.x;
+            gb += o.y;
+            ru += o.z;
+            xx += o.w;
             // paired row scalars {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o}
             const float doo = eb + ru - gb * eb;
-            const int tt = r % T, half = tt & 1;
-            float* pr = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + half;
+            const int tt = r % T, hp = tt & 1;
+            float* pr = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + hp;
             pr[0] = -lse[row] * LOG2E;
             pr[2] = 1.f - gr;
             pr[4] = -eb;
             pr[6] = -(doo - gb * eb + xx);
         }
     }
-    // this CTA's dP_h partial: rows a = TMEM lanes 0..63 (warps 0 and 1)
-    if (ok && warp < 2) {
+    // this CTA's dP_h partial: rows a = TMEM lanes 0..63 (quadrants 0 and 1),
+    // columns split between the two halves
+    if (ok && quad < 2) {
         tc_fence_after();
-        float* dst = dp_partial + ((size_t)h * gridDim.x + blockIdx.x) * D * D + (size_t)tid * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; c++) {
-            uint32_t v[32];
-            tmem_ld32(tDP + lrow + 32 * c, v);
-            tmem_wait_ld();
+        float* dst = dp_partial + ((size_t)h * gridDim.x + blockIdx.x) * D * D + (size_t)rit * D + c0;
+        uint32_t v[32];
+        tmem_ld32(tDP + lrow + c0, v);
+        tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *(float4*)(dst + 32 * c + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-        }
+        for (int i = 0; i < 32; i += 4)
+            *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
     }
     // teardown: every MMA issued must complete before the CTA releases TMEM
     if (warp == 0) {
