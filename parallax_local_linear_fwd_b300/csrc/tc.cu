@@ -1940,22 +1940,34 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             mbar_expect_tx(kv_full, 2 * C::KB);
             tma_load_3d(sK, &tm_k, 0, k0, bh, kv_full);
             tma_load_3d(sV, &tm_v, 0, k0, bh, kv_full);
+            // sub-chunks load in pairs (2p, 2p + 1) onto one barrier, st_full[p & 1],
+            // so the MMA warp waits once per pair
             int issued = 0;
-            for (int j = 0; j < nsub; j++) {
-                const int s = j % NS;
-                const int t0 = k0 + j * C::BQ;
-                if (j >= NS && !mbar_wait(&st_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
-                mbar_expect_tx(&st_full[s], C::STAGE_BYTES);
-                uint8_t* st = sSt + s * C::STAGE;
-                tma_load_3d(st, &tm_q, 0, t0, bh, &st_full[s]);
-                tma_load_3d(st + C::SUB, &tm_u, 0, t0, bh, &st_full[s]);
-                tma_load_3d(st + 2 * C::SUB, &tm_dmu, 0, t0, bh, &st_full[s]);
-                tma_load_3d(st + C::DO_OFF, &tm_do, 0, t0, bh, &st_full[s]);
-                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, &st_full[s]);
-                issued = j + 1;
+            for (int j = 0; j < nsub; j += 2) {
+                const int n2 = nsub - j < 2 ? nsub - j : 2;
+                uint64_t* bar = &st_full[(j >> 1) & 1];
+                bool free_ok = true;
+                for (int e = 0; e < n2 && free_ok; e++) {
+                    const int jj = j + e;
+                    if (jj >= NS && !mbar_wait(&st_empty[jj % NS], ((jj / NS) - 1) & 1, wd, 1)) free_ok = false;
+                }
+                if (!free_ok) break;
+                mbar_expect_tx(bar, n2 * C::STAGE_BYTES);
+                for (int e = 0; e < n2; e++) {
+                    const int jj = j + e, t0 = k0 + jj * C::BQ;
+                    uint8_t* st = sSt + (jj % NS) * C::STAGE;
+                    tma_load_3d(st, &tm_q, 0, t0, bh, bar);
+                    tma_load_3d(st + C::SUB, &tm_u, 0, t0, bh, bar);
+                    tma_load_3d(st + 2 * C::SUB, &tm_dmu, 0, t0, bh, bar);
+                    tma_load_3d(st + C::DO_OFF, &tm_do, 0, t0, bh, bar);
+                    tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, bar);
+                }
+                issued = j + n2;
             }
             mbar_wait_drain(kv_full, 0);
-            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&st_full[j % NS], (j / NS) & 1);
+            // loads can be in flight for the last two pairs only (four slots)
+            const int npairs = (issued + 1) / 2;
+            for (int pq = npairs > 2 ? npairs - 2 : 0; pq < npairs; pq++) mbar_wait_drain(&st_full[pq & 1], (pq >> 1) & 1);
         }
     } else if (warp == 1) {
         // The whole warp runs the loop, so the descriptors stay warp-uniform;
@@ -1970,7 +1982,9 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         for (int j = 0; ok && j <= nsub; j++) {
             if (j < nsub) {
                 const int s = j % NS, b = j & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&st_full[s], (j / NS) & 1, wd, 3))) break;
+                // the pair (j, j + 1) arrives on one barrier: wait at even j only
+                if ((j & 1) == 0 && !__all_sync(0xffffffffu, mbar_wait(&st_full[(j >> 1) & 1], (j >> 2) & 1, wd, 3)))
+                    break;
                 // buffer b's weight operands were read by the accumulation of j - 2,
                 // issued earlier by this thread: MMAs execute in issue order
                 tc_fence_after();
