@@ -282,13 +282,14 @@ struct Dec2 {
     static constexpr int PPR = RB / 16;     // 16-byte pieces per row
     static constexpr int CPL = D / 32;      // value columns per lane
     static constexpr int SUB = 32;          // keys per sub-chunk (one per lane)
-    static constexpr int NSTG = 3;          // cp.async stages per warp
+    static constexpr int NSTG = 3;          // cp.async stages per warp, pass 1
+    static constexpr int NSTG2 = 2;         // pass 2 (K and V): smaller stages let more warps reside
     static constexpr int DW1 = 4;           // warps per CTA, pass 1
     static constexpr int DW2 = D == 64 ? 4 : 2;
     static constexpr int ST1 = SUB * RB;      // pass-1 stage (K)
     static constexpr int ST2 = 2 * SUB * RB;  // pass-2 stage (K then V)
     static constexpr size_t SM1 = (size_t)DW1 * NSTG * ST1 + sizeof(float) * (D + DW1 * (D + 2));
-    static constexpr size_t SM2 = (size_t)DW2 * NSTG * ST2 + sizeof(float) * (4 * D + 2 + DW2 * D);
+    static constexpr size_t SM2 = (size_t)DW2 * NSTG2 * ST2 + sizeof(float) * (4 * D + 2 + DW2 * D);
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
@@ -501,7 +502,7 @@ __global__ void __launch_bounds__(Dec2<D>::DW2 * 32) dec2_pass2(const __nv_bfloa
     using C = Dec2<D>;
     constexpr int NT = C::DW2 * 32;
     extern __shared__ __align__(16) uint8_t dsm2[];
-    float* qs = (float*)(dsm2 + (size_t)C::DW2 * C::NSTG * C::ST2);
+    float* qs = (float*)(dsm2 + (size_t)C::DW2 * C::NSTG2 * C::ST2);
     float* us = qs + D;
     float* mus = us + D;
     float* dl = mus + D;
@@ -515,11 +516,11 @@ __global__ void __launch_bounds__(Dec2<D>::DW2 * 32) dec2_pass2(const __nv_bfloa
     const int nsc = ke > kb ? (ke - kb + C::SUB - 1) / C::SUB : 0;
     const __nv_bfloat16* K = kc + ((size_t)bh * Lmax + (kb < len ? kb : 0)) * D;
     const __nv_bfloat16* V = vc + ((size_t)bh * Lmax + (kb < len ? kb : 0)) * D;
-    uint8_t* stg = dsm2 + (size_t)warp * C::NSTG * C::ST2;
+    uint8_t* stg = dsm2 + (size_t)warp * C::NSTG2 * C::ST2;
     const uint32_t stg_a = smem_addr(stg);
     // start the key and value stream before the prologue
 #pragma unroll
-    for (int i = 0; i < C::NSTG - 1; i++) {
+    for (int i = 0; i < C::NSTG2 - 1; i++) {
         if (i < nsc) {
             dec2_issue<D>(stg_a + i * C::ST2, K + (size_t)i * C::SUB * D, ke - kb - i * C::SUB, lane);
             dec2_issue<D>(stg_a + i * C::ST2 + C::SUB * C::RB, V + (size_t)i * C::SUB * D, ke - kb - i * C::SUB,
@@ -581,16 +582,16 @@ __global__ void __launch_bounds__(Dec2<D>::DW2 * 32) dec2_pass2(const __nv_bfloa
 #pragma unroll
     for (int t = 0; t < 8; t++) acc[t] = 0.f;
     for (int sc = 0; sc < nsc; sc++) {
-        const int nx = sc + C::NSTG - 1;
+        const int nx = sc + C::NSTG2 - 1;
         if (nx < nsc) {
-            const uint32_t sa = stg_a + (nx % C::NSTG) * C::ST2;
+            const uint32_t sa = stg_a + (nx % C::NSTG2) * C::ST2;
             dec2_issue<D>(sa, K + (size_t)nx * C::SUB * D, ke - kb - nx * C::SUB, lane);
             dec2_issue<D>(sa + C::SUB * C::RB, V + (size_t)nx * C::SUB * D, ke - kb - nx * C::SUB, lane);
         }
         cp_async_commit();
-        cp_async_wait<C::NSTG - 1>();
+        cp_async_wait<C::NSTG2 - 1>();
         __syncwarp();
-        const uint8_t* st = stg + (sc % C::NSTG) * C::ST2;
+        const uint8_t* st = stg + (sc % C::NSTG2) * C::ST2;
         const bool valid = kb + sc * C::SUB + lane < ke;
         float sx, sg;
         dec2_dots<D, true>(st, lane, qs, us, sx, sg);
