@@ -21,8 +21,9 @@
 // bf16 caches take a streaming form of the same steps (dec2_*): each warp
 // owns a range of keys (a multiple of 32, sized on the host so that each
 // pass's grid is one wave of resident CTAs) and pulls it through shared
-// memory in 32-key sub-chunks with a three-stage cp.async pipeline, so every
-// warp keeps two sub-chunks in flight while it computes on the third; the
+// memory in 32-key sub-chunks with a cp.async pipeline (three stages in pass
+// 1, so two sub-chunks are in flight while the warp computes on the third;
+// two in pass 2, whose stages hold K and V, so that more warps fit); the
 // warp keeps an online softmax (pass 1) or a running weighted sum (pass 2)
 // and the CTA folds its warps into one partial.  Pass 2 merges pass 1's
 // partials and forms u and gbar in its own prologue, and the last pass-2 CTA
