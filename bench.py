@@ -372,8 +372,10 @@ def run_ours(args, world, rank):
         if fpp is not None:
             achieved = pairs * fpp * d / avg_s / 1e12
             if dom.startswith("tc_"):
-                peak, bound = peaks["bf16_tflops_sustained"], "tensor"
-                peak_note = f"bf16 dense, {peaks['source']} sustained"
+                # the timed region lasts well under a second: the burst peak
+                # (a kernel timed alone), not the seconds-long sustained one
+                peak, bound = peaks["bf16_tflops"], "tensor"
+                peak_note = f"bf16 dense, {peaks['source']} burst (timed region under a second)"
             else:
                 peak, bound = fp32_simt_peak_tflops(peaks["sm_max_mhz"]), "alu"
                 peak_note = "fp32 FFMA: 148 SMs x 128 lanes x 2 x max SM clock"
@@ -381,7 +383,7 @@ def run_ours(args, world, rank):
                         "frac": achieved / peak, "traffic": measured_traffic(dom), "peak_source": peak_note,
                         "flops_per_launch": pairs * fpp * d}
     # whole-step fraction of the tensor peak
-    pct_peak = value / world / peaks["bf16_tflops_sustained"]
+    pct_peak = value / world / peaks["bf16_tflops"]
 
     # forward / backward split (timed separately, same inputs)
     fwd_ms, bwd_ms = split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream,
@@ -618,6 +620,32 @@ def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
             "api": "parallax_step_host", "head_groups": chunks}
 
 
+def run_case(args):
+    """One extra workload alone on cuda:0 (inputs resident in HBM), printed as
+    a JSON line of its own figures; not the benchmark line."""
+    import torch
+    import parallax_local_linear_fwd_b300 as plx
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    plx.parallax_set_path(plx.PLX_PATH_AUTO)
+    if args.case == "fwd_c3":
+        res = forward_workload(torch, plx, "c3", dev, stream, iters=args.steps, warmup=args.warmup)
+    elif args.case == "probe_c3":
+        res = probe_workload(torch, plx, "c3", dev, stream, iters=args.steps, warmup=args.warmup)
+    else:
+        w = plx_synth.WORKLOADS["c4"]
+        inp = plx_synth.generate_workload("c4")
+        k, v, P = (torch.from_numpy(inp[x].view(np.int16)).view(torch.bfloat16).to(dev) if inp[x].dtype == np.uint16
+                   else torch.from_numpy(inp[x]).to(dev) for x in ("k", "v", "P"))
+        res = decode_workload(torch, plx, k, v, P, stream, iters=args.steps, warmup=args.warmup)
+    code, detail = plx.parallax_last_device_error(stream)
+    if code != plx.PLX_OK:
+        raise RuntimeError(f"device watchdog: {plx.parallax_strerror(code)} detail={detail:#x}")
+    print(json.dumps({"case": args.case, **res}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,11 +656,16 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-c3", action="store_true",
                     help="skip the extra measurements: the B4 H16 T4096 d128 forward and the decode step")
+    ap.add_argument("--case", default="step", choices=["step", "fwd_c3", "probe_c3", "decode"],
+                    help="step: the benchmark (default). The others run one of the extra workloads alone "
+                         "and print its figures (used for profiling a single kernel family)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as run
     world, rank, _ = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.case != "step":
+        run_case(args)
     else:
         run_ours(args, world, rank)
 

@@ -32,7 +32,16 @@
  *    asynchronous on it; the return code covers argument checks and launch
  *    errors only.  A device-side watchdog (bounded waits inside kernels) is
  *    read back by parallax_last_device_error().
- *  - Supported: d in {64, 128}; T >= 1; B, H >= 1; B*H*T*d < 2^31.
+ *  - Supported: d in {64, 128}; T >= 1; B, H >= 1; B*H*T*d < 2^31 (else
+ *    PLX_ERR_INVALID_ARG); B*H <= 65535 (else PLX_ERR_UNSUPPORTED: the
+ *    kernels index heads by a grid dimension of that size).
+ *  - Input range of the bf16 tensor-core kernels: every matrix-multiply
+ *    operand is float16 with float32 accumulation.  A bf16 input converts to
+ *    f16 exactly when its magnitude lies in [2^-14, 65504] (or is zero);
+ *    smaller magnitudes keep an absolute error below 2^-25, and larger ones
+ *    SATURATE to +-65504 without any status.  Inputs q, k, v, dout (and rho)
+ *    must therefore stay below 65504 in magnitude on that path; the fp32
+ *    path (PLX_FP32, or PLX_PATH_SIMT) has no such limit.
  *  - The library never aborts, never prints and never throws across the ABI.
  */
 #ifndef PARALLAX_H

@@ -125,14 +125,73 @@ def _check(code: int, where: str):
 
 
 def _shape(q):
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, T, d]")
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
+        raise ValueError("q must be a [B, H, T, d] tensor")
     return tuple(int(x) for x in q.shape)
+
+
+def _expect(name, t, shape, dtype, device, optional=False):
+    """Checks one tensor argument against the shape, dtype and device the C
+    ABI will assume for it; every pointer that reaches the library has passed
+    this, so a mismatched tensor cannot make a kernel read or write past it."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cuda_device(q):
+    if q.device.type != "cuda":
+        raise ValueError(f"tensors must be on a CUDA device, got {q.device}")
+    return q.device
+
+
+def _on(t):
+    """The library launches on the current device: make it the tensors' own."""
+    return torch.cuda.device(t.device)
+
+
+def _expect_workspace(ws, nbytes, device):
+    if ws is None:
+        return
+    if not isinstance(ws, torch.Tensor) or ws.device != device or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    if ws.numel() * ws.element_size() < nbytes:
+        raise ValueError(f"workspace holds {ws.numel() * ws.element_size()} bytes, needs {nbytes}")
+
+
+def _check_dtype(q):
+    _dtype_code(q)
+    return q.dtype
+
+
+def _fwd_checks(q, k, v, P, out, lse, mu_k):
+    B, H, T, d = _shape(q)
+    dt = _check_dtype(q)
+    dev = q.device
+    for name, t in (("k", k), ("v", v)):
+        _expect(name, t, (B, H, T, d), dt, dev)
+    _expect("P", P, (H, d, d), torch.float32, dev)
+    _expect("out", out, (B, H, T, d), dt, dev, optional=True)
+    _expect("lse", lse, (B, H, T), torch.float32, dev, optional=True)
+    _expect("mu_k", mu_k, (B, H, T, d), torch.float32, dev, optional=True)
+    _cuda_device(q)
+    return B, H, T, d
 
 
 def parallax_fwd(q, k, v, P, out=None, lse=None, mu_k=None, stream=None):
     """Forward; returns (out, lse, mu_k).  q, k, v: [B,H,T,d] fp32/bf16 (CUDA)."""
-    B, H, T, d = _shape(q)
+    B, H, T, d = _fwd_checks(q, k, v, P, out, lse, mu_k)
     dt = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
@@ -140,8 +199,9 @@ def parallax_fwd(q, k, v, P, out=None, lse=None, mu_k=None, stream=None):
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     if mu_k is None:
         mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
-    _check(lib().parallax_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
-                              B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd")
+    with _on(q):
+        _check(lib().parallax_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                                  B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd")
     return out, lse, mu_k
 
 
@@ -154,7 +214,7 @@ def parallax_fwd_noalloc(q, k, v, P, out=None, lse=None, mu_k=None, stream=None)
     fixed 32 MiB scratch limits the size; larger problems raise PlxError with
     PLX_ERR_TOO_LARGE.  Calls that overlap on the GPU race on that scratch.
     """
-    B, H, T, d = _shape(q)
+    B, H, T, d = _fwd_checks(q, k, v, P, out, lse, mu_k)
     dt = _dtype_code(q)
     if out is None:
         out = torch.empty_like(q)
@@ -162,16 +222,22 @@ def parallax_fwd_noalloc(q, k, v, P, out=None, lse=None, mu_k=None, stream=None)
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     if mu_k is None:
         mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
-    _check(lib().parallax_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
-                                      B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd_noalloc")
+    with _on(q):
+        _check(lib().parallax_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                                          B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd_noalloc")
     return out, lse, mu_k
 
 
 def parallax_fwd_ws(q, k, v, P, out, lse, mu_k, workspace, stream=None):
-    B, H, T, d = _shape(q)
-    _check(lib().parallax_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
-                                 _ptr(workspace), B, H, T, d, _dtype_code(q), _stream_ptr(stream)),
-           "parallax_fwd_ws")
+    for name, t in (("out", out), ("lse", lse), ("mu_k", mu_k), ("workspace", workspace)):
+        if t is None:
+            raise ValueError(f"{name} is required")
+    B, H, T, d = _fwd_checks(q, k, v, P, out, lse, mu_k)
+    _expect_workspace(workspace, parallax_fwd_workspace_bytes(B, H, T, d, _dtype_code(q)), q.device)
+    with _on(q):
+        _check(lib().parallax_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(out), _ptr(lse), _ptr(mu_k),
+                                     _ptr(workspace), B, H, T, d, _dtype_code(q), _stream_ptr(stream)),
+               "parallax_fwd_ws")
     return out, lse, mu_k
 
 
@@ -188,13 +254,26 @@ def parallax_bwd(q, k, v, P, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None
     """Backward of sum(dout * out); returns (dq, dk, dv, dP)."""
     B, H, T, d = _shape(q)
     dt = _dtype_code(q)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _expect(name, t, (B, H, T, d), q.dtype, dev)
+    _expect("P", P, (H, d, d), torch.float32, dev)
+    _expect("lse", lse, (B, H, T), torch.float32, dev)
+    _expect("mu_k", mu_k, (B, H, T, d), torch.float32, dev)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(name, t, (B, H, T, d), q.dtype, dev, optional=True)
+    _expect("dP", dP, (H, d, d), torch.float32, dev, optional=True)
+    _cuda_device(q)
+    if workspace is not None:
+        _expect_workspace(workspace, parallax_bwd_workspace_bytes(B, H, T, d, dt), dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     dP = torch.empty_like(P) if dP is None else dP
-    _check(lib().parallax_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(lse), _ptr(mu_k),
-                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
-                              B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
+    with _on(q):
+        _check(lib().parallax_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(lse), _ptr(mu_k),
+                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
+                                  B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
     return dq, dk, dv, dP
 
 
@@ -206,10 +285,20 @@ def parallax_fwd_probe(q, k, v, rho, out=None, lse=None, workspace=None, stream=
     """One-pass forward with a given probe rho [B,H,T,d] (bf16): o = o^SA - Sigma_KV rho.
     Returns (out, lse)."""
     B, H, T, d = _shape(q)
+    dt = _check_dtype(q)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("rho", rho)):
+        _expect(name, t, (B, H, T, d), dt, dev)
+    _expect("out", out, (B, H, T, d), dt, dev, optional=True)
+    _expect("lse", lse, (B, H, T), torch.float32, dev, optional=True)
+    _cuda_device(q)
+    if workspace is not None:
+        _expect_workspace(workspace, parallax_fwd_probe_workspace_bytes(B, H, T, d, _dtype_code(q)), dev)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(lib().parallax_fwd_probe(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(workspace),
-                                    B, H, T, d, _dtype_code(q), _stream_ptr(stream)), "parallax_fwd_probe")
+    with _on(q):
+        _check(lib().parallax_fwd_probe(_ptr(q), _ptr(k), _ptr(v), _ptr(rho), _ptr(out), _ptr(lse), _ptr(workspace),
+                                        B, H, T, d, _dtype_code(q), _stream_ptr(stream)), "parallax_fwd_probe")
     return out, lse
 
 
@@ -220,17 +309,27 @@ def parallax_decode_workspace_bytes(B, H, Lmax, d, dtype) -> int:
 def parallax_decode(q, k_cache, v_cache, P, lens=None, out=None, lse=None, workspace=None, stream=None):
     """Decode step: q [B,H,d] against caches [B,H,Lmax,d] (fp32/bf16, CUDA);
     lens: int32 [B] valid keys per sequence (None: Lmax).  Returns (out, lse)."""
-    if q.dim() != 3 or k_cache.dim() != 4:
-        raise ValueError("q must be [B, H, d] and the caches [B, H, Lmax, d]")
+    if not isinstance(k_cache, torch.Tensor) or k_cache.dim() != 4:
+        raise ValueError("the caches must be [B, H, Lmax, d] tensors")
     B, H, Lmax, d = (int(x) for x in k_cache.shape)
-    dt = _dtype_code(q)
-    if lens is not None and (lens.dtype != torch.int32 or lens.numel() != B):
-        raise ValueError("lens must be int32 [B]")
+    dt = _dtype_code(k_cache)
+    dev = k_cache.device
+    _expect("q", q, (B, H, d), k_cache.dtype, dev)
+    _expect("v_cache", v_cache, (B, H, Lmax, d), k_cache.dtype, dev)
+    _expect("k_cache", k_cache, (B, H, Lmax, d), k_cache.dtype, dev)
+    _expect("P", P, (H, d, d), torch.float32, dev)
+    _expect("lens", lens, (B,), torch.int32, dev, optional=True)
+    _expect("out", out, (B, H, d), k_cache.dtype, dev, optional=True)
+    _expect("lse", lse, (B, H), torch.float32, dev, optional=True)
+    _cuda_device(k_cache)
+    if workspace is not None:
+        _expect_workspace(workspace, parallax_decode_workspace_bytes(B, H, Lmax, d, dt), dev)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(lib().parallax_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(P), _ptr(out),
-                                 _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
-           "parallax_decode")
+    with _on(k_cache):
+        _check(lib().parallax_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(P), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
+               "parallax_decode")
     return out, lse
 
 
@@ -244,9 +343,16 @@ def parallax_step_host(q, k, v, P, dout, out=None, dq=None, dk=None, dv=None, dP
     `stream`: synchronize it before reading the outputs.  Returns (out, dq, dk, dv, dP, lse, mu_k).
     """
     B, H, T, d = _shape(q)
-    for t in (q, k, v, P, dout, out, dq, dk, dv, dP, lse, mu_k):
-        if t is not None and t.device.type != "cpu":
-            raise ValueError("parallax_step_host takes host (CPU) tensors")
+    dt = _check_dtype(q)
+    cpu = torch.device("cpu")
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _expect(name, t, (B, H, T, d), dt, cpu)
+    _expect("P", P, (H, d, d), torch.float32, cpu)
+    for name, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(name, t, (B, H, T, d), dt, cpu, optional=True)
+    _expect("dP", dP, (H, d, d), torch.float32, cpu, optional=True)
+    _expect("lse", lse, (B, H, T), torch.float32, cpu, optional=True)
+    _expect("mu_k", mu_k, (B, H, T, d), torch.float32, cpu, optional=True)
 
     def alloc(like):
         return torch.empty(like.shape, dtype=like.dtype).pin_memory()
