@@ -295,8 +295,20 @@ def run_ours(args, world, rank):
     if world > 1:
         dist_init("nccl")
     w = plx_synth.WORKLOADS[args.workload]
-    inp = plx_synth.generate_workload(args.workload, seed=rank_seed(w.seed, rank), backward=True)
-    B, H, T, d = w.B, w.H, w.T, w.d
+    if args.shard == "batch":
+        # one problem split by batch: every rank draws the same inputs and
+        # keeps its slice; dP_h is summed across ranks inside the step
+        from parallax_local_linear_fwd_b300.shard import shard_range
+        inp = plx_synth.generate_workload(args.workload, backward=True)
+        lo, hi = shard_range(w.B, rank, world)
+        if hi <= lo:
+            raise SystemExit(f"--shard batch needs at least one batch per rank (B={w.B}, ranks={world})")
+        inp = {n: (x[lo:hi] if n in ("q", "k", "v", "dout") else x) for n, x in inp.items()}
+        B = hi - lo
+    else:
+        inp = plx_synth.generate_workload(args.workload, seed=rank_seed(w.seed, rank), backward=True)
+        B = w.B
+    H, T, d = w.H, w.T, w.d
 
     def host(x):
         if x.dtype == np.uint16:
@@ -323,6 +335,9 @@ def run_ours(args, world, rank):
     def step():
         plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
         plx.parallax_bwd(q, k, v, P, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+        if args.shard == "batch" and world > 1:
+            from parallax_local_linear_fwd_b300.shard import allreduce_dP
+            allreduce_dP(dP)
 
     for _ in range(args.warmup):
         step()
@@ -356,7 +371,11 @@ def run_ours(args, world, rank):
 
     pairs = plx_synth.causal_pairs(B, H, T)
     flops_step = pairs * (FWD_FLOPS_PER_PAIR_D + BWD_FLOPS_PER_PAIR_D) * d
-    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    # the whole job's work per step: N independent problems (head replicas),
+    # or one problem split by batch
+    job_pairs = plx_synth.causal_pairs(w.B, H, T) if args.shard == "batch" else world * pairs
+    job_flops_step = job_pairs * (FWD_FLOPS_PER_PAIR_D + BWD_FLOPS_PER_PAIR_D) * d
+    value = job_flops_step * args.steps / (ms / 1e3) / 1e12
     peaks = load_peaks()
 
     # dominant kernel and its live roofline
@@ -383,22 +402,26 @@ def run_ours(args, world, rank):
                         "frac": achieved / peak, "traffic": measured_traffic(dom), "peak_source": peak_note,
                         "flops_per_launch": pairs * fpp * d}
     # whole-step fraction of the tensor peak
-    pct_peak = value / world / peaks["bf16_tflops"]
+    pct_peak = flops_step * args.steps / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]
 
     # forward / backward split (timed separately, same inputs)
     fwd_ms, bwd_ms = split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws, bws, stream,
                                    max(3, args.steps // 2))
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step)
+    e2e = run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, job_flops_step,
+                  allreduce=args.shard == "batch" and world > 1)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "strong" if args.shard == "batch" else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, path),
+        "config": {**workload_config(w, path),
+                   "parallelism": (f"batch-shard x{world} (dP all-reduce)" if args.shard == "batch"
+                                   else f"independent head sets x{world}")},
         "pct_of_bf16_peak": pct_peak,
-        "tokens_per_s": world * B * T * args.steps / (ms / 1e3),
+        "tokens_per_s": (w.B if args.shard == "batch" else world * B) * T * args.steps / (ms / 1e3),
         "fwd": {"ms": fwd_ms, "tflops": pairs * FWD_FLOPS_PER_PAIR_D * d / (fwd_ms / 1e3) / 1e12},
         "bwd": {"ms": bwd_ms, "tflops": pairs * BWD_FLOPS_PER_PAIR_D * d / (bwd_ms / 1e3) / 1e12},
         "gpu_launches": launches,
@@ -585,7 +608,7 @@ def split_fwd_bwd(torch, plx, q, k, v, P, out, lse, mu, do, dq, dk, dv, dP, fws,
     return ev[0].elapsed_time(ev[1]) / n, ev[1].elapsed_time(ev[2]) / n
 
 
-def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
+def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, job_flops_step, allreduce=False):
     """Same step through the public host-buffer entry point, parallax_step_host:
     from pinned host inputs to pinned host outputs, with the H2D copies, the
     forward + backward and the D2H copies (overlapped by head groups) all
@@ -594,6 +617,7 @@ def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
         ("out", (B, H, T, d), h_in["q"].dtype), ("dq", (B, H, T, d), h_in["q"].dtype),
         ("dk", (B, H, T, d), h_in["q"].dtype), ("dv", (B, H, T, d), h_in["q"].dtype),
         ("dP", (H, d, d), torch.float32))}
+    dP_dev = torch.empty(h_out["dP"].shape, dtype=torch.float32, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
     chunks = min(H, 8)
@@ -602,6 +626,13 @@ def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
         plx.parallax_step_host(h_in["q"], h_in["k"], h_in["v"], h_in["P"], h_in["dout"], out=h_out["out"],
                                dq=h_out["dq"], dk=h_out["dk"], dv=h_out["dv"], dP=h_out["dP"], chunks=chunks,
                                stream=stream)
+        if allreduce:
+            # the batch-shard exchange: the host dP of every rank summed
+            import torch.distributed as dist
+            stream.synchronize()
+            dP_dev.copy_(h_out["dP"])
+            dist.all_reduce(dP_dev)
+            h_out["dP"].copy_(dP_dev)
 
     n = max(3, args.steps // 2)
     for _ in range(2):
@@ -615,7 +646,7 @@ def run_e2e(torch, plx, h_in, dev, stream, args, B, H, T, d, world, flops_step):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    return {"value": world * flops_step * n / (ms / 1e3) / 1e12, "unit": UNIT, "steps": n,
+    return {"value": job_flops_step * n / (ms / 1e3) / 1e12, "unit": UNIT, "steps": n,
             "ms_per_step": ms / n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "parallax_step_host", "head_groups": chunks}
 
@@ -656,6 +687,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-c3", action="store_true",
                     help="skip the extra measurements: the B4 H16 T4096 d128 forward and the decode step")
+    ap.add_argument("--shard", default="heads", choices=["heads", "batch"],
+                    help="heads: every rank runs its own independent set of heads (no collective); batch: "
+                         "the ranks split one problem's batch and all-reduce dP_h each step")
     ap.add_argument("--case", default="step", choices=["step", "fwd_c3", "probe_c3", "decode"],
                     help="step: the benchmark (default). The others run one of the extra workloads alone "
                          "and print its figures (used for profiling a single kernel family)")

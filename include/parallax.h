@@ -41,7 +41,11 @@
  *    smaller magnitudes keep an absolute error below 2^-25, and larger ones
  *    SATURATE to +-65504 without any status.  Inputs q, k, v, dout (and rho)
  *    must therefore stay below 65504 in magnitude on that path; the fp32
- *    path (PLX_FP32, or PLX_PATH_SIMT) has no such limit.
+ *    path (PLX_FP32, or PLX_PATH_SIMT) has no such limit.  The probe u and
+ *    the weights p (1 + g - gbar) are rounded to f16 as well (relative
+ *    2^-11), so the correction is accurate to about 2^-11 |g|: where
+ *    g = k . u reaches 1e3 or more, the output depends on P beyond that
+ *    precision, and the fp32 path is the one to use.
  *  - The library never aborts, never prints and never throws across the ABI.
  */
 #ifndef PARALLAX_H
@@ -236,6 +240,24 @@ PLX_API int parallax_step_host(const void* q, const void* k, const void* v, cons
  * receives the raw word (kernel id << 16 | wait site) of the first timeout.
  */
 PLX_API int parallax_last_device_error(void* stream, unsigned* detail);
+
+/*
+ * Failure-detection hook.  Sets how long a bounded wait inside the
+ * tensor-core kernels of the current device may take, in SM clock cycles,
+ * before it gives up; cycles <= 0 restores the default (4e9 cycles, about
+ * two seconds).  A wait that gives up records (kernel id << 16 | wait site)
+ * in the device's status word and raises its CTA's abort flag; every role of
+ * the CTA then leaves its loop, waits (with the long bound) for the copies
+ * and MMAs it has in flight, releases its TMEM and returns, so the context
+ * stays usable and parallax_last_device_error() reports PLX_ERR_TIMEOUT.
+ * A short limit makes waits that would have completed time out: it exists
+ * to exercise that path in tests, and the outputs of calls made under it
+ * are unspecified.  Synchronises the device; applies to kernels launched
+ * after it returns.  The setting is kept until changed (reading the status
+ * with parallax_last_device_error() does not reset it).
+ * Returns PLX_OK, PLX_ERR_UNSUPPORTED (not an sm_103 device) or PLX_ERR_CUDA.
+ */
+PLX_API int parallax_set_wait_limit(long long cycles);
 
 /* Selects the kernel family for later calls in this process; returns the
  * previous setting, or -1 if `path` is not a PLX_PATH_* value. */

@@ -25,7 +25,7 @@ __all__ = [
     "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
     "parallax_timing_get", "parallax_timing_reset", "kernel_times",
     "parallax_decode", "parallax_decode_workspace_bytes",
-    "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes",
+    "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes", "parallax_set_wait_limit",
 ]
 
 PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -48,6 +48,7 @@ _SIGNATURES = {
     "parallax_bwd": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_last_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "parallax_set_path": (_i, [_i]),
+    "parallax_set_wait_limit": (_i, [ctypes.c_longlong]),
     "parallax_strerror": (ctypes.c_char_p, [_i]),
     "parallax_launch_count": (ctypes.c_ulonglong, []),
     "parallax_timing_enable": (_i, [_i]),
@@ -377,6 +378,13 @@ def parallax_last_device_error(stream=None):
 
 def parallax_set_path(path: int) -> int:
     return int(lib().parallax_set_path(path))
+
+
+def parallax_set_wait_limit(cycles: int) -> None:
+    """Bounded-wait limit of the tensor-core kernels on the current device,
+    in SM cycles (<= 0: the default, about two seconds).  A test hook for the
+    watchdog path: a short limit makes waits time out on purpose."""
+    _check(lib().parallax_set_wait_limit(int(cycles)), "parallax_set_wait_limit")
 
 
 def parallax_strerror(code: int) -> str:

@@ -15,11 +15,19 @@
 // that loads this library holds it until the process exits.  Host code cannot
 // use the array's name as a device address.  The first call on each device
 // therefore looks up the address with cudaGetSymbolAddress, with that device
-// current, and caches it.  Make that first call outside any stream capture.
+// current, and caches it together with the identity of the device's CUDA
+// context.  A later call in another context of that device (after
+// cudaDeviceReset destroyed the one the address belonged to) looks the
+// address up again instead of using a stale one.  Make the first call, and
+// the first call after a reset, outside any stream capture.
 // All calls share the one array, which keeps the last call's contents.  The
 // forward writes every scratch element it reads, so nothing needs clearing.
 // Calls that overlap on the GPU (different streams, or threads that share a
 // device) race on the array, and the caller must serialise them.
+// The SIMT forward kernels have no bounded device waits, so no watchdog word
+// is needed either: this path touches no memory but the caller's buffers and
+// the static array.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,34 +42,60 @@ constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
-static __device__ __align__(16) unsigned g_noalloc_status[4];
 
 std::mutex g_noalloc_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
-unsigned* g_status_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // context the address belongs to
 
-// Once per device, with that device current: look up the device addresses of
-// the static arrays.  No allocation happens here.
-int noalloc_setup(void** scratch, unsigned** status) {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Identity of the calling thread's current CUDA context (unique for the
+// process's lifetime, so a context created after a reset never repeats it).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = (CtxGetCurrentFn)p;
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = (CtxGetIdFn)p;
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Once per device and context, with that device current: look up the device
+// address of the static array.  No allocation happens here.
+int noalloc_setup(void** scratch) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PLX_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PLX_ERR_UNSUPPORTED;
+    // cudaGetDevice alone does not create the context; cudaSetDevice does
+    // (it initialises the device's primary context) and allocates nothing
+    if (cudaSetDevice(dev) != cudaSuccess) return PLX_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) return PLX_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return PLX_ERR_CUDA;
         if (major != 10 || minor != 3) return PLX_ERR_UNSUPPORTED;
         void* s = nullptr;
-        void* st = nullptr;
         if (cudaGetSymbolAddress(&s, g_noalloc_scratch) != cudaSuccess || s == nullptr) return PLX_ERR_CUDA;
-        if (cudaGetSymbolAddress(&st, g_noalloc_status) != cudaSuccess || st == nullptr) return PLX_ERR_CUDA;
-        g_status_ptr[dev] = (unsigned*)st;
         g_scratch_ptr[dev] = s;
+        g_scratch_ctx[dev] = ctx;
     }
     *scratch = g_scratch_ptr[dev];
-    *status = g_status_ptr[dev];
     return PLX_OK;
 }
 
@@ -83,9 +117,8 @@ extern "C" int parallax_fwd_noalloc(const void* q, const void* k, const void* v,
         return PLX_ERR_INVALID_ARG;
     if (plx::simt_fwd_ws_bytes(B, H, T, d) > kScratchBytes) return PLX_ERR_TOO_LARGE;
     void* scratch = nullptr;
-    unsigned* status = nullptr;
-    int rc = noalloc_setup(&scratch, &status);
+    int rc = noalloc_setup(&scratch);
     if (rc) return rc;
-    plx::FwdArgs a{q, k, v, P, out, lse, mu_k, scratch, B, H, T, d, dtype, (cudaStream_t)stream, status};
+    plx::FwdArgs a{q, k, v, P, out, lse, mu_k, scratch, B, H, T, d, dtype, (cudaStream_t)stream, nullptr};
     return plx::simt_fwd(a) == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }

@@ -480,8 +480,24 @@ int parallax_last_device_error(void* stream, unsigned* detail) {
     if (cudaMemcpy(word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return PLX_ERR_CUDA;
     if (word[0] == 0) return PLX_OK;
     if (detail) *detail = word[1];
-    if (cudaMemset(status, 0, sizeof(word)) != cudaSuccess) return PLX_ERR_CUDA;
+    // clear the flag and the detail; word [2] (the wait limit) stays
+    if (cudaMemset(status, 0, 2 * sizeof(unsigned)) != cudaSuccess) return PLX_ERR_CUDA;
     return PLX_ERR_TIMEOUT;
+}
+
+int parallax_set_wait_limit(long long cycles) {
+    unsigned* status = nullptr;
+    int rc = device_state(&status);
+    if (rc) return rc;
+    // word [2] of the status word, in units of 64 cycles (0 = the default)
+    unsigned units = 0;
+    if (cycles > 0) {
+        const long long u = (cycles + 63) / 64;
+        units = u > 0xFFFFFFFFll ? 0xFFFFFFFFu : (unsigned)u;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return PLX_ERR_CUDA;
+    if (cudaMemcpy(status + 2, &units, sizeof(units), cudaMemcpyHostToDevice) != cudaSuccess) return PLX_ERR_CUDA;
+    return PLX_OK;
 }
 
 int parallax_set_path(int path) {

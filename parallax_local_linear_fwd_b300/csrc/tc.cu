@@ -44,6 +44,13 @@ constexpr int NTHREADS = 192;
 // moved when a row max exceeds it by more than this, so p~ <= 2^8.
 constexpr float RESCALE_TH = 8.f;
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int qt = ntq - 1 - rank;  // longest rows first
     const int q0 = qt * C::BM;
     const int nkt = min(qt, (T - 1) / C::BN) + 1;
-    const Watchdog wd{status, abortf, KID_TC_PASS1};
+    const Watchdog wd{status, abortf, KID_TC_PASS1, wait_limit(status)};
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -279,15 +286,25 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             tc_fence_after();
             const int k0 = j * C::BN;
             const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;  // key k0 + c valid iff c <= lim
-            float mx = -INFINITY;
+            // the row's whole score tile in registers: one TMEM round trip
+            uint32_t v[C::BN];
 #pragma unroll
-            for (int c = 0; c < C::BN / 32; c++) {
-                uint32_t v[32];
-                tmem_ld32(tS + lrow + c * 32, v);
-                tmem_wait_ld();
+            for (int c = 0; c < C::BN / 32; c++) tmem_ld32(tS + lrow + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+            tmem_wait_ld();
+            if (lim < C::BN) {  // the diagonal tile only: masked keys score -inf (weight 0)
 #pragma unroll
-                for (int i = 0; i < 32; i++)
-                    if (c * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+                for (int i = 0; i < C::BN; i++)
+                    if (i > lim) v[i] = __float_as_uint(-INFINITY);
+            }
+            float mx;
+            {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < C::BN; i += 8)
+#pragma unroll
+                    for (int u = 0; u < 4; u++)
+                        m4[u] = fmax3(m4[u], __uint_as_float(v[i + 2 * u]), __uint_as_float(v[i + 2 * u + 1]));
+                mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
             }
             mx *= scale_log2;
             const float m_new = fmaxf(m_use, mx);
@@ -298,49 +315,44 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 m_use = m_new;
             }
             l *= alpha;
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                ok = mbar_wait(o_done, (j - 1) & 1, wd, 7);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(tMu + lrow + c * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(tMu + lrow + c * 32, v);
-                }
-            }
             const uint64_t SL2 = f2(scale_log2, scale_log2), NM2 = f2(-m_use, -m_use);
-            const bool need_mask = lim < C::BN;
             uint64_t sum2 = f2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < C::BN / 32; c++) {
-                uint32_t v[32];
-                tmem_ld32(tS + lrow + c * 32, v);
-                tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1: one f32x2 op each
-                    const int c0 = c * 32 + 2 * i;
-                    const float2 x = uf2(ffma2(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), SL2, NM2));
-                    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                    if (need_mask) {
-                        if (c0 > lim) p0 = 0.f;
-                        if (c0 + 1 > lim) p1 = 0.f;
-                    }
-                    const uint64_t p2 = f2(p0, p1);
-                    sum2 = fadd2(sum2, p2);
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1: one f32x2 op each (2^-inf = 0)
+                    const uint32_t* vv = v + c * 32 + 2 * i;
+                    const float2 x = uf2(ffma2(f2(__uint_as_float(vv[0]), __uint_as_float(vv[1])), SL2, NM2));
+                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    sum2 = fadd2(sum2, f2(p0, p1));
                     pk[i] = pack_f16(p0, p1);
                 }
                 tmem_st16(tS + lrow + c * 16, pk);
             }
             const float2 sp = uf2(sum2);
             l += sp.x + sp.y;
+            // rescale the accumulator to the moved maximum once the previous
+            // tile's P~ K has landed, before this tile's is issued (the score
+            // row is dead by now, which keeps the registers for it)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok = mbar_wait(o_done, (j - 1) & 1, wd, 7);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    tmem_wait_st();
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t u[32];
+                    tmem_ld32(tMu + lrow + c * 32, u);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                    tmem_st32(tMu + lrow + c * 32, u);
+                }
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_full);
@@ -503,7 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const int qt = ntq - 1 - rank;
     const int q0 = qt * C::BM;
     const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
-    const Watchdog wd{status, abortf, MODE == 0 ? (unsigned)KID_TC_PASS2 : (unsigned)KID_TC_BWD_B1};
+    const Watchdog wd{status, abortf, MODE == 0 ? (unsigned)KID_TC_PASS2 : (unsigned)KID_TC_BWD_B1, wait_limit(status)};
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -691,6 +703,281 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
 }
 
+// ============================================ dual-score pass, two query tiles
+// The d = 128 form of tc_dual.  Two 128-row A tiles (Q and U, or Q and dO)
+// take 64 KB of shared memory per query tile, so two independent CTAs per SM
+// leave room for one K|V stage each, and every key tile's load latency is
+// exposed.  Here one CTA per SM holds two adjacent query tiles, a = 2m and
+// b = 2m + 1, which read the same key tiles (b one 128-key block further):
+// three K|V stages serve both, and each key tile is loaded once for the two.
+// Warpgroup 0 (warps 2-5) forms tile a's weights and warpgroup 1 (warps 6-9)
+// tile b's, so the tensor core works on one tile while the other tile's
+// weights are formed.  The MMA thread issues, per key tile j:
+//   Acc_a += W_a(j) V,  S_a(j+1) | X_a(j+1),  Acc_b += W_b(j) V,  S_b(j+1) | X_b(j+1)
+// TMEM: tile x at column 256 x: S [0,64) (W aliases [0,32)), X [64,128),
+// Acc [128,256).
+template <int D>
+struct DualPP {
+    static constexpr int BM = 128, BN = 64, NT = 320;
+    static constexpr int NS = 3;             // K+V stages, shared by both tiles
+    static constexpr int AB = BM * D * 2;    // one A tile (Q, U or dO)
+    static constexpr int KB = BN * D * 2;    // one K or V tile
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 1;
+    static constexpr int SMEM = 1024 + 4 * AB + NS * 2 * KB + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 512;
+    static_assert(SMEM <= 232448, "one CTA per SM must fit");
+};
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(DualPP<D>::NT, 1)
+    tc_dual_pp(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
+               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const float* __restrict__ lse, const float* __restrict__ gbar, void* __restrict__ acc_out,
+               float* __restrict__ ebar_out, int T, int BH, int npairs, float scale_log2, unsigned* status) {
+    using C = DualPP<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sA = sm;                   // tile x: A1 at 2x AB, A2 at (2x + 1) AB
+    uint8_t* sKV = sA + 4 * C::AB;      // stage s: K at s * 2KB, V at s * 2KB + KB
+    uint64_t* bars = (uint64_t*)(sKV + NS * 2 * C::KB);
+    uint64_t* a_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + NS;
+    uint64_t* s_full = kv_empty + NS;   // [2]
+    uint64_t* w_full = s_full + 2;      // [2]
+    uint64_t* acc_done = w_full + 2;    // [2]
+    uint64_t* drain = acc_done + 2;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int rank, bh;
+    work_item(blockIdx.x, BH, npairs, &rank, &bh);
+    const int m = npairs - 1 - rank;  // longest pairs first
+    // tile a (x = 0) is always inside the sequence; tile b (x = 1) may lie past T
+    const int q0a = 2 * m * C::BM, q0b = q0a + C::BM;
+    const int nkta = min(q0a + C::BM - 1, T - 1) / C::BN + 1;
+    const int nktb = q0b < T ? min(q0b + C::BM - 1, T - 1) / C::BN + 1 : 0;
+    const int nk = nktb > nkta ? nktb : nkta;
+    const int ntiles = nktb > 0 ? 2 : 1;
+    const Watchdog wd{status, abortf, MODE == 0 ? (unsigned)KID_TC_PASS2 : (unsigned)KID_TC_BWD_B1, wait_limit(status)};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(a_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int x = 0; x < 2; x++) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&w_full[x], 128);
+            mbar_init(&acc_done[x], 1);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_a1);
+            prefetch_tmap(&tm_a2);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(a_full, ntiles * 2 * C::AB);
+            for (int x = 0; x < ntiles; x++) {
+                const int qx = x ? q0b : q0a;
+#pragma unroll
+                for (int r = 0; r < D / 64; r++) {
+                    tma_load_3d(sA + (2 * x) * C::AB + r * C::BM * 128, &tm_a1, r * 64, qx, bh, a_full);
+                    tma_load_3d(sA + (2 * x + 1) * C::AB + r * C::BM * 128, &tm_a2, r * 64, qx, bh, a_full);
+                }
+            }
+            int issued = 0;
+            for (int j = 0; j < nk; j++) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&kv_full[s], 2 * C::KB);
+                uint8_t* st = sKV + s * 2 * C::KB;
+#pragma unroll
+                for (int r = 0; r < D / 64; r++) {
+                    tma_load_3d(st + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &kv_full[s]);
+                    tma_load_3d(st + C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &kv_full[s]);
+                }
+                issued = j + 1;
+            }
+            mbar_wait_drain(a_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        // The whole warp runs the issue loop (warp-uniform descriptors); the
+        // elected lane issues every tcgen05 instruction, in order.
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        const uint32_t idA = idesc_mma(128, D, false, true);
+        auto scores = [&](int x, int j) {  // S_x(j) = A1_x K_j^T, X_x(j) = A2_x (K or V)_j^T
+            const uint32_t kaddr = smem_u32(sKV + (j % NS) * 2 * C::KB);
+            const uint32_t xb = MODE == 0 ? kaddr : kaddr + C::KB;
+            const uint32_t a1 = smem_u32(sA + (2 * x) * C::AB), a2 = smem_u32(sA + (2 * x + 1) * C::AB);
+            const uint32_t tS = tmem + 256 * x, tX = tS + 64;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
+                mma_commit(&s_full[x]);
+            }
+            __syncwarp();
+        };
+        auto accumulate = [&](int x, int j) {  // Acc_x += W_x(j) (V or K)_j
+            const uint32_t kaddr = smem_u32(sKV + (j % NS) * 2 * C::KB);
+            const uint32_t ab = MODE == 0 ? kaddr + C::KB : kaddr;
+            const uint32_t tS = tmem + 256 * x, tAcc = tS + 128;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; kk++)
+                    mma_ts(tAcc, tS + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == (x ? nktb : nkta) - 1) mma_commit(&acc_done[x]);  // one phase: the epilogue's only wait
+            }
+            __syncwarp();
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2)) &&
+                  __all_sync(0xffffffffu, mbar_wait(&kv_full[0], 0, wd, 3));
+        if (ok) {
+            tc_fence_after();
+            scores(0, 0);
+            if (nktb > 0) scores(1, 0);
+        }
+        for (int j = 0; ok && j < nk; j++) {
+            // S_x(j + 1) aliases W_x(j): the accumulation that reads W_x(j)
+            // is issued first, and MMAs issued by one thread run in order
+            if (j < nkta) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&w_full[0], j & 1, wd, 5))) break;
+                tc_fence_after();
+                accumulate(0, j);
+            }
+            if (j + 1 < nk) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
+                tc_fence_after();
+                if (j + 1 < nkta) scores(0, j + 1);
+            }
+            if (j < nktb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&w_full[1], j & 1, wd, 6))) break;
+                tc_fence_after();
+                accumulate(1, j);
+            }
+            // every MMA that reads key tile j has been issued
+            if (elect_one()) mma_commit(&kv_empty[j % NS]);
+            __syncwarp();
+            if (j + 1 < nktb) scores(1, j + 1);
+        }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
+    } else {
+        const int x = (warp - 2) >> 2;  // query tile of this warpgroup
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int q0 = x ? q0b : q0a;
+        const int t = q0 + row;
+        const int my_nkt = x ? nktb : nkta;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        const uint32_t tS = tmem + 256 * x, tX = tS + 64, tAcc = tS + 128;
+        const bool valid = t < T;
+        const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
+        const float g1 = (MODE == 0 && valid) ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
+        const uint64_t SL2 = f2(scale_log2, scale_log2), NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+        uint64_t rs2 = f2(0.f, 0.f);  // row sum of the rounded weights, as an (even, odd) pair
+        bool ok = my_nkt > 0;
+        for (int j = 0; j < my_nkt; j++) {
+            ok = mbar_wait(&s_full[x], j & 1, wd, 7);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * C::BN;
+            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+            const bool need_mask = lim < C::BN;
+#pragma unroll
+            for (int c = 0; c < C::BN / 32; c++) {
+                uint32_t vs[32], vx[32];
+                tmem_ld32(tS + lrow + c * 32, vs);
+                tmem_ld32(tX + lrow + c * 32, vx);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
+                    const int cc = c * 32 + 2 * i;
+                    const float2 xs = uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])),
+                                                SL2, NL2));
+                    float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
+                    if (need_mask) {
+                        if (cc > lim) p0 = 0.f;
+                        if (cc + 1 > lim) p1 = 0.f;
+                    }
+                    const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
+                    const float2 w = uf2(MODE == 0 ? fmul2(f2(p0, p1), fadd2(xv, G1)) : fmul2(f2(p0, p1), xv));
+                    pk[i] = pack_f16(w.x, w.y);
+                    if (MODE == 1) rs2 = fadd2(rs2, f2(f16_lo(pk[i]), f16_hi(pk[i])));
+                }
+                tmem_st16(tS + lrow + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&w_full[x]);
+        }
+        if (ok) {
+            ok = mbar_wait(&acc_done[x], 0, wd, 8);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tAcc + lrow + c * 32, v);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const size_t off = ((size_t)bh * T + t) * D + c * 32;
+                        if (MODE == 0) {
+                            uint4* dst = (uint4*)((__nv_bfloat16*)acc_out + off);
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                dst[i] = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+                        } else {
+                            float* dst = (float*)acc_out + off;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        }
+                    }
+                }
+                if (MODE == 1 && valid) {
+                    const float2 r2 = uf2(rs2);
+                    ebar_out[(size_t)bh * T + t] = r2.x + r2.y;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 // ============================================================ given probe
 // The one-pass form with a probe rho supplied as input ("Parallax: Parameterized
 // Local Linear Attention for Language Modeling", technical summary, "Core
@@ -746,7 +1033,7 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
     const int qt = ntq - 1 - rank;
     const int q0 = qt * C::BM;
     const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
-    const Watchdog wd{status, abortf, KID_TC_PROBE};
+    const Watchdog wd{status, abortf, KID_TC_PROBE, wait_limit(status)};
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -852,15 +1139,25 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
             tc_fence_after();
             const int k0 = j * C::BN;
             const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;  // key k0 + c valid iff c <= lim
-            float mx = -INFINITY;
+            // the row's whole score tile in registers: one TMEM round trip
+            uint32_t v[C::BN];
 #pragma unroll
-            for (int c = 0; c < C::BN / 32; c++) {
-                uint32_t v[32];
-                tmem_ld32(tS + lrow + c * 32, v);
-                tmem_wait_ld();
+            for (int c = 0; c < C::BN / 32; c++) tmem_ld32(tS + lrow + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+            tmem_wait_ld();
+            if (lim < C::BN) {  // the diagonal tile only: masked keys score -inf (weight 0)
 #pragma unroll
-                for (int i = 0; i < 32; i++)
-                    if (c * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+                for (int i = 0; i < C::BN; i++)
+                    if (i > lim) v[i] = __float_as_uint(-INFINITY);
+            }
+            float mx;
+            {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < C::BN; i += 8)
+#pragma unroll
+                    for (int u = 0; u < 4; u++)
+                        m4[u] = fmax3(m4[u], __uint_as_float(v[i + 2 * u]), __uint_as_float(v[i + 2 * u + 1]));
+                mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
             }
             mx *= scale_log2;
             const float m_new = fmaxf(m_use, mx);
@@ -1296,7 +1593,7 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
     const int h = blockIdx.y;
     const int nrows = B * T;
     const int r_begin = blockIdx.x * C::BM * C::TILES, r_end = min(r_begin + C::BM * C::TILES, nrows);
-    const Watchdog wd{status, abortf, KID_TC_BWD_B2};
+    const Watchdog wd{status, abortf, KID_TC_BWD_B2, wait_limit(status)};
     if (tid == 0) {
         *abortf = 0;
         mbar_init(&bars[0], 1);
@@ -1616,7 +1913,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
     // sub-chunk j covers queries [k0 + 64 j, k0 + 64 j + 64); pairs j = 2m, 2m + 1
     // form the m-th 128-query tile of the dQ product
     const int nsub = (T - k0 + C::BQ - 1) / C::BQ;
-    const Watchdog wd{status, abortf, KID_TC_BWD_B3};
+    const Watchdog wd{status, abortf, KID_TC_BWD_B3, wait_limit(status)};
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -1865,7 +2162,7 @@ struct B3P {
     static constexpr int STAGE = 17 * 1024;        // stage stride (1024-aligned)
     static constexpr int DSB = BK * QT * 2;        // one ds tile, f16 [keys][128 queries]
     static constexpr int DQB = QT * D * 4;         // dQ staging: two 32-column boxes, 128-byte swizzle
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 4;
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 6;
     static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + DQB + NS * STAGE + NBAR * 8 + 16;
 };
 
@@ -1896,6 +2193,8 @@ __global__ void __launch_bounds__(B3P::NT, 1)
     uint64_t* dq_free = dq_full + 1;
     uint64_t* drain = dq_free + 1;
     uint64_t* fin = drain + 1;           // the last accumulation has completed (one phase)
+    uint64_t* st_free = fin + 1;         // dQ staging may be overwritten (warpgroup 1)
+    uint64_t* st_ready = st_free + 1;    // dQ staging is written (warpgroup 1)
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
@@ -1904,7 +2203,7 @@ __global__ void __launch_bounds__(B3P::NT, 1)
     work_item(blockIdx.x, BH, nkt, &kt, &bh);
     const int k0 = kt * C::BK;
     const int nsub = (T - k0 + C::BQ - 1) / C::BQ;  // sub-chunk j: queries [k0 + 32 j, k0 + 32 j + 32)
-    const Watchdog wd{status, abortf, KID_TC_BWD_B3};
+    const Watchdog wd{status, abortf, KID_TC_BWD_B3, wait_limit(status)};
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -1922,6 +2221,8 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         mbar_init(dq_free, 128);
         mbar_init(drain, 1);
         mbar_init(fin, 1);
+        mbar_init(st_free, 128);
+        mbar_init(st_ready, 128);
         fence_barrier_init();
     }
     // ds tiles start at zero: a tile cut by T leaves part unwritten, and the dQ
@@ -2050,13 +2351,19 @@ __global__ void __launch_bounds__(B3P::NT, 1)
         // dQ of the 128-query tile m (thread = query row i): staged in shared
         // memory and added into the fp32 accumulator by one tensor reduce-add
         // per 32-column box (rows past T are clipped by the tensor map).
+        // The warpgroup meets on two mbarriers (st_free, st_ready; one phase
+        // per call, parity = calls so far) rather than on a named barrier:
+        // their waits are bounded and see the abort flag, so a warp that
+        // left after a timed-out wait cannot strand the others.
+        int ndq = 0;
         auto read_dq = [&](int m) -> bool {
             const bool got = mbar_wait(dq_full, m & 1, wd, 9);
             if (!__all_sync(0xffffffffu, got)) return false;
             tc_fence_after();
             const bool leader = warp == 6 && lane == 0;
             if (leader) bulk_wait_read_all();  // the previous tile's reduce has read the staging
-            named_bar_sync(2, 128);
+            mbar_arrive(st_free);
+            if (!__all_sync(0xffffffffu, mbar_wait(st_free, ndq & 1, wd, 11))) return false;
 #pragma unroll 1
             for (int c = 0; c < D / 32; c++) {
                 uint32_t v[32];
@@ -2070,14 +2377,19 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             tc_fence_before();
             mbar_arrive(dq_free);
             fence_proxy_async_smem();
-            named_bar_sync(2, 128);
-            if (leader) {
+            mbar_arrive(st_ready);
+            bool done = true;
+            if (leader) {  // every thread's staging writes are visible to the reduce
+                done = mbar_wait(st_ready, ndq & 1, wd, 12);
+                if (done) {
 #pragma unroll
-                for (int c = 0; c < D / 32; c++)
-                    tma_reduce_add_3d(&tm_dq, 32 * c, k0 + m * C::QT, bh, sDQ + c * (C::QT * 128));
-                bulk_commit();
+                    for (int c = 0; c < D / 32; c++)
+                        tma_reduce_add_3d(&tm_dq, 32 * c, k0 + m * C::QT, bh, sDQ + c * (C::QT * 128));
+                    bulk_commit();
+                }
             }
-            return true;
+            ndq++;
+            return __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
         };
         bool ok = true;
         for (int j = wg; j < nsub && ok; j += 2) {
@@ -2326,7 +2638,17 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
-    {  // pass 2
+    if constexpr (D == 128) {  // pass 2: two query tiles per CTA sharing the K|V stages
+        using C = DualPP<D>;
+        const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
+        PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_pass2");
+        tc_dual_pp<D, 0><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, a.lse, w.gbar,
+                                                                     a.out, nullptr, a.T, BH, npairs, scale_log2,
+                                                                     a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    } else {  // pass 2
         using C = DualCfg<D>;
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
@@ -2359,7 +2681,17 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         __half* dst[4] = {w.q16, w.k16, w.v16, w.do16};
         PLX_TRY(to_f16(src, dst, 4, n, a.stream));
     }
-    {  // B1: R = sum p e k, ebar = sum p e
+    if constexpr (D == 128) {  // B1: R = sum p e k, ebar = sum p e (two query tiles per CTA)
+        using C = DualPP<D>;
+        const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
+        PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        timing_begin(a.stream, "tc_bwd_b1");
+        tc_dual_pp<D, 1><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr,
+                                                                     w.R, w.ebar, a.T, BH, npairs, scale_log2,
+                                                                     a.status);
+        timing_end(a.stream);
+        PLX_TRY(cudaGetLastError());
+    } else {  // B1: R = sum p e k, ebar = sum p e
         using C = DualCfg<D>;
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));

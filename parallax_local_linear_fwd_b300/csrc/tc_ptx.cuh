@@ -30,12 +30,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // and returns false; waits in other roles see the flag and return false too,
 // so every role leaves its loop and the CTA reaches its teardown.
 struct Watchdog {
-    unsigned* status;         // device word: [0] flag, [1] kid << 16 | site
+    unsigned* status;         // device word: [0] flag, [1] kid << 16 | site, [2] wait limit / 64
     volatile int* abort_flag; // shared memory
     unsigned kid;
+    unsigned limit64;         // clock64 cycles a watched wait may take, in units of 64
 };
 
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds at 2 GHz
+
+// The wait limit of the kernels launched with this status word, in units of
+// 64 cycles: its word [2] when set (> 0, written by the host), else
+// kWaitCycles.  Read once per thread at kernel start.
+__device__ __forceinline__ unsigned wait_limit(const unsigned* status) {
+    const unsigned v = *reinterpret_cast<const volatile unsigned*>(status + 2);
+    return v > 0 ? v : (unsigned)(kWaitCycles >> 6);
+}
 
 __device__ __forceinline__ void watchdog_fire(const Watchdog& w, unsigned site) {
     if (atomicCAS(w.status, 0u, 1u) == 0u) {
@@ -98,14 +107,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, const 
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > ((long long)w.limit64 << 6)) {
             watchdog_fire(w, site);
             return false;
         }
     }
 }
 
-// Bounded wait used only on the teardown path: no abort-flag check.
+// Bounded wait used only on the teardown path: no abort-flag check, and
+// always the long bound, so every copy and MMA in flight lands before the
+// CTA releases its shared memory and TMEM.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, unsigned parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))

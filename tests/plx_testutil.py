@@ -64,3 +64,29 @@ def sample_rows(B, H, T, n, seed=0):
     while len(rows) < n:
         rows.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(T))))
     return sorted(rows)
+
+
+# Guard bands: an output is a view into a larger buffer whose leading and
+# trailing GUARD elements hold a sentinel; a kernel that stores past either end
+# of its output (a row past T, a ragged tail) changes a sentinel.  The sentinel
+# is finite and exactly representable in bf16 and fp32, so a stray store of
+# NaN, inf or any ordinary value is caught.
+GUARD = 256
+SENTINEL = -12288.0
+
+
+def guarded_empty(shape, dtype, device="cuda"):
+    """(buffer, view): `view` has `shape`, starts 16-byte aligned, and is
+    surrounded by GUARD sentinel elements on each side; its own elements are
+    NaN until written."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), SENTINEL, dtype=dtype, device=device)
+    view = buf[GUARD:GUARD + n].view(shape)
+    view.fill_(float("nan"))
+    return buf, view
+
+
+def guards_intact(buf, shape) -> bool:
+    n = int(np.prod(shape))
+    band = torch.cat([buf[:GUARD], buf[GUARD + n:]])
+    return bool((band == SENTINEL).all())

@@ -1,10 +1,12 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
-Small cases are compared element by element on every output; the full-size
-workloads are compared on sampled rows (forward) and on a subset of heads
-(backward) that the oracle computes directly.  Tolerances are
-max |gpu - oracle| / RMS(oracle): 1e-4 for fp32, 2e-2 for bf16 outputs,
-3e-2 for bf16 gradients.
+Small cases are compared element by element on every output, with every
+output surrounded by guard bands that must come back untouched.  The
+full-size workloads are compared element by element on one complete head
+(every query row of it) plus rows sampled from every head (forward), and on
+all batches of one head (backward), which the oracle computes directly.
+Tolerances are max |gpu - oracle| / RMS(oracle): 1e-4 for fp32, 2e-2 for
+bf16 outputs, 3e-2 for bf16 gradients.
 """
 import numpy as np
 import pytest
@@ -13,8 +15,8 @@ import torch
 import oracle
 import parallax_local_linear_fwd_b300 as plx
 import plx_synth
-from plx_testutil import (TOL_BF16, TOL_BF16_GRAD, TOL_FP32, inputs_f64, rel_err, sample_rows,
-                          to_device, to_host64)
+from plx_testutil import (TOL_BF16, TOL_BF16_GRAD, TOL_FP32, guarded_empty, guards_intact, inputs_f64,
+                          rel_err, sample_rows, to_device, to_host64)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,11 +48,21 @@ def _use_path(name, dtype):
     plx.parallax_set_path(PATHS[name])
 
 
-def _run_fwd(inp):
+def _run_fwd(inp, guard=False):
     q, k, v, P = (to_device(inp[x]) for x in ("q", "k", "v", "P"))
-    out, lse, mu = plx.parallax_fwd(q, k, v, P)
+    if guard:
+        B, H, T, d = q.shape
+        shapes = {"out": ((B, H, T, d), q.dtype), "lse": ((B, H, T), torch.float32),
+                  "mu": ((B, H, T, d), torch.float32)}
+        g = {n: guarded_empty(sh, dt) for n, (sh, dt) in shapes.items()}
+        out, lse, mu = plx.parallax_fwd(q, k, v, P, out=g["out"][1], lse=g["lse"][1], mu_k=g["mu"][1])
+    else:
+        out, lse, mu = plx.parallax_fwd(q, k, v, P)
     code, detail = plx.parallax_last_device_error()
     assert code == plx.PLX_OK, (code, hex(detail))
+    if guard:
+        for n, (sh, _) in shapes.items():
+            assert guards_intact(g[n][0], sh), f"{n}: a store landed outside the tensor"
     return to_host64(out), to_host64(lse), to_host64(mu)
 
 
@@ -65,7 +77,9 @@ SMALL = [
     (2, 3, 77, 128, "fp32"),
     (1, 1, 1, 64, "bf16"),
     (1, 2, 7, 128, "bf16"),
+    (1, 2, 33, 64, "bf16"),
     (2, 2, 130, 64, "bf16"),
+    (1, 1, 257, 128, "bf16"),
     (1, 3, 300, 128, "bf16"),
     (2, 1, 513, 64, "bf16"),
 ]
@@ -78,11 +92,35 @@ def test_forward_small_full_compare(path, B, H, T, d, dtype):
     inp = plx_synth.generate(B, H, T, d, dtype, seed=T + d, p_std=0.3 / np.sqrt(d))
     f = inputs_f64(inp)
     ro, rl, rm = oracle.forward(f["q"], f["k"], f["v"], f["P"])
-    go, gl, gm = _run_fwd(inp)
+    go, gl, gm = _run_fwd(inp, guard=True)
     tol = _tol(dtype)
     assert rel_err(go, ro, dtype) < tol
     assert rel_err(gm, rm) < tol
     assert np.abs(gl - rl).max() < tol * max(1.0, np.sqrt(np.mean(rl * rl)))
+
+
+@pytest.mark.parametrize("path", ["simt", "tc"])
+@pytest.mark.parametrize("qk_scale,v_scale,p_scale,d", [(30.0, 100.0, 1.0, 64), (100.0, 1.0e4, 1.0e-4, 128)])
+def test_forward_large_magnitude_inputs(path, qk_scale, v_scale, p_scale, d):
+    # q, k and v far from unit scale but inside f16's range (|x| < 65504): the
+    # tensor-core path converts every operand to f16 exactly there.  In the
+    # second case P shrinks by 1/qk_scale^2, so that g = k . P (q - mu_k) keeps
+    # its usual size: with P unscaled, g reaches ~1e5 there, and the output
+    # then depends on P's last bits (f16 weights, relative 2^-11) -- a
+    # conditioning limit of the problem stated in the header, not a range one.
+    _use_path(path, "bf16")
+    B, H, T = 1, 2, 300
+    inp = plx_synth.generate(B, H, T, d, "bf16", seed=90 + d, p_std=0.3 / np.sqrt(d))
+    for name, sc in (("q", qk_scale), ("k", qk_scale), ("v", v_scale)):
+        inp[name] = plx_synth.to_bf16_bits(plx_synth.widen(inp[name]) * sc)
+    inp["P"] = (inp["P"].astype(np.float64) * p_scale).astype(np.float32)
+    assert np.abs(plx_synth.widen(inp["v"])).max() < 65504
+    f = inputs_f64(inp)
+    ro, rl, rm = oracle.forward(f["q"], f["k"], f["v"], f["P"])
+    go, gl, gm = _run_fwd(inp, guard=True)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert rel_err(gm, rm) < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, np.sqrt(np.mean(rl * rl)))
 
 
 @pytest.mark.parametrize("path", ["simt", "tc"])
@@ -106,29 +144,56 @@ def test_pr1_workload_and_zero_projector(path):
             assert rel_err(go, sd, dtype) < tol
 
 
-@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
-def test_forward_full_size_sampled_rows(name):
+# One complete head per full-size workload: (b, h) of the head compared over
+# every query row.
+FULL_HEAD = {"c2": (7, 5), "c3": (3, 15), "c4": (5, 9), "c5": (0, 11)}
+
+
+@pytest.mark.parametrize("name", ["c2", "c3", "c5", "c4"])
+def test_forward_full_size(name):
+    """The forward at full size, in the launch configuration the benchmark
+    times: one complete head element by element against the oracle, rows
+    sampled from every head, and at every row of every head the bound
+    lse_t >= c q_t . k_t (the log-sum-exp is at least its diagonal term)."""
     plx.parallax_set_path(plx.PLX_PATH_AUTO)
     inp = plx_synth.generate_workload(name)
     B, H, T, d = inp["B"], inp["H"], inp["T"], inp["d"]
     go, gl, gm = _run_fwd(inp)
-    rows = sample_rows(B, H, T, 48, seed=len(name))
     f = inputs_f64(inp)
+    b, h = FULL_HEAD[name]
+    rows = sorted(set(sample_rows(B, H, T, 48, seed=len(name))) | {(b, h, t) for t in range(T)})
     ro, rl, rm = oracle.forward_rows(f["q"], f["k"], f["v"], f["P"], rows)
     idx = tuple(np.array(rows).T)
     assert rel_err(go[idx], ro, "bf16") < TOL_BF16
     assert rel_err(gm[idx], rm) < TOL_BF16
     assert np.abs(gl[idx] - rl).max() < TOL_BF16 * max(1.0, np.sqrt(np.mean(rl * rl)))
+    head = np.array([r[0] == b and r[1] == h for r in rows])
+    assert head.sum() == T
+    assert rel_err(go[idx][head], ro[head], "bf16") < TOL_BF16
+    assert rel_err(gm[idx][head], rm[head]) < TOL_BF16
     # properties at every row: finite outputs, lse >= the diagonal score
     assert np.isfinite(go).all() and np.isfinite(gl).all() and np.isfinite(gm).all()
+    diag = np.einsum("bhtd,bhtd->bht", f["q"], f["k"]) / np.sqrt(d)
+    assert (gl >= diag - 1e-5 * np.maximum(1.0, np.abs(diag))).all()
 
 
-def _run_bwd(inp, out_dev=None):
+def _run_bwd(inp, guard=False):
     q, k, v, P, do = (to_device(inp[x]) for x in ("q", "k", "v", "P", "dout"))
     out, lse, mu = plx.parallax_fwd(q, k, v, P)
-    dq, dk, dv, dP = plx.parallax_bwd(q, k, v, P, lse, mu, do)
+    if guard:
+        B, H, T, d = q.shape
+        shapes = {"dq": ((B, H, T, d), q.dtype), "dk": ((B, H, T, d), q.dtype), "dv": ((B, H, T, d), q.dtype),
+                  "dP": ((H, d, d), torch.float32)}
+        g = {n: guarded_empty(sh, dt) for n, (sh, dt) in shapes.items()}
+        dq, dk, dv, dP = plx.parallax_bwd(q, k, v, P, lse, mu, do, dq=g["dq"][1], dk=g["dk"][1], dv=g["dv"][1],
+                                          dP=g["dP"][1])
+    else:
+        dq, dk, dv, dP = plx.parallax_bwd(q, k, v, P, lse, mu, do)
     code, detail = plx.parallax_last_device_error()
     assert code == plx.PLX_OK, (code, hex(detail))
+    if guard:
+        for n, (sh, _) in shapes.items():
+            assert guards_intact(g[n][0], sh), f"{n}: a store landed outside the tensor"
     return [to_host64(x) for x in (dq, dk, dv, dP)]
 
 
@@ -151,7 +216,7 @@ def test_backward_small_full_compare(path, B, H, T, d, dtype):
     inp = plx_synth.generate(B, H, T, d, dtype, seed=3 * T + d, p_std=0.3 / np.sqrt(d), backward=True)
     f = inputs_f64(inp)
     ref = oracle.backward(f["q"], f["k"], f["v"], f["P"], f["dout"])
-    got = _run_bwd(inp)
+    got = _run_bwd(inp, guard=True)
     tol = TOL_FP32 if dtype == "fp32" else TOL_BF16_GRAD
     for name, g, r in zip(("dq", "dk", "dv", "dP"), got, ref):
         assert rel_err(g, r, dtype if name != "dP" else "fp32") < tol, name
