@@ -7,8 +7,8 @@
 // Layer ("Parallax: Parameterized Local Linear Attention for Language
 // Modeling", technical summary, "Core mechanism" and "Hardware-aware
 // algorithm"; probe u = P_h (q - mu_k)):
-//   pass 1 (tc_pass1) : S = c Q K^T on a key tile, online softmax, Mu += P~ K;
-//                       emits lse and mu_k = Mu / l.
+//   pass 1 (tc_pass1_pp): S = c Q K^T on a key tile, online softmax,
+//                       Mu += P~ K; emits lse and mu_k = Mu / l; then the
 //   projection        : u = P_h (q - mu_k) rounded to f16, gbar = mu_k . u.
 //   pass 2 (tc_dual)  : S = c Q K^T and G = U K^T on the SAME key tile in
 //                       shared memory (both branches read one KV stream);
@@ -17,9 +17,11 @@
 //   backward B1 (tc_dual, second mode): S = c Q K^T and E = dO V^T;
 //                       weights p e; R += W K and ebar = sum p e.
 //
-// Warp roles in every tensor-core kernel (192 threads): warp 0 issues TMA
-// loads, warp 1 owns TMEM and issues the MMAs (one thread), warps 2-5 move
-// scores between TMEM and registers (thread = query row) and write results.
+// Warp roles in the tensor-core kernels: warp 0 issues TMA loads, warp 1 owns
+// TMEM and issues the MMAs (one thread), and warpgroups of four warps move
+// scores between TMEM and registers (thread = query row) and write results:
+// one warpgroup per CTA in the one-tile kernels (192 threads), one per query
+// tile in the two-tile kernels (tc_pass1_pp, tc_dual_pp; 320 threads).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -103,19 +105,6 @@ __device__ __forceinline__ void work_item(int item, int BH, int ntiles, int* ran
     *bh = g * kHeadGroup + r % gsize;
 }
 
-// ================================================================ pass 1
-template <int D>
-struct P1 {
-    static constexpr int BM = 128, BN = 128;
-    static constexpr int NS = D == 64 ? 4 : 2;  // K-tile stages
-    static constexpr int QB = BM * D * 2;
-    static constexpr int KB = BN * D * 2;
-    static constexpr int NBAR = 1 + 2 * NS + 6;
-    static constexpr int SMEM = 1024 + QB + NS * KB + NBAR * 8 + 16;
-    static constexpr unsigned TMEM_COLS = 256;  // S [0,128) (P~ f16 aliases [0,64)), Mu [128, 128+D)
-    static_assert(NS >= 2 && KB == QB, "the projection reuses two K stages for delta_hi / delta_lo");
-};
-
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -140,36 +129,69 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
     return (uint32_t)((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
 }
 
+// ======================================================= pass 1, two query tiles
+// Pass 1 with one CTA per SM holding two adjacent query
+// tiles, a = 2m and b = 2m + 1, which read the same key tiles (b one more):
+// every K tile is loaded once for both, and warpgroup 0 (warps 2-5) runs
+// tile a's softmax while warpgroup 1 (warps 6-9) runs tile b's, so the
+// tensor core works on one tile while the other's weights are formed.  The
+// MMA thread issues, per key tile j:
+//   Mu_a += P~_a(j) K,  S_a(j+1),  Mu_b += P~_b(j) K,  S_b(j+1)
+// The projection U = delta P_h^T of both tiles runs once every key MMA is
+// done: delta_a (hi, lo) goes to K stages 0, 1 and delta_b to stages 2, 3,
+// and P_h (f16, one head, both tiles) replaces tile a's Q tile.
+// TMEM: tile x at column 256 x: S [0,128) (P~ aliases [0,64); U after the
+// loop), Mu [128, 128 + D).
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 2)
-    tc_pass1(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ mu_k, __half* __restrict__ U,
-             float* __restrict__ gbar, int T, int H, int BH, int ntq, float scale_log2, unsigned* status) {
-    using C = P1<D>;
+struct P1PP {
+    static constexpr int BM = 128, BN = 128, NT = 320;
+    static constexpr int NS = D == 64 ? 6 : 4;  // K stages, shared by both tiles
+    static constexpr int QB = BM * D * 2;
+    static constexpr int KB = BN * D * 2;
+    // q_full, k_full[NS], k_empty[NS], s_full[2], p_full[2], o_done[2],
+    // kfree, proj_ready[2], proj_done[2], drain
+    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 1 + 2 + 2 + 1;
+    static constexpr int SMEM = 1024 + 2 * QB + NS * KB + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 512;
+    static_assert(NS >= 4 && KB == QB, "the projection of each tile takes two K stages");
+    static_assert(SMEM <= 232448, "one CTA per SM must fit");
+};
+
+template <int D>
+__global__ void __launch_bounds__(P1PP<D>::NT, 1)
+    tc_pass1_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ mu_k,
+                __half* __restrict__ U, float* __restrict__ gbar, int T, int H, int BH, int npairs,
+                float scale_log2, unsigned* status) {
+    using C = P1PP<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    uint8_t* sQ = sm;
-    uint8_t* sK = sQ + C::QB;
+    uint8_t* sQ = sm;                // tile x at x QB
+    uint8_t* sK = sQ + 2 * C::QB;    // stage s at s KB
     uint64_t* bars = (uint64_t*)(sK + NS * C::KB);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = bars + 1 + NS;
-    uint64_t* s_full = bars + 1 + 2 * NS;
-    uint64_t* p_full = s_full + 1;
-    uint64_t* o_done = s_full + 2;
-    uint64_t* drain = s_full + 3;
-    uint64_t* proj_ready = s_full + 4;  // delta_hi/lo and P_h (f16) staged for U = delta P_h^T
-    uint64_t* proj_done = s_full + 5;   // U is in TMEM
+    uint64_t* k_empty = k_full + NS;
+    uint64_t* s_full = k_empty + NS;     // [2]
+    uint64_t* p_full = s_full + 2;       // [2]
+    uint64_t* o_done = p_full + 2;       // [2]
+    uint64_t* kfree = o_done + 2;        // every MMA reading a K stage has completed (one phase)
+    uint64_t* proj_ready = kfree + 1;    // [2] delta_x and P_h staged
+    uint64_t* proj_done = proj_ready + 2;  // [2] U_x in TMEM
+    uint64_t* drain = proj_done + 2;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
-    work_item(blockIdx.x, BH, ntq, &rank, &bh);
-    const int qt = ntq - 1 - rank;  // longest rows first
-    const int q0 = qt * C::BM;
-    const int nkt = min(qt, (T - 1) / C::BN) + 1;
+    work_item(blockIdx.x, BH, npairs, &rank, &bh);
+    const int m = npairs - 1 - rank;  // longest pairs first
+    const int q0a = 2 * m * C::BM, q0b = q0a + C::BM;
+    const int nkta = min(q0a + C::BM - 1, T - 1) / C::BN + 1;
+    const int nktb = q0b < T ? min(q0b + C::BM - 1, T - 1) / C::BN + 1 : 0;
+    const int nk = nktb > nkta ? nktb : nkta;
+    const int ntiles = nktb > 0 ? 2 : 1;
     const Watchdog wd{status, abortf, KID_TC_PASS1, wait_limit(status)};
 
     if (threadIdx.x == 0) {
@@ -179,12 +201,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
+        for (int x = 0; x < 2; x++) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 128);
+            mbar_init(&o_done[x], 1);
+            mbar_init(&proj_ready[x], 128);
+            mbar_init(&proj_done[x], 1);
+        }
+        mbar_init(kfree, 1);
         mbar_init(drain, 1);
-        mbar_init(proj_ready, 128);
-        mbar_init(proj_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
@@ -192,17 +217,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
-    const uint32_t tS = tmem, tMu = tmem + 128;
 
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            mbar_expect_tx(q_full, C::QB);
+            mbar_expect_tx(q_full, ntiles * C::QB);
+            for (int x = 0; x < ntiles; x++) {
 #pragma unroll
-            for (int r = 0; r < D / 64; r++) tma_load_3d(sQ + r * C::BM * 128, &tm_q, r * 64, q0, bh, q_full);
+                for (int r = 0; r < D / 64; r++)
+                    tma_load_3d(sQ + x * C::QB + r * C::BM * 128, &tm_q, r * 64, x ? q0b : q0a, bh, q_full);
+            }
             int issued = 0;
-            for (int j = 0; j < nkt; j++) {
+            for (int j = 0; j < nk; j++) {
                 const int s = j % NS;
                 if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
                 mbar_expect_tx(&k_full[s], C::KB);
@@ -216,44 +243,76 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
         }
     } else if (warp == 1) {
-        // The whole warp runs the issue loop, so the descriptors stay
-        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
-        // every tcgen05 instruction, so one thread issues all MMAs, in order.
+        // The whole warp runs the issue loop (warp-uniform descriptors); the
+        // elected lane issues every tcgen05 instruction, in order.
         const uint32_t idS = idesc_mma(128, C::BN, false, false);
         const uint32_t idM = idesc_mma(128, D, false, true);
-        const uint32_t qaddr = smem_u32(sQ);
-        if (__all_sync(0xffffffffu, mbar_wait(q_full, 0, wd, 2))) {
-            for (int j = 0; j < nkt; j++) {
-                const int s = j % NS;
-                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[s], (j / NS) & 1, wd, 3))) break;
-                // S aliases the previous tile's P~; tcgen05.mma ops issued by one
-                // thread execute in issue order, so no wait for that MMA here.
-                tc_fence_after();
-                const uint32_t kaddr = smem_u32(sK + s * C::KB);
-                if (elect_one()) {
+        auto scores = [&](int x, int j) {  // S_x(j) = Q_x K_j^T
+            const uint32_t qaddr = smem_u32(sQ + x * C::QB), kaddr = smem_u32(sK + (j % NS) * C::KB);
+            const uint32_t tS = tmem + 256 * x;
+            if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++)
-                        mma_ss(tS, desc_kmajor(qaddr, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
-                    mma_commit(s_full);
-                }
-                __syncwarp();
-                if (!__all_sync(0xffffffffu, mbar_wait(p_full, j & 1, wd, 5))) break;
-                tc_fence_after();
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; kk++)
-                        mma_ts(tMu, tS + kk * 8, desc_mnmajor(kaddr, C::BN, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(o_done);
-                    mma_commit(&k_empty[s]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tS, desc_kmajor(qaddr, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                mma_commit(&s_full[x]);
             }
-            // projection U = delta P_h^T (delta = delta_hi + delta_lo, P_h in f16):
-            // M = 128 rows, N = D, K = D, into the S columns
-            if (__all_sync(0xffffffffu, mbar_wait(proj_ready, 0, wd, 9))) {
+            __syncwarp();
+        };
+        auto accumulate = [&](int x, int j) {  // Mu_x += P~_x(j) K_j (K read MN-major)
+            const uint32_t kaddr = smem_u32(sK + (j % NS) * C::KB);
+            const uint32_t tS = tmem + 256 * x, tMu = tS + 128;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; kk++)
+                    mma_ts(tMu, tS + kk * 8, desc_mnmajor(kaddr, C::BN, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&o_done[x]);
+            }
+            __syncwarp();
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, wd, 2)) &&
+                  __all_sync(0xffffffffu, mbar_wait(&k_full[0], 0, wd, 3));
+        if (ok) {
+            tc_fence_after();
+            scores(0, 0);
+            if (nktb > 0) scores(1, 0);
+        }
+        for (int j = 0; ok && j < nk; j++) {
+            // S_x(j + 1) aliases P~_x(j): the accumulation reading it is issued
+            // first, and MMAs issued by one thread run in order
+            if (j < nkta) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&p_full[0], j & 1, wd, 5)))) break;
                 tc_fence_after();
-                const uint32_t idP = idesc_mma(128, D, false, false);
-                const uint32_t dhi = smem_u32(sK), dlo = smem_u32(sK + C::KB), pb = smem_u32(sQ);
+                accumulate(0, j);
+            }
+            if (j + 1 < nk) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&k_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))))
+                    break;
+                tc_fence_after();
+                if (j + 1 < nkta) scores(0, j + 1);
+            }
+            if (j < nktb) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&p_full[1], j & 1, wd, 6)))) break;
+                tc_fence_after();
+                accumulate(1, j);
+            }
+            if (elect_one()) mma_commit(&k_empty[j % NS]);  // every MMA reading key tile j is issued
+            __syncwarp();
+            if (j + 1 < nktb) scores(1, j + 1);
+        }
+        if (ok) {
+            if (elect_one()) mma_commit(kfree);
+            __syncwarp();
+            // projections U_x = delta_x P_h^T (delta = hi + lo, P_h in f16 in tile
+            // a's Q slot): M = 128 rows, N = D, K = D, into S_x's columns
+            const uint32_t idP = idesc_mma(128, D, false, false);
+            const uint32_t pb = smem_u32(sQ);
+            for (int x = 0; x < ntiles; x++) {
+                // U_b's B operand is written by warpgroup 0: wait for both
+                if (!__all_sync(0xffffffffu, mbar_wait(&proj_ready[0], 0, wd, 9))) break;
+                if (x == 1 && !__all_sync(0xffffffffu, mbar_wait(&proj_ready[1], 0, wd, 10))) break;
+                tc_fence_after();
+                const uint32_t dhi = smem_u32(sK + (2 * x) * C::KB), dlo = smem_u32(sK + (2 * x + 1) * C::KB);
+                const uint32_t tS = tmem + 256 * x;
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
@@ -261,7 +320,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tS, desc_kmajor(dlo, C::BM, kk), desc_kmajor(pb, D, kk), idP, 1u);
-                    mma_commit(proj_done);
+                    mma_commit(&proj_done[x]);
                 }
                 __syncwarp();
             }
@@ -270,15 +329,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
         mbar_wait_drain(drain, 0);
     } else {
-        // softmax / epilogue warps: thread <-> query row (TMEM lane)
+        // softmax / epilogue warpgroup x: thread <-> query row (TMEM lane)
+        const int x = (warp - 2) >> 2;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
+        const int q0 = x ? q0b : q0a;
         const int t = q0 + row;
+        const int my_nkt = x ? nktb : nkta;
         const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        const uint32_t tS = tmem + 256 * x, tMu = tS + 128;
+        uint8_t* sQx = sQ + x * C::QB;
         float m_use = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nkt; j++) {
-            ok = mbar_wait(s_full, j & 1, wd, 6);
+        bool ok = my_nkt > 0;
+        for (int j = 0; j < my_nkt; j++) {
+            ok = mbar_wait(&s_full[x], j & 1, wd, 6);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
@@ -323,8 +387,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
                 for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1: one f32x2 op each (2^-inf = 0)
                     const uint32_t* vv = v + c * 32 + 2 * i;
-                    const float2 x = uf2(ffma2(f2(__uint_as_float(vv[0]), __uint_as_float(vv[1])), SL2, NM2));
-                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    const float2 xx = uf2(ffma2(f2(__uint_as_float(vv[0]), __uint_as_float(vv[1])), SL2, NM2));
+                    const float p0 = fast_exp2(xx.x), p1 = fast_exp2(xx.y);
                     sum2 = fadd2(sum2, f2(p0, p1));
                     pk[i] = pack_f16(p0, p1);
                 }
@@ -332,11 +396,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
             const float2 sp = uf2(sum2);
             l += sp.x + sp.y;
-            // rescale the accumulator to the moved maximum once the previous
-            // tile's P~ K has landed, before this tile's is issued (the score
-            // row is dead by now, which keeps the registers for it)
+            // rescale the accumulator to the moved maximum; the previous tile's
+            // P~ K has completed (this tile's scores were issued after it)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                ok = mbar_wait(o_done, (j - 1) & 1, wd, 7);
+                ok = mbar_wait(&o_done[x], (j - 1) & 1, wd, 7);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     tmem_wait_st();
@@ -355,26 +418,30 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[x]);
         }
-        if (ok) ok = mbar_wait(o_done, (nkt - 1) & 1, wd, 8);
-        // The four epilogue warps agree on ok before the projection (whose
-        // steps synchronise on a named barrier): an abort anywhere skips it.
-        ok = named_bar_and(1, 128, ok);
+        // the last P~ K of this tile, then every MMA that reads a K stage
+        if (ok) ok = mbar_wait(&o_done[x], (my_nkt - 1) & 1, wd, 8);
+        if (ok) ok = mbar_wait(kfree, 0, wd, 11);
+        // The four warps agree on ok before the projection (whose steps
+        // synchronise on a named barrier): an abort anywhere skips it.
+        ok = named_bar_and(1 + x, 128, ok);
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
             const size_t grow = (size_t)bh * T + t;
+            uint8_t* sDhi = sK + (2 * x) * C::KB;
+            uint8_t* sDlo = sK + (2 * x + 1) * C::KB;
             // mu_k = Mu / l (output), delta = q - mu_k split into f16 hi + lo,
-            // written as the K-major A tile of the projection into K stages 0, 1
+            // written as the K-major A tile of the projection
 #pragma unroll 1
             for (int c = 0; c < D / 32; c++) {
-                uint32_t v[32];
-                tmem_ld32(tMu + lrow + c * 32, v);
+                uint32_t u[32];
+                tmem_ld32(tMu + lrow + c * 32, u);
                 tmem_wait_ld();
                 float mu[32];
 #pragma unroll
-                for (int i = 0; i < 32; i++) mu[i] = __uint_as_float(v[i]) * inv;
+                for (int i = 0; i < 32; i++) mu[i] = __uint_as_float(u[i]) * inv;
                 if (t < T) {
                     float* dst = mu_k + grow * D + c * 32;
 #pragma unroll
@@ -383,37 +450,39 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
                 for (int g = 0; g < 4; g++) {
                     const uint32_t off = sw_off(row, c * 32 + g * 8, C::BM);
-                    const uint4 qv = *(const uint4*)(sQ + off);
+                    const uint4 qv = *(const uint4*)(sQx + off);
                     const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
                     uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int x = 0; x < 4; x++) {
-                        const float d0 = f16_lo(qw[x]) - mu[g * 8 + 2 * x];
-                        const float d1 = f16_hi(qw[x]) - mu[g * 8 + 2 * x + 1];
-                        hi[x] = pack_f16(d0, d1);
-                        lo[x] = pack_f16(d0 - f16_lo(hi[x]), d1 - f16_hi(hi[x]));
+                    for (int e = 0; e < 4; e++) {
+                        const float d0 = f16_lo(qw[e]) - mu[g * 8 + 2 * e];
+                        const float d1 = f16_hi(qw[e]) - mu[g * 8 + 2 * e + 1];
+                        hi[e] = pack_f16(d0, d1);
+                        lo[e] = pack_f16(d0 - f16_lo(hi[e]), d1 - f16_hi(hi[e]));
                     }
-                    *(uint4*)(sK + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *(uint4*)(sK + C::KB + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *(uint4*)(sDhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *(uint4*)(sDlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
-            // every thread has read its q row: P_h (f16) replaces the Q tile as
-            // the K-major B operand (rows = output index a, K = input index b)
-            named_bar_sync(1, 128);
-            const float* Ph = P + (size_t)(bh % H) * D * D;
-            const int et = (warp - 2) * 32 + lane;  // 0..127
+            if (x == 0) {
+                // every thread of warpgroup 0 has read its q row: P_h (f16)
+                // replaces tile a's Q tile as the K-major B operand of both
+                // projections (rows = output index a, K = input index b)
+                named_bar_sync(1, 128);
+                const float* Ph = P + (size_t)(bh % H) * D * D;
 #pragma unroll 1
-            for (int id = et; id < D * D / 8; id += 128) {
-                const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
-                const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
-                const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
-                *(uint4*)(sQ + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
-                                                                pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
+                for (int id = row; id < D * D / 8; id += 128) {
+                    const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
+                    const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
+                    const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
+                    *(uint4*)(sQ + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
+                                                                    pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(proj_ready);
-            ok = mbar_wait(proj_done, 0, wd, 10);
+            mbar_arrive(&proj_ready[x]);
+            ok = mbar_wait(&proj_done[x], 0, wd, 12);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 float g = 0.f;
@@ -2628,13 +2697,13 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         __half* dst[3] = {w.q16, w.k16, w.v16};
         PLX_TRY(to_f16(src, dst, 3, n, a.stream));
     }
-    {  // pass 1 (with the projection in its epilogue)
-        using C = P1<D>;
-        const int ntq = (a.T + C::BM - 1) / C::BM;
-        PLX_TRY(cudaFuncSetAttribute(tc_pass1<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    {  // pass 1: two query tiles per CTA, projection after the key loop
+        using C = P1PP<D>;
+        const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
+        PLX_TRY(cudaFuncSetAttribute(tc_pass1_pp<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass1");
-        tc_pass1<D><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mk128, a.P, a.lse, a.mu_k, w.U, w.gbar, a.T,
-                                                                a.H, BH, ntq, scale_log2, a.status);
+        tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mk128, a.P, a.lse, a.mu_k, w.U, w.gbar,
+                                                                   a.T, a.H, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
