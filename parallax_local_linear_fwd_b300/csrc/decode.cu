@@ -729,13 +729,13 @@ size_t decode_ws_bytes(int B, int H, int Lmax, int d) {
     const size_t BH = (size_t)B * H, nsplit = ((size_t)Lmax + DC - 1) / DC;
     const size_t simt = align256(BH * nsplit * (d + 2) * 4) + align256(BH * (d + 2) * 4) +
                         align256(BH * nsplit * d * 4);
-    const size_t stream = d == 64 ? dec2_ws_bytes<64>(BH, Lmax) : dec2_ws_bytes<128>(BH, Lmax);
-    return simt > stream ? simt : stream;
+    const size_t onepass = decode_tc_ws_bytes(B, H, Lmax, d);
+    return simt > onepass ? simt : onepass;
 }
 
 cudaError_t decode(const DecodeArgs& a) {
     if (a.dtype == 0) return a.d == 64 ? decode_impl<float, 64>(a) : decode_impl<float, 128>(a);
-    return a.d == 64 ? decode2_impl<64>(a) : decode2_impl<128>(a);
+    return decode_tc(a);
 }
 
 }  // namespace plx

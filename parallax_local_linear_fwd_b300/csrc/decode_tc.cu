@@ -1,0 +1,557 @@
+// Decode, bf16 caches: one pass over the keys and values.
+//
+// The layer at one new query per (sequence, head) ("Parallax: Parameterized
+// Local Linear Attention for Language Modeling", technical summary, "Core
+// mechanism"; the paper's own kernel is a decode kernel that runs both
+// branches over one KV stream, "Hardware-aware algorithm"):
+//   p_i = softmax(c q.k_i),  mu_k = sum p_i k_i,  mu_v = sum p_i v_i,
+//   u = P_h (q - mu_k),  gbar = mu_k . u,
+//   o = sum_i p_i (1 + k_i.u - gbar) v_i = mu_v + M u - gbar mu_v,
+//   M = sum_i p_i v_i k_i^T   (d x d).
+// u needs mu_k, which needs every key, so the weights p (1 + k.u - gbar)
+// cannot be formed in the same pass as the softmax.  M can: it does not
+// depend on u.  So each CTA streams its chunk of keys once and keeps, with
+// an online softmax, l = sum p, sum p k, sum p v (registers) and
+// M = V^T diag(p) K (a tcgen05 MMA into TMEM, d x d per chunk: 2 d^2 flops
+// per key, far below the tensor rate, while the stream is HBM-bound).  A
+// second kernel merges the chunks of a head by their log-sum-exp and forms
+// u, gbar and o.  Keys and values are read once.
+//
+//   dec1_chunk<D> : grid (chunks, B H), 128 threads (TPK = D/32 threads per
+//                   key, 32 features each), three CTAs per SM.  K and V tiles
+//                   of KT = 128 / TPK keys (8 KB each) arrive by TMA (128-byte
+//                   swizzle) in NS = 4 stages; thread 0 refills each stage two
+//                   tiles after its MMA was issued, so its wait is short.
+//                   Per tile: scores, tile max (lazy rescale by 2^8), p, the
+//                   register sums, then p k and v are written back in place
+//                   as f16 and one thread issues M += V^T (p K) (A = V^T read
+//                   MN-major; at d = 64 its second 64-row block is a zero
+//                   tile, so M = 128 rows of which the first 64 are used).
+//   dec1_merge<D> : grid (B H).  m = max m_c, w_c = 2^(m_c - m), then the
+//                   merged sums, u = P_h (q - mu_k), gbar, o and lse.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "plx_internal.h"
+#include "tc_ptx.cuh"
+
+namespace plx {
+namespace {
+
+using namespace tc;
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float RESCALE_TH = 8.f;  // log2 units: p~ <= 2^8 between rescales
+
+__device__ __forceinline__ float fast_exp2_dec(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// bar.red.and over the worker warps (barrier 1): every worker gets the AND
+// of everyone's predicate, so all take the same branch after a wait.
+__device__ __forceinline__ bool workers_and(bool pred, int nthreads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+template <int D>
+struct Dec1 {
+    static constexpr int TPK = D / 32;       // threads per key (32 features each)
+    static constexpr int KT = 128 / TPK;     // keys per tile: 64 (d 64) or 32 (d 128)
+    static constexpr int NW = 4;             // warps: 128 threads, KT keys x TPK
+    static constexpr int NT = 32 * NW;
+    static constexpr int MIN_CTAS = 3;       // resident CTAs per SM
+    static constexpr int NS = 4;             // K|V stages
+    static constexpr int TB = KT * D * 2;    // one K or V tile (bf16 / f16): 8 KB
+    static constexpr int ZB = D == 64 ? TB : 0;  // zero tile: rows 64..127 of A at d = 64
+    static constexpr int NBAR = 2 * NS + 2;  // full[NS], empty[NS], mma_done, drain
+    static constexpr int QS = 33;            // stride of q's 32-feature parts in shared memory
+    static constexpr int SMEM = 1024 + NS * 2 * TB + ZB + NBAR * 8 + 16 + 8 * 4 + TPK * QS * 4 + 16;
+    static_assert(KT * TPK == NW * 32, "one thread per (key, feature part)");
+    static_assert(MIN_CTAS * (SMEM + 1024) <= 233472, "MIN_CTAS CTAs fit an SM's shared memory");
+    static constexpr unsigned TMEM_COLS = D;
+    // partial of one chunk: {m, l, pad[2]}, sum p k [D], sum p v [D], M [D][D]
+    static constexpr int PART = 4 + 2 * D + D * D;
+};
+
+__device__ __forceinline__ int seq_len1(const int* lens, int b, int Lmax) {
+    return lens ? min(max(lens[b], 1), Lmax) : Lmax;
+}
+
+__device__ __forceinline__ uint32_t swz(int r, int c, int rows) {  // 16-bit tile, 64-column blocks
+    return (uint32_t)((c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void workers_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(const __grid_constant__ CUtensorMap tm_k,
+                                                           const __grid_constant__ CUtensorMap tm_v,
+                                                           const __nv_bfloat16* __restrict__ q,
+                                                           const int* __restrict__ lens, int H, int Lmax,
+                                                           int chunk, float scale_log2, float* __restrict__ part,
+                                                           unsigned* status) {
+    // (q, lens, the caches and part are device pointers; status is the
+    // device watchdog word of the calling device)
+    using C = Dec1<D>;
+    constexpr int NS = C::NS, KT = C::KT, TPK = C::TPK, NW = C::NW;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sKV = sm;                       // stage s: K at 2 s TB, V at (2 s + 1) TB
+    uint8_t* sZ = sKV + NS * 2 * C::TB;      // d = 64: zero tile (rows 64..127 of the A operand)
+    uint64_t* bars = (uint64_t*)(sZ + C::ZB);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + NS;
+    uint64_t* mma_done = bars + 2 * NS;
+    uint64_t* drain = mma_done + 1;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+    float* wmax = (float*)(holder + 4);      // [NW] tile maxima per worker warp
+    float* sq = wmax + 8;                    // [D] the query, fp32
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, b = bh / H;
+    const int len = seq_len1(lens, b, Lmax);
+    const int k_begin = blockIdx.x * chunk;
+    const int k_end = min(k_begin + chunk, len);
+    if (k_begin >= k_end) return;  // no keys of this sequence in this chunk (uniform per CTA)
+    const int nt = (k_end - k_begin + KT - 1) / KT;
+    const Watchdog wd{status, abortf, KID_DECODE, wait_limit(status)};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(mma_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (C::ZB) {
+        for (int i = threadIdx.x; i < C::ZB / 16; i += C::NT) ((uint4*)sZ)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tM = *holder;
+
+    // loads of tile j into stage j % NS (rows past Lmax read as zero)
+    auto load_tile = [&](int j) {
+        const int s = j % NS;
+        mbar_expect_tx(&full[s], 2 * C::TB);
+#pragma unroll
+        for (int r = 0; r < D / 64; r++) {
+            tma_load_3d(sKV + (2 * s) * C::TB + r * KT * 128, &tm_k, r * 64, k_begin + j * KT, bh, &full[s]);
+            tma_load_3d(sKV + (2 * s + 1) * C::TB + r * KT * 128, &tm_v, r * 64, k_begin + j * KT, bh, &full[s]);
+        }
+    };
+    int issued = 0;  // thread 0: tiles whose loads are issued
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        for (; issued < 2 && issued < nt; issued++) load_tile(issued);
+    }
+    {
+        // workers: lane = fp * KW + kl, thread = (key r = warp KW + kl of the
+        // tile, feature part fp); eight lanes of one part read eight keys'
+        // rows, which the swizzle spreads over all banks
+        constexpr int KW = 32 / TPK;  // keys per warp
+        const int kl = lane % KW, fp = lane / KW;
+        const int r = warp * KW + kl;
+        const int f0 = fp * 32;  // features [f0, f0 + 32)
+        // q in shared memory as fp32 (threads of one feature part read the
+        // same words: broadcasts), which keeps 32 registers free
+        // (part fp at fp * QS: the parts' words fall in different banks)
+        for (int i = threadIdx.x; i < D; i += NW * 32) sq[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(q[(size_t)bh * D + i]);
+        workers_sync(NW * 32);
+        const float* qf = sq + fp * C::QS;
+        float ak[32], av[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) ak[i] = av[i] = 0.f;
+        float l = 0.f, m_run = -INFINITY;
+        const uint32_t idM = idesc_mma(128, D, true, true);
+        bool ok = true;
+        for (int j = 0; j < nt; j++) {
+            const int s = j % NS;
+            // refill: tile j + 2 into the stage of tile j - 2 (NS = 4), whose MMA
+            // was issued two tiles ago, so the wait is short; tiles j, j + 1
+            // and j + 2 are then loaded or in flight
+            static_assert(NS == 4, "the refill distance assumes four stages");
+            if (threadIdx.x == 0 && ok && issued < nt && issued == j + 2) {
+                if (j < 2 || mbar_wait(&empty[(j - 2) % NS], ((j - 2) / NS) & 1, wd, 1)) {
+                    load_tile(issued);
+                    issued++;
+                } else {
+                    ok = false;
+                }
+            }
+            ok = mbar_wait(&full[s], (j / NS) & 1, wd, 2) && ok;
+            // every worker takes the same decisions below: agree on ok first
+            if (!__all_sync(0xffffffffu, ok)) ok = false;
+            uint8_t* sk = sKV + (2 * s) * C::TB;
+            uint8_t* sv = sKV + (2 * s + 1) * C::TB;
+            const int key = k_begin + j * KT + r;
+            const bool valid = key < k_end;
+            // scores: this thread's 32 features of key r, summed over the TPK threads of the key
+            uint4 kc[4];
+            float dp[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                kc[c] = *(const uint4*)(sk + swz(r, f0 + 8 * c, KT));
+                const uint32_t w[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    dp[c] = fmaf(qf[8 * c + 2 * e], bf16_lo(w[e]), dp[c]);
+                    dp[c] = fmaf(qf[8 * c + 2 * e + 1], bf16_hi(w[e]), dp[c]);
+                }
+            }
+            float dot = (dp[0] + dp[1]) + (dp[2] + dp[3]);
+#pragma unroll
+            for (int o = KW; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float sc = valid ? dot * scale_log2 : -INFINITY;
+            float tmax = sc;
+#pragma unroll
+            for (int o = 1; o < KW; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            if (lane == 0) wmax[warp] = tmax;
+            // the abort decision rides on the same barrier
+            if (!workers_and(ok, NW * 32)) {
+                ok = false;
+                break;
+            }
+            float tm = wmax[0];
+#pragma unroll
+            for (int w = 1; w < NW; w++) tm = fmaxf(tm, wmax[w]);
+            const float m_new = fmaxf(m_run, tm);
+            float alpha = 1.f;
+            if (m_new > m_run + RESCALE_TH) {  // uniform across the CTA
+                alpha = fast_exp2_dec(m_run - m_new);
+                m_run = m_new;
+                l *= alpha;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    ak[i] *= alpha;
+                    av[i] *= alpha;
+                }
+                if (j > 0) {
+                    // M *= alpha once the previous tile's MMA has landed (warps 0-3
+                    // own TMEM lanes 0-127, thread = row of M)
+                    const bool got = mbar_wait(mma_done, (j - 1) & 1, wd, 3);
+                    ok = ok && got;  // agreed on at the next tile's barrier
+                    if (warp < 4 && __all_sync(0xffffffffu, got)) {
+                        tc_fence_after();
+                        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; c++) {
+                            uint32_t u[32];
+                            tmem_ld32(tM + lrow + c * 32, u);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; i++) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            tmem_st32(tM + lrow + c * 32, u);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                }
+            }
+            const float p = valid ? fast_exp2_dec(sc - m_run) : 0.f;
+            if (fp == 0) l += p;
+            // p k and v in f16, written back in place; the register sums
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const uint32_t off = swz(r, f0 + 8 * c, KT);
+                const uint4 vc = *(const uint4*)(sv + off);
+                const uint32_t kw[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
+                const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
+                uint32_t ko[4], vo[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+                    const float v0 = valid ? bf16_lo(vw[e]) : 0.f, v1 = valid ? bf16_hi(vw[e]) : 0.f;
+                    const float pk0 = valid ? p * k0 : 0.f, pk1 = valid ? p * k1 : 0.f;
+                    ak[8 * c + 2 * e] += pk0;
+                    ak[8 * c + 2 * e + 1] += pk1;
+                    av[8 * c + 2 * e] = fmaf(p, v0, av[8 * c + 2 * e]);
+                    av[8 * c + 2 * e + 1] = fmaf(p, v1, av[8 * c + 2 * e + 1]);
+                    ko[e] = pack_f16(pk0, pk1);
+                    vo[e] = pack_f16_sat(v0, v1);
+                }
+                *(uint4*)(sk + off) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+                *(uint4*)(sv + off) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+            }
+            fence_proxy_async_smem();
+            workers_sync(NW * 32);
+            if (warp == 0) {
+                // M += V^T (p K): A = V^T (MN-major: features contiguous), B = p K
+                // (MN-major), K dimension = the tile's 64 keys in steps of 16
+                tc_fence_after();
+                const uint32_t va = smem_u32(sv), kb = smem_u32(sk);
+                const uint32_t lboA = D == 64 ? (uint32_t)(smem_u32(sZ) - va) : (uint32_t)(KT * 128);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < KT / 16; kk++)
+                        mma_ss(tM, desc_mn_lbo(va, kk, lboA), desc_mnmajor(kb, KT, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                    mma_commit(mma_done);
+                }
+                __syncwarp();
+            }
+        }
+        // loads issued but not consumed (only after an abort) land before
+        // stage 0 is reused below and before the CTA exits
+        if (threadIdx.x == 0)
+            for (int jj = issued > NS ? issued - NS : 0; jj < issued; jj++) mbar_wait_drain(&full[jj % NS], (jj / NS) & 1);
+        // ---- the chunk's partial (every worker agrees whether it is valid)
+        ok = workers_and(ok, NW * 32);
+        float* dst = part + ((size_t)bh * gridDim.x + blockIdx.x) * C::PART;
+        // l, sum p k, sum p v: reduce over the keys (lanes of one feature part
+        // first, then the worker warps through shared memory, reusing stage 0)
+#pragma unroll
+        for (int o = 1; o < KW; o <<= 1) {
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], o);
+                av[i] += __shfl_xor_sync(0xffffffffu, av[i], o);
+            }
+        }
+        // every tile's MMA must be done before stage 0 is reused below
+        if (warp == 0) {
+            if (elect_one()) mma_commit(drain);
+            __syncwarp();
+            mbar_wait_drain(drain, 0);
+        }
+        workers_sync(NW * 32);
+        float* red = (float*)sKV;  // [NW][2 D + 1]
+        if (ok && kl == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                red[warp * (2 * D + 1) + f0 + i] = ak[i];
+                red[warp * (2 * D + 1) + D + f0 + i] = av[i];
+            }
+            if (lane == 0) red[warp * (2 * D + 1) + 2 * D] = l;
+        }
+        workers_sync(NW * 32);
+        for (int e = threadIdx.x; ok && e < 2 * D + 1; e += NW * 32) {
+            float x = 0.f;
+            for (int w = 0; w < NW; w++) x += red[w * (2 * D + 1) + e];
+            if (e < 2 * D) dst[4 + e] = x;
+            else dst[1] = x;
+        }
+        if (threadIdx.x == 0) dst[0] = ok ? m_run : -INFINITY;  // an aborted chunk weighs 0 in the merge
+        // M from TMEM: warps 0-3, thread = row m of M (rows past D at d = 64 are the zero block's)
+        if (warp < 4 && ok) {
+            tc_fence_after();
+            const int mrow = warp * 32 + lane;
+            const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; c++) {
+                uint32_t u[32];
+                tmem_ld32(tM + lrow + c * 32, u);
+                tmem_wait_ld();
+                if (mrow < D) {
+                    float* mr = dst + 4 + 2 * D + (size_t)mrow * D + c * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *(float4*)(mr + i) = make_float4(__uint_as_float(u[i]), __uint_as_float(u[i + 1]),
+                                                         __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tM, C::TMEM_COLS);
+    }
+}
+
+// Merge the chunks of one head (only those holding keys of the sequence)
+// and finish the layer: lse, mu_k, mu_v, u = P_h (q - mu_k), gbar = mu_k . u,
+// o = mu_v + M u - gbar mu_v.  256 threads; the matrix-vector products (P_h
+// and each chunk's M) run one row per warp with coalesced loads.
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16* __restrict__ q,
+                                                            const int* __restrict__ lens, const float* __restrict__ P,
+                                                            const float* __restrict__ part, int H, int Lmax,
+                                                            int chunk, int nchunk, float* __restrict__ lse,
+                                                            __nv_bfloat16* __restrict__ out) {
+    using C = Dec1<D>;
+    constexpr int NWM = kMergeThreads / 32;
+    __shared__ float s_d[D], s_mk[D], s_mv[D], s_u[D], s_red[NWM];
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int len = seq_len1(lens, b, Lmax);
+    const int nc = min(nchunk, (len + chunk - 1) / chunk);
+    const float* pb = part + (size_t)bh * nchunk * C::PART;
+    float m = -INFINITY;
+    for (int c = 0; c < nc; c++) m = fmaxf(m, pb[(size_t)c * C::PART]);
+    float l = 0.f;
+    for (int c = 0; c < nc; c++) l = fmaf(exp2f(pb[(size_t)c * C::PART] - m), pb[(size_t)c * C::PART + 1], l);
+    const float inv = 1.f / l;
+    if (tid < D) {
+        float mk = 0.f, mv = 0.f;
+        for (int c = 0; c < nc; c++) {
+            const float* pc = pb + (size_t)c * C::PART;
+            const float w = exp2f(pc[0] - m);
+            mk = fmaf(w, pc[4 + tid], mk);
+            mv = fmaf(w, pc[4 + D + tid], mv);
+        }
+        s_mk[tid] = mk * inv;
+        s_mv[tid] = mv * inv;
+        s_d[tid] = __bfloat162float(q[(size_t)bh * D + tid]) - mk * inv;  // delta = q - mu_k
+    }
+    __syncthreads();
+    // u = P_h delta: warp w takes rows a = w, w + NWM, ...
+    for (int a = warp; a < D; a += NWM) {
+        const float* Pr = P + ((size_t)h * D + a) * D;
+        float x = 0.f;
+#pragma unroll
+        for (int i = lane; i < D; i += 32) x = fmaf(Pr[i], s_d[i], x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) s_u[a] = x;
+    }
+    __syncthreads();
+    // gbar = mu_k . u
+    {
+        float g = tid < D ? s_mk[tid] * s_u[tid] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+        if (lane == 0) s_red[warp] = g;
+    }
+    __syncthreads();
+    float gbar = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWM; w++) gbar += s_red[w];
+    // o_e = mu_v,e + (sum_c w_c (M_c u)_e) / l - gbar mu_v,e: warp w takes rows e = w, w + NWM, ...
+    for (int e = warp; e < D; e += NWM) {
+        float x = 0.f;
+        for (int c = 0; c < nc; c++) {
+            const float* pc = pb + (size_t)c * C::PART;
+            const float* mr = pc + 4 + 2 * D + (size_t)e * D;
+            float y = 0.f;
+#pragma unroll
+            for (int i = lane; i < D; i += 32) y = fmaf(mr[i], s_u[i], y);
+            x = fmaf(exp2f(pc[0] - m), y, x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) out[(size_t)bh * D + e] = __float2bfloat16_rn(s_mv[e] + x * inv - gbar * s_mv[e]);
+    }
+    if (tid == 0) lse[bh] = (m + __log2f(l)) * LN2;
+}
+
+// ----------------------------------------------------------------- host
+#define PLX_TRY(x)                         \
+    do {                                   \
+        cudaError_t e_ = (x);              \
+        if (e_ != cudaSuccess) return e_;  \
+    } while (0)
+
+// Chunks per head: at most kMaxCtas / (B H) (so the partials' workspace is
+// bounded without knowing the device), at most one per 64 keys.
+constexpr int kMaxCtas = 1024;
+
+size_t dec1_nchunk_max(size_t BH, int Lmax) {
+    const size_t by_keys = ((size_t)Lmax + 63) / 64;
+    const size_t by_ctas = BH >= (size_t)kMaxCtas ? 1 : (kMaxCtas + BH - 1) / BH;
+    return by_keys < by_ctas ? by_keys : by_ctas;
+}
+
+// Per device, once: the SM count; the kernel's shared-memory attributes are
+// set at the same time.  Resident CTAs per SM are the kernel's design point
+// (MIN_CTAS: its launch bounds keep the registers within it, and MIN_CTAS
+// times its shared memory fits an SM), not an occupancy query.
+struct Dec1Dev {
+    int sms = 0, occ = 0;
+};
+template <int D>
+cudaError_t dec1_device(Dec1Dev* out) {
+    static Dec1Dev cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    PLX_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        using C = Dec1<D>;
+        Dec1Dev x;
+        PLX_TRY(cudaFuncSetAttribute(dec1_chunk<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        PLX_TRY(cudaFuncSetAttribute(dec1_chunk<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared));
+        PLX_TRY(cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, dev));
+        x.occ = C::MIN_CTAS;
+        cache[dev] = x;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t decode_tc_impl(const DecodeArgs& a) {
+    using C = Dec1<D>;
+    const int BH = a.B * a.H;
+    Dec1Dev dv;
+    PLX_TRY(dec1_device<D>(&dv));
+    // one wave of resident CTAs: chunks per head, rounded to whole 64-key tiles
+    const size_t cap = dec1_nchunk_max(BH, a.Lmax);
+    size_t per_head = (size_t)dv.sms * dv.occ / BH;
+    if (per_head < 1) per_head = 1;
+    if (per_head > cap) per_head = cap;
+    int chunk = (int)((a.Lmax + per_head - 1) / per_head);
+    chunk = (chunk + C::KT - 1) / C::KT * C::KT;
+    const int nchunk = (a.Lmax + chunk - 1) / chunk;
+    CUtensorMap mk, mv;
+    if (!tc_make_map(&mk, a.k, D, a.Lmax, BH, C::KT) || !tc_make_map(&mv, a.v, D, a.Lmax, BH, C::KT))
+        return cudaErrorInvalidValue;
+    const float scale_log2 = LOG2E / sqrtf((float)D);
+    float* part = (float*)a.ws;
+    timing_begin(a.stream, "dec_chunk");
+    dec1_chunk<D><<<dim3(nchunk, BH), C::NT, C::SMEM, a.stream>>>(mk, mv, (const __nv_bfloat16*)a.q, a.lens, a.H,
+                                                                   a.Lmax, chunk, scale_log2, part, a.status);
+    timing_end(a.stream);
+    PLX_TRY(cudaGetLastError());
+    timing_begin(a.stream, "dec_merge");
+    dec1_merge<D><<<BH, kMergeThreads, 0, a.stream>>>((const __nv_bfloat16*)a.q, a.lens, a.P, part, a.H, a.Lmax, chunk, nchunk,
+                                           a.lse, (__nv_bfloat16*)a.out);
+    timing_end(a.stream);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_tc_ws_bytes(int B, int H, int Lmax, int d) {
+    const size_t BH = (size_t)B * H;
+    const size_t part = d == 64 ? (size_t)Dec1<64>::PART : (size_t)Dec1<128>::PART;
+    return align256(BH * dec1_nchunk_max(BH, Lmax) * part * sizeof(float));
+}
+
+cudaError_t decode_tc(const DecodeArgs& a) {
+    if (a.dtype != 1 || !tc_available()) return cudaErrorNotSupported;
+    return a.d == 64 ? decode_tc_impl<64>(a) : decode_tc_impl<128>(a);
+}
+
+}  // namespace plx

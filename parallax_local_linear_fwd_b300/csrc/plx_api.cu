@@ -338,7 +338,7 @@ int parallax_decode(const void* q, const void* k_cache, const void* v_cache, con
     const bool own = workspace == nullptr;
     void* ws = workspace;
     if (own && cudaMallocAsync(&ws, plx::decode_ws_bytes(B, H, Lmax, d), s) != cudaSuccess) return PLX_ERR_CUDA;
-    plx::DecodeArgs a{q, k_cache, v_cache, lens, P, out, lse, ws, B, H, Lmax, d, dtype, s};
+    plx::DecodeArgs a{q, k_cache, v_cache, lens, P, out, lse, ws, B, H, Lmax, d, dtype, s, status};
     cudaError_t e = plx::decode(a);
     if (own) {
         cudaError_t e2 = cudaFreeAsync(ws, s);

@@ -17,6 +17,7 @@ enum KernelId : unsigned {
     KID_TC_PROJ = 5,
     KID_TC_PROBE = 6,
     KID_TC_BWD_B2 = 7,
+    KID_DECODE = 8,
 };
 
 struct FwdArgs {
@@ -62,6 +63,7 @@ struct DecodeArgs {
     void* ws;          // decode_ws_bytes()
     int B, H, Lmax, d, dtype;
     cudaStream_t stream;
+    unsigned* status;  // device watchdog word
 };
 
 struct ProbeArgs {
@@ -105,6 +107,12 @@ cudaError_t decode(const DecodeArgs& a);
 
 // Tensor-core (tcgen05) family: bf16, d in {64,128}.
 bool tc_available();
+// A 16-bit [BH][T][D] tensor viewed as 3-D (D, T, BH) with a box of 64 x rows
+// x 1 and the 128-byte swizzle (rows past T read as zero); false on failure.
+bool tc_make_map(void* map, const void* base, int D, int T, int BH, int rows);
+// One-pass decode for bf16 caches (tensor-core M = V^T diag(p) K per chunk).
+size_t decode_tc_ws_bytes(int B, int H, int Lmax, int d);
+cudaError_t decode_tc(const DecodeArgs& a);
 size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
 cudaError_t tc_fwd(const FwdArgs& a);

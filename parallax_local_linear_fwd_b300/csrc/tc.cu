@@ -140,17 +140,23 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
 // The projection U = delta P_h^T of both tiles runs once every key MMA is
 // done: delta_a (hi, lo) goes to K stages 0, 1 and delta_b to stages 2, 3,
 // and P_h (f16, one head, both tiles) replaces tile a's Q tile.
+// Q and K arrive as the bf16 inputs and are converted to f16 in shared
+// memory: each softmax warpgroup converts its Q tile once (and writes its q
+// rows in f16 for pass 2); warps 10-11 convert each K tile as soon as it
+// lands, up to NS tiles ahead of its MMAs, and produce the other f16 copies
+// pass 2 reads: this CTA's own two K tiles (keys [256 m, 256 m + 256), by a
+// TMA store of the converted tile) and V rows [256 m, 256 m + 256).
 // TMEM: tile x at column 256 x: S [0,128) (P~ aliases [0,64); U after the
 // loop), Mu [128, 128 + D).
 template <int D>
 struct P1PP {
-    static constexpr int BM = 128, BN = 128, NT = 320;
+    static constexpr int BM = 128, BN = 128, NT = 384;
     static constexpr int NS = D == 64 ? 6 : 4;  // K stages, shared by both tiles
     static constexpr int QB = BM * D * 2;
     static constexpr int KB = BN * D * 2;
-    // q_full, k_full[NS], k_empty[NS], s_full[2], p_full[2], o_done[2],
-    // kfree, proj_ready[2], proj_done[2], drain
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 1 + 2 + 2 + 1;
+    // q_full, k_full[NS], k_empty[NS], k16[NS], q16[2], s_full[2], p_full[2],
+    // o_done[2], kfree, cdone, proj_ready[2], proj_done[2], drain
+    static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1;
     static constexpr int SMEM = 1024 + 2 * QB + NS * KB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 512;
     static_assert(NS >= 4 && KB == QB, "the projection of each tile takes two K stages");
@@ -160,9 +166,10 @@ struct P1PP {
 template <int D>
 __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     tc_pass1_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_k16, const __nv_bfloat16* __restrict__ v_in,
                 const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ mu_k,
-                __half* __restrict__ U, float* __restrict__ gbar, int T, int H, int BH, int npairs,
-                float scale_log2, unsigned* status) {
+                __half* __restrict__ U, float* __restrict__ gbar, __half* __restrict__ q16,
+                __half* __restrict__ v16, int T, int H, int BH, int npairs, float scale_log2, unsigned* status) {
     using C = P1PP<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -172,12 +179,15 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     uint64_t* bars = (uint64_t*)(sK + NS * C::KB);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = k_full + NS;
-    uint64_t* s_full = k_empty + NS;     // [2]
+    uint64_t* k_empty = k_full + NS;     // the MMA thread and the converter leader
+    uint64_t* k16 = k_empty + NS;        // stage s holds K in f16
+    uint64_t* q16r = k16 + NS;           // [2] tile x's Q in f16
+    uint64_t* s_full = q16r + 2;         // [2]
     uint64_t* p_full = s_full + 2;       // [2]
     uint64_t* o_done = p_full + 2;       // [2]
     uint64_t* kfree = o_done + 2;        // every MMA reading a K stage has completed (one phase)
-    uint64_t* proj_ready = kfree + 1;    // [2] delta_x and P_h staged
+    uint64_t* cdone = kfree + 1;         // the converters' K stores have read their stages (one phase)
+    uint64_t* proj_ready = cdone + 1;    // [2] delta_x and P_h staged
     uint64_t* proj_done = proj_ready + 2;  // [2] U_x in TMEM
     uint64_t* drain = proj_done + 2;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
@@ -199,9 +209,11 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < NS; s++) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], 2);
+            mbar_init(&k16[s], 1);
         }
         for (int x = 0; x < 2; x++) {
+            mbar_init(&q16r[x], 128);
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 128);
             mbar_init(&o_done[x], 1);
@@ -209,6 +221,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             mbar_init(&proj_done[x], 1);
         }
         mbar_init(kfree, 1);
+        mbar_init(cdone, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
     }
@@ -222,6 +235,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_k16);
             mbar_expect_tx(q_full, ntiles * C::QB);
             for (int x = 0; x < ntiles; x++) {
 #pragma unroll
@@ -269,8 +283,10 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             }
             __syncwarp();
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, wd, 2)) &&
-                  __all_sync(0xffffffffu, mbar_wait(&k_full[0], 0, wd, 3));
+        // every operand in f16: the Q tiles and key tile 0 converted
+        bool ok = __all_sync(0xffffffffu, mbar_wait(&q16r[0], 0, wd, 2)) &&
+                  (nktb == 0 || __all_sync(0xffffffffu, mbar_wait(&q16r[1], 0, wd, 2))) &&
+                  __all_sync(0xffffffffu, mbar_wait(&k16[0], 0, wd, 3));
         if (ok) {
             tc_fence_after();
             scores(0, 0);
@@ -284,8 +300,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                 tc_fence_after();
                 accumulate(0, j);
             }
-            if (j + 1 < nk) {
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&k_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))))
+            if (j + 1 < nk) {  // key tile j + 1, converted to f16
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&k16[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))))
                     break;
                 tc_fence_after();
                 if (j + 1 < nkta) scores(0, j + 1);
@@ -328,7 +344,55 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         if (elect_one()) mma_commit(drain);
         __syncwarp();
         mbar_wait_drain(drain, 0);
-    } else {
+    } else if (warp >= 10) {
+        // converters (warps 10-11): K tile j to f16 in place as soon as it
+        // lands, then this pair's V rows to f16
+        const int ct = threadIdx.x - 320;  // 0..63
+        bool ok = true;
+        for (int j = 0; j < nk; j++) {
+            const int s = j % NS;
+            ok = mbar_wait(&k_full[s], (j / NS) & 1, wd, 13);
+            if (!named_bar_and(3, 64, ok)) {
+                ok = false;
+                break;
+            }
+            uint4* tile = (uint4*)(sK + s * C::KB);
+#pragma unroll 4
+            for (int c = ct; c < C::KB / 16; c += 64) {
+                const uint4 x = tile[c];
+                tile[c] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
+                                     pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(3, 64);
+            if (ct == 0) {
+                mbar_arrive(&k16[s]);
+                // this pair's own key tiles go to the f16 copy pass 2 reads
+                if ((j >> 1) == m && j * C::BN < T) {
+#pragma unroll
+                    for (int r = 0; r < D / 64; r++)
+                        tma_store_3d(&tm_k16, r * 64, j * C::BN, bh, sK + s * C::KB + r * C::BN * 128);
+                    bulk_commit();
+                    bulk_wait_read_all();  // the stage may be reloaded once the store has read it
+                }
+                mbar_arrive(&k_empty[s]);
+            }
+        }
+        if (ct == 0) {
+            bulk_wait_all();
+            if (ok) mbar_arrive(cdone);  // the K stages may now take delta
+        }
+        if (ok) {  // V rows [q0a, q0a + 256) of head bh in f16
+            const int rows = min(2 * C::BM, T - q0a);
+            const uint4* src = (const uint4*)(v_in + ((size_t)bh * T + q0a) * D);
+            uint4* dst = (uint4*)(v16 + ((size_t)bh * T + q0a) * D);
+            for (int c = ct; c < rows * (D / 8); c += 64) {
+                const uint4 x = src[c];
+                dst[c] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
+                                    pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
+            }
+        }
+    } else if (warp >= 2) {
         // softmax / epilogue warpgroup x: thread <-> query row (TMEM lane)
         const int x = (warp - 2) >> 2;
         const int qd = warp & 3;
@@ -341,6 +405,29 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         uint8_t* sQx = sQ + x * C::QB;
         float m_use = -INFINITY, l = 0.f;
         bool ok = my_nkt > 0;
+        if (ok) {
+            // this thread's q row to f16: in place in the Q tile (the MMA
+            // operand) and in the copy pass 2 reads
+            ok = mbar_wait(q_full, 0, wd, 14);
+            if (__all_sync(0xffffffffu, ok)) {
+                const size_t grow = (size_t)bh * T + t;
+#pragma unroll 4
+                for (int c = 0; c < D / 8; c++) {
+                    const uint32_t off = sw_off(row, 8 * c, C::BM);
+                    const uint4 x8 = *(const uint4*)(sQx + off);
+                    const uint4 h8 = make_uint4(pack_f16_sat(bf16_lo(x8.x), bf16_hi(x8.x)),
+                                                pack_f16_sat(bf16_lo(x8.y), bf16_hi(x8.y)),
+                                                pack_f16_sat(bf16_lo(x8.z), bf16_hi(x8.z)),
+                                                pack_f16_sat(bf16_lo(x8.w), bf16_hi(x8.w)));
+                    *(uint4*)(sQx + off) = h8;
+                    if (t < T) *(uint4*)(q16 + grow * D + 8 * c) = h8;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&q16r[x]);
+            } else {
+                ok = false;
+            }
+        }
         for (int j = 0; j < my_nkt; j++) {
             ok = mbar_wait(&s_full[x], j & 1, wd, 6);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -423,6 +510,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         // the last P~ K of this tile, then every MMA that reads a K stage
         if (ok) ok = mbar_wait(&o_done[x], (my_nkt - 1) & 1, wd, 8);
         if (ok) ok = mbar_wait(kfree, 0, wd, 11);
+        if (ok) ok = mbar_wait(cdone, 0, wd, 15);
         // The four warps agree on ok before the projection (whose steps
         // synchronise on a named barrier): an abort anywhere skips it.
         ok = named_bar_and(1 + x, 128, ok);
@@ -450,7 +538,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
 #pragma unroll
                 for (int g = 0; g < 4; g++) {
                     const uint32_t off = sw_off(row, c * 32 + g * 8, C::BM);
-                    const uint4 qv = *(const uint4*)(sQx + off);
+                    const uint4 qv = *(const uint4*)(sQx + off);  // f16 q
                     const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
                     uint32_t hi[4], lo[4];
 #pragma unroll
@@ -2687,23 +2775,23 @@ cudaError_t fwd_impl(const FwdArgs& a) {
     const float scale_log2 = LOG2E / sqrtf((float)D);
     const size_t n = (size_t)BH * a.T * D;
     TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
-    CUtensorMap mq128, mk128, mu128, mk64, mv64;
-    if (!make_map(&mq128, w.q16, D, a.T, BH, 128) || !make_map(&mk128, w.k16, D, a.T, BH, 128) ||
+    // pass 1 reads the bf16 inputs (a 16-bit map copies the bytes as they
+    // are) and writes the f16 copies of q, k, v that pass 2 reads
+    CUtensorMap mq_in, mk_in, mk16_128, mq128, mu128, mk64, mv64;
+    if (!make_map(&mq_in, a.q, D, a.T, BH, 128) || !make_map(&mk_in, a.k, D, a.T, BH, 128) ||
+        !make_map(&mk16_128, w.k16, D, a.T, BH, 128) || !make_map(&mq128, w.q16, D, a.T, BH, 128) ||
         !make_map(&mu128, w.U, D, a.T, BH, 128) || !make_map(&mk64, w.k16, D, a.T, BH, 64) ||
         !make_map(&mv64, w.v16, D, a.T, BH, 64))
         return cudaErrorInvalidValue;
-    {
-        const void* src[3] = {a.q, a.k, a.v};
-        __half* dst[3] = {w.q16, w.k16, w.v16};
-        PLX_TRY(to_f16(src, dst, 3, n, a.stream));
-    }
+    (void)n;
     {  // pass 1: two query tiles per CTA, projection after the key loop
         using C = P1PP<D>;
         const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
         PLX_TRY(cudaFuncSetAttribute(tc_pass1_pp<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass1");
-        tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mk128, a.P, a.lse, a.mu_k, w.U, w.gbar,
-                                                                   a.T, a.H, BH, npairs, scale_log2, a.status);
+        tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(
+            mq_in, mk_in, mk16_128, (const __nv_bfloat16*)a.v, a.P, a.lse, a.mu_k, w.U, w.gbar, w.q16, w.v16, a.T,
+            a.H, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
@@ -2874,6 +2962,10 @@ cudaError_t probe_impl(const ProbeArgs& a) {
 }  // namespace
 
 bool tc_available() { return encode_fn() != nullptr; }
+
+bool tc_make_map(void* map, const void* base, int D, int T, int BH, int rows) {
+    return make_map(reinterpret_cast<CUtensorMap*>(map), base, D, T, BH, rows);
+}
 
 size_t tc_fwd_ws_bytes(int B, int H, int T, int d) {
     const size_t n = (size_t)B * H * T;

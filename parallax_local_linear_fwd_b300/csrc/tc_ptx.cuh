@@ -144,6 +144,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, int c0
         "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
         : "memory");
 }
+// Store a shared-memory tile to global memory through a tensor map
+// (coordinates >= 0; rows and columns past the tensor's extent are not
+// written).  Completion is tracked per issuing thread with bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int c1, int c2, const void* src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The shared-memory sources of every committed group have been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

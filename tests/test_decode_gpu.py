@@ -92,3 +92,45 @@ def test_decode_invalid_arguments():
         plx.parallax_decode(q, kc, kc, P)
     assert e.value.code == plx.PLX_ERR_UNSUPPORTED
     assert plx.parallax_last_device_error()[0] == plx.PLX_OK
+
+
+def test_decode_full_size_d128_many_tiles_per_chunk():
+    # B4 H16 with a 4096-key cache at d = 128 (the B4 H16 T4096 d128 forward's
+    # shape): each head's keys split into a few chunks of many 64-key tiles,
+    # so the stage ring wraps many times per chunk and the merge combines
+    # several chunks; ragged lengths put chunk ends inside tiles
+    B, H, L, d = 4, 16, 4096, 128
+    lens = [4096, 1, 2047, 3001]
+    go, gl, ro, rl = _case(B, H, L, d, "bf16", lens, seed=77)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+
+
+def test_decode_nan_rows_past_the_lengths_are_ignored():
+    # cache rows past lens[b] are not part of the sequence: even NaN there
+    # must not reach the output
+    B, H, L, d = 3, 2, 500, 64
+    inp = plx_synth.generate(B, H, L, d, "bf16", seed=88, p_std=0.3 / np.sqrt(d))
+    lens = [37, 500, 129]
+    for b_, n in enumerate(lens):
+        inp["k"][b_, :, n:] = 0x7FC0  # bf16 NaN
+        inp["v"][b_, :, n:] = 0x7FC0
+    rng = np.random.default_rng(89)
+    qn_store = plx_synth.to_bf16_bits(rng.standard_normal((B, H, d)))
+    f = inputs_f64(inp)
+    qfull = np.zeros((B, H, L, d))
+    rows = []
+    for b_ in range(B):
+        for h in range(H):
+            qfull[b_, h, lens[b_] - 1] = plx_synth.bf16_bits_to_f32(qn_store[b_, h]).astype(np.float64)
+            rows.append((b_, h, lens[b_] - 1))
+    kk = np.nan_to_num(f["k"], nan=0.0)
+    vv = np.nan_to_num(f["v"], nan=0.0)
+    ro, rl, _ = oracle.forward_rows(qfull, kk, vv, f["P"], rows)
+    q = to_device(qn_store)
+    k, v, P = (to_device(inp[x]) for x in ("k", "v", "P"))
+    out, lse = plx.parallax_decode(q, k, v, P, lens=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    assert plx.parallax_last_device_error()[0] == plx.PLX_OK
+    go = to_host64(out).reshape(-1, d)
+    assert np.isfinite(go).all()
+    assert rel_err(go, ro, "bf16") < TOL_BF16
