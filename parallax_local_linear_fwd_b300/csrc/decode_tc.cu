@@ -79,7 +79,7 @@ struct Dec1 {
     static constexpr int TB = KT * D * 2;    // one K or V tile (bf16 / f16): 8 KB
     static constexpr int ZB = D == 64 ? TB : 0;  // zero tile: rows 64..127 of A at d = 64
     static constexpr int NBAR = 2 * NS + 2;  // full[NS], empty[NS], mma_done, drain
-    static constexpr int QS = 33;            // stride of q's 32-feature parts in shared memory
+    static constexpr int QS = 34;            // stride of q's 32-feature parts in shared memory (even: float2)
     static constexpr int SMEM = 1024 + NS * 2 * TB + ZB + NBAR * 8 + 16 + 8 * 4 + TPK * QS * 4 + 16;
     static_assert(KT * TPK == NW * 32, "one thread per (key, feature part)");
     static_assert(MIN_CTAS * (SMEM + 1024) <= 233472, "MIN_CTAS CTAs fit an SM's shared memory");
@@ -180,13 +180,14 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
         const int f0 = fp * 32;  // features [f0, f0 + 32)
         // q in shared memory as fp32 (threads of one feature part read the
         // same words: broadcasts), which keeps 32 registers free
-        // (part fp at fp * QS: the parts' words fall in different banks)
+        // (part fp at fp * QS: the parts' words fall in different banks; QS is
+        // even so pairs load as float2)
         for (int i = threadIdx.x; i < D; i += NW * 32) sq[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(q[(size_t)bh * D + i]);
         workers_sync(NW * 32);
         const float* qf = sq + fp * C::QS;
-        float ak[32], av[32];
+        uint64_t ak[16], av[16];  // sum p k, sum p v over this thread's keys, as f32x2 pairs
 #pragma unroll
-        for (int i = 0; i < 32; i++) ak[i] = av[i] = 0.f;
+        for (int i = 0; i < 16; i++) ak[i] = av[i] = 0;
         float l = 0.f, m_run = -INFINITY;
         const uint32_t idM = idesc_mma(128, D, true, true);
         bool ok = true;
@@ -213,18 +214,19 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             const bool valid = key < k_end;
             // scores: this thread's 32 features of key r, summed over the TPK threads of the key
             uint4 kc[4];
-            float dp[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+            uint64_t dp[4] = {0, 0, 0, 0};  // four independent chains of f32x2 pairs
 #pragma unroll
             for (int c = 0; c < 4; c++) {
                 kc[c] = *(const uint4*)(sk + swz(r, f0 + 8 * c, KT));
                 const uint32_t w[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    dp[c] = fmaf(qf[8 * c + 2 * e], bf16_lo(w[e]), dp[c]);
-                    dp[c] = fmaf(qf[8 * c + 2 * e + 1], bf16_hi(w[e]), dp[c]);
+                    const float2 qq = *(const float2*)(qf + 8 * c + 2 * e);
+                    dp[c] = ffma2(f2(qq.x, qq.y), f2(bf16_lo(w[e]), bf16_hi(w[e])), dp[c]);
                 }
             }
-            float dot = (dp[0] + dp[1]) + (dp[2] + dp[3]);
+            const float2 d01 = uf2(fadd2(fadd2(dp[0], dp[1]), fadd2(dp[2], dp[3])));
+            float dot = d01.x + d01.y;
 #pragma unroll
             for (int o = KW; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
             const float sc = valid ? dot * scale_log2 : -INFINITY;
@@ -246,10 +248,11 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
                 alpha = fast_exp2_dec(m_run - m_new);
                 m_run = m_new;
                 l *= alpha;
+                const uint64_t A2 = f2(alpha, alpha);
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    ak[i] *= alpha;
-                    av[i] *= alpha;
+                for (int i = 0; i < 16; i++) {
+                    ak[i] = fmul2(ak[i], A2);
+                    av[i] = fmul2(av[i], A2);
                 }
                 if (j > 0) {
                     // M *= alpha once the previous tile's MMA has landed (warps 0-3
@@ -275,28 +278,33 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             }
             const float p = valid ? fast_exp2_dec(sc - m_run) : 0.f;
             if (fp == 0) l += p;
-            // p k and v in f16, written back in place; the register sums
+            // p k and v in f16, written back in place; the register sums.  A key
+            // past the sequence writes zeros (its cache row may hold anything)
+            const uint64_t P2 = f2(p, p);
 #pragma unroll
             for (int c = 0; c < 4; c++) {
                 const uint32_t off = swz(r, f0 + 8 * c, KT);
-                const uint4 vc = *(const uint4*)(sv + off);
-                const uint32_t kw[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
-                const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
-                uint32_t ko[4], vo[4];
+                uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
+                if (valid) {
+                    const uint4 vc = *(const uint4*)(sv + off);
+                    const uint32_t kw[4] = {kc[c].x, kc[c].y, kc[c].z, kc[c].w};
+                    const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
+                    uint32_t kp[4], vp[4];
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const float k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
-                    const float v0 = valid ? bf16_lo(vw[e]) : 0.f, v1 = valid ? bf16_hi(vw[e]) : 0.f;
-                    const float pk0 = valid ? p * k0 : 0.f, pk1 = valid ? p * k1 : 0.f;
-                    ak[8 * c + 2 * e] += pk0;
-                    ak[8 * c + 2 * e + 1] += pk1;
-                    av[8 * c + 2 * e] = fmaf(p, v0, av[8 * c + 2 * e]);
-                    av[8 * c + 2 * e + 1] = fmaf(p, v1, av[8 * c + 2 * e + 1]);
-                    ko[e] = pack_f16(pk0, pk1);
-                    vo[e] = pack_f16_sat(v0, v1);
+                    for (int e = 0; e < 4; e++) {
+                        const uint64_t pk = fmul2(P2, f2(bf16_lo(kw[e]), bf16_hi(kw[e])));
+                        const uint64_t vv = f2(bf16_lo(vw[e]), bf16_hi(vw[e]));
+                        ak[4 * c + e] = fadd2(ak[4 * c + e], pk);
+                        av[4 * c + e] = ffma2(P2, vv, av[4 * c + e]);
+                        const float2 pkf = uf2(pk);
+                        kp[e] = pack_f16(pkf.x, pkf.y);
+                        vp[e] = pack_f16_sat(bf16_lo(vw[e]), bf16_hi(vw[e]));
+                    }
+                    ko = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+                    vo = make_uint4(vp[0], vp[1], vp[2], vp[3]);
                 }
-                *(uint4*)(sk + off) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-                *(uint4*)(sv + off) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+                *(uint4*)(sk + off) = ko;
+                *(uint4*)(sv + off) = vo;
             }
             fence_proxy_async_smem();
             workers_sync(NW * 32);
@@ -325,13 +333,22 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
         float* dst = part + ((size_t)bh * gridDim.x + blockIdx.x) * C::PART;
         // l, sum p k, sum p v: reduce over the keys (lanes of one feature part
         // first, then the worker warps through shared memory, reusing stage 0)
+        float akf[32], avf[32];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const float2 a2 = uf2(ak[i]), b2 = uf2(av[i]);
+            akf[2 * i] = a2.x;
+            akf[2 * i + 1] = a2.y;
+            avf[2 * i] = b2.x;
+            avf[2 * i + 1] = b2.y;
+        }
 #pragma unroll
         for (int o = 1; o < KW; o <<= 1) {
             l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
             for (int i = 0; i < 32; i++) {
-                ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], o);
-                av[i] += __shfl_xor_sync(0xffffffffu, av[i], o);
+                akf[i] += __shfl_xor_sync(0xffffffffu, akf[i], o);
+                avf[i] += __shfl_xor_sync(0xffffffffu, avf[i], o);
             }
         }
         // every tile's MMA must be done before stage 0 is reused below
@@ -345,8 +362,8 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
         if (ok && kl == 0) {
 #pragma unroll
             for (int i = 0; i < 32; i++) {
-                red[warp * (2 * D + 1) + f0 + i] = ak[i];
-                red[warp * (2 * D + 1) + D + f0 + i] = av[i];
+                red[warp * (2 * D + 1) + f0 + i] = akf[i];
+                red[warp * (2 * D + 1) + D + f0 + i] = avf[i];
             }
             if (lane == 0) red[warp * (2 * D + 1) + 2 * D] = l;
         }
@@ -389,7 +406,9 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
 // Merge the chunks of one head (only those holding keys of the sequence)
 // and finish the layer: lse, mu_k, mu_v, u = P_h (q - mu_k), gbar = mu_k . u,
 // o = mu_v + M u - gbar mu_v.  256 threads; the matrix-vector products (P_h
-// and each chunk's M) run one row per warp with coalesced loads.
+// and each chunk's M) give four threads to a row (D/4 columns each) and
+// issue all their loads before using them, so each product is about one
+// memory latency.
 constexpr int kMergeThreads = 256;
 
 template <int D>
@@ -400,9 +419,12 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
                                                             __nv_bfloat16* __restrict__ out) {
     using C = Dec1<D>;
     constexpr int NWM = kMergeThreads / 32;
-    __shared__ float s_d[D], s_mk[D], s_mv[D], s_u[D], s_red[NWM];
+    constexpr int RPP = kMergeThreads / 4;   // rows per pass, four threads per row
+    constexpr int CQ = D / 4;                // columns per thread
+    __shared__ float s_d[D], s_mk[D], s_mv[D], s_u[D], s_red[NWM], s_w[2];
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int qr = tid & 3, rr = tid >> 2;   // column quarter, row within a pass
     const int len = seq_len1(lens, b, Lmax);
     const int nc = min(nchunk, (len + chunk - 1) / chunk);
     const float* pb = part + (size_t)bh * nchunk * C::PART;
@@ -424,15 +446,24 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
         s_d[tid] = __bfloat162float(q[(size_t)bh * D + tid]) - mk * inv;  // delta = q - mu_k
     }
     __syncthreads();
-    // u = P_h delta: warp w takes rows a = w, w + NWM, ...
-    for (int a = warp; a < D; a += NWM) {
-        const float* Pr = P + ((size_t)h * D + a) * D;
+    // u = P_h delta
+    for (int a0 = 0; a0 < D; a0 += RPP) {
+        const int a = a0 + rr;
         float x = 0.f;
+        if (a < D) {
+            const float4* Pr = (const float4*)(P + ((size_t)h * D + a) * D + qr * CQ);
+            float4 pv[CQ / 4];
 #pragma unroll
-        for (int i = lane; i < D; i += 32) x = fmaf(Pr[i], s_d[i], x);
+            for (int i = 0; i < CQ / 4; i++) pv[i] = Pr[i];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) s_u[a] = x;
+            for (int i = 0; i < CQ / 4; i++) {
+                const float* dd = s_d + qr * CQ + 4 * i;
+                x = fmaf(pv[i].x, dd[0], fmaf(pv[i].y, dd[1], fmaf(pv[i].z, dd[2], fmaf(pv[i].w, dd[3], x))));
+            }
+        }
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if (a < D && qr == 0) s_u[a] = x;
     }
     __syncthreads();
     // gbar = mu_k . u
@@ -446,22 +477,32 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
     float gbar = 0.f;
 #pragma unroll
     for (int w = 0; w < NWM; w++) gbar += s_red[w];
-    // o_e = mu_v,e + (sum_c w_c (M_c u)_e) / l - gbar mu_v,e: warp w takes rows e = w, w + NWM, ...
-    for (int e = warp; e < D; e += NWM) {
+    // o_e = mu_v,e + (sum_c w_c (M_c u)_e) / l - gbar mu_v,e
+    for (int e0 = 0; e0 < D; e0 += RPP) {
+        const int e = e0 + rr;
         float x = 0.f;
-        for (int c = 0; c < nc; c++) {
-            const float* pc = pb + (size_t)c * C::PART;
-            const float* mr = pc + 4 + 2 * D + (size_t)e * D;
-            float y = 0.f;
+        if (e < D) {
+            for (int c = 0; c < nc; c++) {
+                const float* pc = pb + (size_t)c * C::PART;
+                const float4* mr = (const float4*)(pc + 4 + 2 * D + (size_t)e * D + qr * CQ);
+                float4 mv4[CQ / 4];
 #pragma unroll
-            for (int i = lane; i < D; i += 32) y = fmaf(mr[i], s_u[i], y);
-            x = fmaf(exp2f(pc[0] - m), y, x);
+                for (int i = 0; i < CQ / 4; i++) mv4[i] = mr[i];
+                float y = 0.f;
+#pragma unroll
+                for (int i = 0; i < CQ / 4; i++) {
+                    const float* uu = s_u + qr * CQ + 4 * i;
+                    y = fmaf(mv4[i].x, uu[0], fmaf(mv4[i].y, uu[1], fmaf(mv4[i].z, uu[2], fmaf(mv4[i].w, uu[3], y))));
+                }
+                x = fmaf(exp2f(pc[0] - m), y, x);
+            }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) out[(size_t)bh * D + e] = __float2bfloat16_rn(s_mv[e] + x * inv - gbar * s_mv[e]);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if (e < D && qr == 0) out[(size_t)bh * D + e] = __float2bfloat16_rn(s_mv[e] + x * inv - gbar * s_mv[e]);
     }
     if (tid == 0) lse[bh] = (m + __log2f(l)) * LN2;
+    (void)s_w;
 }
 
 // ----------------------------------------------------------------- host

@@ -305,6 +305,35 @@ __device__ __forceinline__ uint64_t desc_mn_lbo(uint32_t tile, int kk, uint32_t 
     return sdesc_sw128(tile + (uint32_t)(kk * 16 * 128), lbo, 1024);
 }
 
+// ------------------------------------------------------------ f32x2
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes
+// of work.  A pair lives in a 64-bit register; mov.b64 packs and unpacks it.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 uf2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ------------------------------------------------------------ packing
 // Two floats -> one 32-bit word of two 16-bit values, round to nearest even;
 // `lo` lands in the low half (the even element of an MMA operand pair).
