@@ -111,7 +111,8 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c, int rows) {
 //   Mu_a += P~_a(j) K,  S_a(j+1),  Mu_b += P~_b(j) K,  S_b(j+1)
 // The projection U = delta P_h^T of both tiles runs once every key MMA is
 // done: delta_a (hi, lo) goes to K stages 0, 1 and delta_b to stages 2, 3,
-// and P_h (f16, one head, both tiles) replaces tile a's Q tile.
+// and P_h (f16, one head, both tiles) sits in a slot of its own, written by
+// the converter warps once the first key stages are converted.
 // Q and K arrive as the bf16 inputs and are converted to f16 in shared
 // memory: each softmax warpgroup converts its Q tile once (and writes its q
 // rows in f16 for pass 2); warps 10-11 convert each K tile as soon as it
@@ -126,10 +127,11 @@ struct P1PP {
     static constexpr int NS = D == 64 ? 6 : 4;  // K stages, shared by both tiles
     static constexpr int QB = BM * D * 2;
     static constexpr int KB = BN * D * 2;
+    static constexpr int PB = D * D * 2;  // P_h in f16
     // q_full, k_full[NS], k_empty[NS], k16[NS], q16[2], s_full[2], p_full[2],
-    // o_done[2], kfree, cdone, proj_ready[2], proj_done[2], drain
-    static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1;
-    static constexpr int SMEM = 1024 + 2 * QB + NS * KB + NBAR * 8 + 16;
+    // o_done[2], kfree, cdone, ph_full, proj_ready[2], proj_done[2], drain
+    static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 2 + 1;
+    static constexpr int SMEM = 1024 + 2 * QB + NS * KB + PB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 512;
     static_assert(NS >= 4 && KB == QB, "the projection of each tile takes two K stages");
     static_assert(SMEM <= 232448, "one CTA per SM must fit");
@@ -148,7 +150,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     uint8_t* sm = align1024(smem_raw);
     uint8_t* sQ = sm;                // tile x at x QB
     uint8_t* sK = sQ + 2 * C::QB;    // stage s at s KB
-    uint64_t* bars = (uint64_t*)(sK + NS * C::KB);
+    uint8_t* sP = sK + NS * C::KB;   // P_h (f16, K-major [a][b]): the projections' B operand
+    uint64_t* bars = (uint64_t*)(sP + C::PB);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
     uint64_t* k_empty = k_full + NS;     // the MMA thread and the converter leader
@@ -159,7 +162,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     uint64_t* o_done = p_full + 2;       // [2]
     uint64_t* kfree = o_done + 2;        // every MMA reading a K stage has completed (one phase)
     uint64_t* cdone = kfree + 1;         // the converters' K stores have read their stages (one phase)
-    uint64_t* proj_ready = cdone + 1;    // [2] delta_x and P_h staged
+    uint64_t* ph_full = cdone + 1;       // P_h staged in f16 (one phase)
+    uint64_t* proj_ready = ph_full + 1;  // [2] delta_x staged
     uint64_t* proj_done = proj_ready + 2;  // [2] U_x in TMEM
     uint64_t* drain = proj_done + 2;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
@@ -194,6 +198,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         }
         mbar_init(kfree, 1);
         mbar_init(cdone, 1);
+        mbar_init(ph_full, 1);
         mbar_init(drain, 1);
         fence_barrier_init();
     }
@@ -290,14 +295,13 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         if (ok) {
             if (elect_one()) mma_commit(kfree);
             __syncwarp();
-            // projections U_x = delta_x P_h^T (delta = hi + lo, P_h in f16 in tile
-            // a's Q slot): M = 128 rows, N = D, K = D, into S_x's columns
+            // projections U_x = delta_x P_h^T (delta = hi + lo, P_h in f16 in its
+            // slot): M = 128 rows, N = D, K = D, into S_x's columns
             const uint32_t idP = idesc_mma(128, D, false, false);
-            const uint32_t pb = smem_u32(sQ);
+            const uint32_t pb = smem_u32(sP);
             for (int x = 0; x < ntiles; x++) {
-                // U_b's B operand is written by warpgroup 0: wait for both
-                if (!__all_sync(0xffffffffu, mbar_wait(&proj_ready[0], 0, wd, 9))) break;
-                if (x == 1 && !__all_sync(0xffffffffu, mbar_wait(&proj_ready[1], 0, wd, 10))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(ph_full, 0, wd, 9))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&proj_ready[x], 0, wd, 10))) break;
                 tc_fence_after();
                 const uint32_t dhi = smem_u32(sK + (2 * x) * C::KB), dlo = smem_u32(sK + (2 * x + 1) * C::KB);
                 const uint32_t tS = tmem + 256 * x;
@@ -318,8 +322,10 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         mbar_wait_drain(drain, 0);
     } else if (warp >= 10) {
         // converters (warps 10-11): K tile j to f16 in place as soon as it
-        // lands, then this pair's V rows to f16
+        // lands; P_h to f16 once the first stages are done (tile NS arrives
+        // only after tile 0's scores complete); then this pair's V rows
         const int ct = threadIdx.x - 320;  // 0..63
+        const int ph_at = min(nk, NS) - 1;
         bool ok = true;
         for (int j = 0; j < nk; j++) {
             const int s = j % NS;
@@ -348,6 +354,22 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                     bulk_wait_read_all();  // the stage may be reloaded once the store has read it
                 }
                 mbar_arrive(&k_empty[s]);
+            }
+            if (j == ph_at) {
+                // P_h (fp32, row a = output index) as the K-major B operand of
+                // both projections: rows = a, K = b
+                const float* Ph = P + (size_t)(bh % H) * D * D;
+#pragma unroll 8
+                for (int id = ct; id < D * D / 8; id += 64) {
+                    const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
+                    const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
+                    const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
+                    *(uint4*)(sP + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
+                                                                    pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(3, 64);
+                if (ct == 0) mbar_arrive(ph_full);
             }
         }
         if (ct == 0) {
@@ -522,21 +544,6 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                     }
                     *(uint4*)(sDhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     *(uint4*)(sDlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-            }
-            if (x == 0) {
-                // every thread of warpgroup 0 has read its q row: P_h (f16)
-                // replaces tile a's Q tile as the K-major B operand of both
-                // projections (rows = output index a, K = input index b)
-                named_bar_sync(1, 128);
-                const float* Ph = P + (size_t)(bh % H) * D * D;
-#pragma unroll 1
-                for (int id = row; id < D * D / 8; id += 128) {
-                    const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
-                    const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
-                    const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
-                    *(uint4*)(sQ + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
-                                                                    pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
                 }
             }
             fence_proxy_async_smem();
