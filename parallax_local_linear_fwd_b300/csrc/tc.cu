@@ -1685,50 +1685,69 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
 //   U = delta P_h^T and ddelta = du P_h, with delta and du split into f16
 //   hi + lo halves against P_h in f16 (the forward's projection: delta is
 //   formed from the same f16 copy of q, so U equals the forward's);
-//   dP_h partial += du^T delta over the CTA's 512 rows as one M = 128
+//   dP_h partial += du^T delta over a chunk of 512 rows as one M = 128
 //   product whose A stacks [du | delta] along M (rows 0..63 of the result
 //   are du^T delta), in three passes hi.hi + lo.hi + hi.lo.
-// Two threads per row: warps w and w + 4 cover rows 32 (w % 4) .. + 31 (their
-// TMEM lane quadrant) and the column halves [0, 32) and [32, 64), so twice as
-// many row loads are in flight; the halves' row sums meet in shared memory.
+// Two persistent CTAs per SM each walk a contiguous range of the (head,
+// chunk) list tile by tile and write each chunk's partial when the chunk
+// ends.  Global memory is read and written in row-contiguous order: thread
+// item (row, quad) covers columns [4 quad, 4 quad + 4) of one row, sixteen
+// consecutive threads one whole row.  The products leave U and ddelta in
+// TMEM, one row per lane; they go through shared memory (fp32, in the space
+// of the finished MMA operand tiles) back to the (row, quad) layout, where
+// the row dot products are summed across the row's sixteen threads.
 struct B2T {
-    static constexpr int D = 64, BM = 128, NT = 256, TILES = 4;  // 512 rows per CTA
+    static constexpr int D = 64, BM = 128, NT = 256, TILES = 4;  // 512 rows per chunk
     static constexpr int TB = BM * D * 2;                         // one f16 [128][64] tile
     static constexpr int PB = D * D * 2;                          // P_h in f16
-    static constexpr int RED = BM * 4 * 4;                        // the upper half's 4 row sums
+    static constexpr int LDF = D + 4;                             // row stride of the fp32 U / ddelta tiles
+    static constexpr int XB = BM * LDF * 4;
+    static constexpr int OPS = (4 * TB > 2 * XB ? 4 * TB : 2 * XB + 1023) / 1024 * 1024;
+    static constexpr int ITEMS = BM * (D / 4) / NT;               // (row, quad) items per thread per tile
     // tiles in this order: [du_hi | delta_hi] and [du_lo | delta_lo] sit TB
     // apart, as the two 64-row M blocks of the dP product's A operand
-    static constexpr int SMEM = 1024 + 4 * TB + PB + RED + 64;
+    static constexpr int SMEM = 1024 + OPS + PB + 2 * BM * 4 + 64;
     static constexpr unsigned TMEM_COLS = 256;  // U [0,64), ddelta [64,128), dP [128,192)
 };
 static_assert(B2T::BM * B2T::TILES == RowCfg<64>::ROWS_PER_CTA, "dP partial layout shared with tc_rows");
+static_assert(B2T::ITEMS == 8, "the item loops are written for 8 items per thread");
+
+// One tile of B2's walk: item = h * nchunks + chunk, rows [r0, r_end) of the
+// chunk's rows [chunk * 512, min(chunk * 512 + 512, B T)).
+struct B2Tile {
+    int item, r0, r_end;
+};
 
 __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q16, const float* __restrict__ mu_k,
                                                  const float* __restrict__ P, const float* __restrict__ lse,
                                                  const float* __restrict__ R, const float* __restrict__ ebar,
                                                  __half* __restrict__ U, __half* __restrict__ dmu,
                                                  float* __restrict__ dq_acc, float* __restrict__ rowpack,
-                                                 float* __restrict__ dp_partial, int B, int H, int T,
+                                                 float* __restrict__ dp_partial, int B, int H, int T, int nchunks,
                                                  unsigned* status) {
     using C = B2T;
-    constexpr int D = C::D;
+    constexpr int D = C::D, LDF = C::LDF, RPC = C::BM * C::TILES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* sUH = sm;
     uint8_t* sDH = sUH + C::TB;
     uint8_t* sUL = sDH + C::TB;
     uint8_t* sDL = sUL + C::TB;
-    uint8_t* sP = sDL + C::TB;
-    float4* sRed = (float4*)(sP + C::PB);       // [128] the upper column half's row sums
-    uint64_t* bars = (uint64_t*)(sP + C::PB + C::RED);  // [0] the tile's MMAs are done, [1] teardown drain
+    float* sXU = (float*)sm;                   // after the products: U (fp32) [128][LDF]
+    float* sXD = (float*)(sm + C::XB);         // and ddelta
+    uint8_t* sP = sm + C::OPS;
+    float* sEb = (float*)(sP + C::PB);         // the tile's ebar
+    float* sL = sEb + C::BM;                   // and lse
+    uint64_t* bars = (uint64_t*)(sL + C::BM);  // [0] the tile's MMAs are done, [1] teardown drain
     uint32_t* holder = (uint32_t*)(bars + 2);
     volatile int* abortf = (volatile int*)(holder + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
     const int rit = quad * 32 + lane;             // row in the tile = TMEM lane
-    const int h = blockIdx.y;
     const int nrows = B * T;
-    const int r_begin = blockIdx.x * C::BM * C::TILES, r_end = min(r_begin + C::BM * C::TILES, nrows);
+    const int nitems = H * nchunks;
+    const int it_begin = (int)((long long)blockIdx.x * nitems / gridDim.x);
+    const int it_end = (int)((long long)(blockIdx.x + 1) * nitems / gridDim.x);
     const Watchdog wd{status, abortf, KID_TC_BWD_B2, wait_limit(status)};
     if (tid == 0) {
         *abortf = 0;
@@ -1736,63 +1755,110 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
         mbar_init(&bars[1], 1);
         fence_barrier_init();
     }
-    // P_h in f16 as a K-major [a][b] tile: the B operand of U (N = a, K = b)
-    // and, read MN-major, of ddelta (N = b, K = a)
-    const float* Ph = P + (size_t)h * D * D;
-    for (int id = tid; id < D * D / 8; id += C::NT) {
-        const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
-        const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
-        const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
-        *(uint4*)(sP + sw_off(pa, pb0, D)) =
-            make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w), pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
-    }
     if (warp == 0) tmem_alloc(holder, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder, tU = tmem, tDD = tmem + 64, tDP = tmem + 128;
     const uint32_t lrow = (uint32_t)(quad * 32) << 16;
-    const int c0 = 32 * half;  // this thread's columns [c0, c0 + 32)
+    const int c0 = 32 * half;  // this thread's TMEM columns [c0, c0 + 32)
+    const int qd = tid & 15;   // item column quad: columns [4 qd, 4 qd + 4)
     const uint32_t idN = idesc_mma(128, D, false, false);  // U: A and B K-major
     const uint32_t idNb = idesc_mma(128, D, false, true);  // ddelta: B = P_h read MN-major
     const uint32_t idPd = idesc_mma(128, D, true, true);   // dP: A = [du | delta], B = delta, both MN-major
+
+    auto first_tile = [&](int item) -> B2Tile {
+        const int chunk = item % nchunks;
+        return B2Tile{item, chunk * RPC, min(chunk * RPC + RPC, nrows)};
+    };
+    auto next_tile = [&](const B2Tile& c) -> B2Tile {
+        if (c.r0 + C::BM < c.r_end) return B2Tile{c.item, c.r0 + C::BM, c.r_end};
+        return c.item + 1 < it_end ? first_tile(c.item + 1) : B2Tile{-1, 0, 0};
+    };
+    // item k of this thread: row (k * NT + tid) / 16 of the tile, quad qd
+    auto item_row = [&](const B2Tile& c, int k, int& rl, size_t& row) -> bool {
+        rl = (k * C::NT + tid) >> 4;
+        const int r = c.r0 + rl;
+        const bool valid = r < c.r_end;
+        const int h = c.item / nchunks;
+        row = valid ? ((size_t)(r / T) * H + h) * T + r % T : 0;
+        return valid;
+    };
+
     bool ok = true;
-    int tile = 0;
-    for (int r0 = r_begin; r0 < r_end; r0 += C::BM, tile++) {
-        const int r = r0 + rit;
-        const bool valid = r < r_end;
-        const size_t row = valid ? ((size_t)(r / T) * H + h) * T + r % T : 0;
-        const float eb = valid ? ebar[row] : 0.f;
-        // delta = q - mu_k and du = R - ebar mu_k as f16 hi + lo, K-major rows
-#pragma unroll 2
-        for (int c = c0 / 8; c < c0 / 8 + 4; c++) {
-            uint32_t dh[4] = {0, 0, 0, 0}, dl[4] = {0, 0, 0, 0}, uh[4] = {0, 0, 0, 0}, ul[4] = {0, 0, 0, 0};
-            if (valid) {
-                const uint4 qv = *(const uint4*)(q16 + row * D + 8 * c);
-                const float4 m0 = *(const float4*)(mu_k + row * D + 8 * c);
-                const float4 m1 = *(const float4*)(mu_k + row * D + 8 * c + 4);
-                const float4 x0 = *(const float4*)(R + row * D + 8 * c);
-                const float4 x1 = *(const float4*)(R + row * D + 8 * c + 4);
-                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                const float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-                const float rv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                for (int x = 0; x < 4; x++) {
-                    const float d0 = f16_lo(qw[x]) - m[2 * x];
-                    const float d1 = f16_hi(qw[x]) - m[2 * x + 1];
-                    dh[x] = pack_f16(d0, d1);
-                    dl[x] = pack_f16(d0 - f16_lo(dh[x]), d1 - f16_hi(dh[x]));
-                    const float u0 = rv[2 * x] - eb * m[2 * x];
-                    const float u1 = rv[2 * x + 1] - eb * m[2 * x + 1];
-                    uh[x] = pack_f16(u0, u1);
-                    ul[x] = pack_f16(u0 - f16_lo(uh[x]), u1 - f16_hi(uh[x]));
-                }
+    int head = -1, ntile = 0;
+    B2Tile cur = it_begin < it_end ? first_tile(it_begin) : B2Tile{-1, 0, 0};
+    while (cur.item >= 0) {
+        const int h = cur.item / nchunks;
+        const bool chunk_first = cur.r0 % RPC == 0;
+        const bool chunk_last = cur.r0 + C::BM >= cur.r_end;
+        if (h != head) {
+            // P_h in f16 as a K-major [a][b] tile: the B operand of U (N = a,
+            // K = b) and, read MN-major, of ddelta (N = b, K = a); the previous
+            // tile's products have completed
+            const float* Ph = P + (size_t)h * D * D;
+            for (int id = tid; id < D * D / 8; id += C::NT) {
+                const int pa = id / (D / 8), pb0 = (id % (D / 8)) * 8;
+                const float4 x0 = *(const float4*)(Ph + pa * D + pb0);
+                const float4 x1 = *(const float4*)(Ph + pa * D + pb0 + 4);
+                *(uint4*)(sP + sw_off(pa, pb0, D)) = make_uint4(pack_f16(x0.x, x0.y), pack_f16(x0.z, x0.w),
+                                                                pack_f16(x1.x, x1.y), pack_f16(x1.z, x1.w));
             }
-            const uint32_t off = sw_off(rit, 8 * c, C::BM);
-            *(uint4*)(sDH + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-            *(uint4*)(sDL + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-            *(uint4*)(sUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-            *(uint4*)(sUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+            head = h;
+        }
+        // delta = q - mu_k and du = R - ebar mu_k as f16 hi + lo, K-major
+        // rows; ebar and lse of each row kept for the epilogue
+#pragma unroll 1
+        for (int kb = 0; kb < C::ITEMS; kb += 4) {
+        uint2 pq[4];
+        float4 pm[4], pr[4];
+        float pe[4], pl[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            int rl;
+            size_t row;
+            pq[e] = make_uint2(0, 0);
+            pm[e] = pr[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            pe[e] = pl[e] = 0.f;
+            if (item_row(cur, kb + e, rl, row)) {
+                pq[e] = *(const uint2*)(q16 + row * D + 4 * qd);
+                pm[e] = *(const float4*)(mu_k + row * D + 4 * qd);
+                pr[e] = *(const float4*)(R + row * D + 4 * qd);
+                pe[e] = ebar[row];
+                if (qd == 0) pl[e] = lse[row];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            int rl;
+            size_t row;
+            const bool valid = item_row(cur, kb + e, rl, row);
+            const float m[4] = {pm[e].x, pm[e].y, pm[e].z, pm[e].w};
+            const float x[4] = {pr[e].x, pr[e].y, pr[e].z, pr[e].w};
+            const uint32_t qw[2] = {pq[e].x, pq[e].y};
+            uint32_t dh[2], dl[2], uh[2], ul[2];
+#pragma unroll
+            for (int w = 0; w < 2; w++) {
+                const float d0 = f16_lo(qw[w]) - m[2 * w];
+                const float d1 = f16_hi(qw[w]) - m[2 * w + 1];
+                dh[w] = pack_f16(d0, d1);
+                dl[w] = pack_f16(d0 - f16_lo(dh[w]), d1 - f16_hi(dh[w]));
+                const float u0 = x[2 * w] - pe[e] * m[2 * w];
+                const float u1 = x[2 * w + 1] - pe[e] * m[2 * w + 1];
+                uh[w] = pack_f16(u0, u1);
+                ul[w] = pack_f16(u0 - f16_lo(uh[w]), u1 - f16_hi(uh[w]));
+            }
+            if (!valid) dh[0] = dh[1] = dl[0] = dl[1] = uh[0] = uh[1] = ul[0] = ul[1] = 0u;
+            if (qd == 0) {
+                sEb[rl] = pe[e];
+                sL[rl] = pl[e];
+            }
+            const uint32_t off = sw_off(rl, (4 * qd) & ~7, C::BM) + ((qd & 1) << 3);
+            *(uint2*)(sDH + off) = make_uint2(dh[0], dh[1]);
+            *(uint2*)(sDL + off) = make_uint2(dl[0], dl[1]);
+            *(uint2*)(sUH + off) = make_uint2(uh[0], uh[1]);
+            *(uint2*)(sUL + off) = make_uint2(ul[0], ul[1]);
+        }
         }
         fence_proxy_async_smem();
         tc_fence_before();  // the previous tile's TMEM reads come before these MMAs
@@ -1817,7 +1883,7 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; kk++)
                     mma_ss(tDP, desc_mn_lbo(uh, kk, C::TB), desc_mnmajor(dh, C::BM, kk), idPd,
-                           (tile > 0 || kk > 0) ? 1u : 0u);
+                           (!chunk_first || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; kk++)
                     mma_ss(tDP, desc_mn_lbo(ul, kk, C::TB), desc_mnmajor(dh, C::BM, kk), idPd, 1u);
@@ -1828,84 +1894,106 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
             }
             __syncwarp();
         }
-        ok = __syncthreads_and(mbar_wait(&bars[0], tile & 1, wd, 1)) != 0;
+        ok = __syncthreads_and(mbar_wait(&bars[0], ntile & 1, wd, 1)) != 0;
         if (!ok) break;
         tc_fence_after();
-        // tcgen05.ld is warp-collective: every lane loads, only valid rows compute and store
-        float gr = 0.f, gb = 0.f, ru = 0.f, xx = 0.f;
+        // U and ddelta, one row per TMEM lane, to shared memory (the operand
+        // tiles were read by the completed products)
         {
             uint32_t vu[32], vd[32];
             tmem_ld32(tU + lrow + c0, vu);
             tmem_ld32(tDD + lrow + c0, vd);
             tmem_wait_ld();
-            if (valid) {
-                const float* mrow = mu_k + row * D + c0;
-                const float* rrow = R + row * D + c0;
-                uint32_t uhp[16], mh[16];
+            float* xu = sXU + rit * LDF + c0;
+            float* xd = sXD + rit * LDF + c0;
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const float4 m = *(const float4*)(mrow + 2 * i);
-                    const float4 x = *(const float4*)(rrow + 2 * i);
-                    const float u[4] = {__uint_as_float(vu[2 * i]), __uint_as_float(vu[2 * i + 1]),
-                                        __uint_as_float(vu[2 * i + 2]), __uint_as_float(vu[2 * i + 3])};
-                    const float dd[4] = {__uint_as_float(vd[2 * i]), __uint_as_float(vd[2 * i + 1]),
-                                         __uint_as_float(vd[2 * i + 2]), __uint_as_float(vd[2 * i + 3])};
-                    const float mm[4] = {m.x, m.y, m.z, m.w}, xr[4] = {x.x, x.y, x.z, x.w};
-                    uhp[i] = pack_f16(u[0], u[1]);
-                    uhp[i + 1] = pack_f16(u[2], u[3]);
-                    gr = fmaf(mm[0], f16_lo(uhp[i]), gr);
-                    gr = fmaf(mm[1], f16_hi(uhp[i]), gr);
-                    gr = fmaf(mm[2], f16_lo(uhp[i + 1]), gr);
-                    gr = fmaf(mm[3], f16_hi(uhp[i + 1]), gr);
+            for (int i = 0; i < 32; i += 4) {
+                *(uint4*)(xu + i) = make_uint4(vu[i], vu[i + 1], vu[i + 2], vu[i + 3]);
+                *(uint4*)(xd + i) = make_uint4(vd[i], vd[i + 1], vd[i + 2], vd[i + 3]);
+            }
+        }
+        // the chunk's dP_h partial: rows a = TMEM lanes 0..63 (quadrants 0
+        // and 1), columns split between the two halves
+        if (chunk_last && quad < 2) {
+            const int chunk = cur.item % nchunks;
+            float* dst = dp_partial + ((size_t)h * nchunks + chunk) * D * D + (size_t)rit * D + c0;
+            uint32_t v[32];
+            tmem_ld32(tDP + lrow + c0, v);
+            tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        gb = fmaf(mm[e], u[e], gb);
-                        ru = fmaf(xr[e], u[e], ru);
-                        xx = fmaf(mm[e], -dd[e], xx);
-                    }
-                    mh[i] = pack_f16(-dd[0], -dd[1]);
-                    mh[i + 1] = pack_f16(-dd[2], -dd[3]);
-                    *(float4*)(dq_acc + row * D + c0 + 2 * i) = make_float4(dd[0], dd[1], dd[2], dd[3]);
+            for (int i = 0; i < 32; i += 4)
+                *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
+        __syncthreads();
+        // per item: U (f16), dmu = -ddelta (f16), dq_acc = ddelta, and the row
+        // sums gr = mu_k . f16(U), gb = mu_k . U, ru = R . U, xx = -mu_k . ddelta
+#pragma unroll 2
+        for (int kb = 0; kb < C::ITEMS; kb += 4) {
+            float4 mv[4], rv[4];
+            bool valid[4];
+            int rl[4];
+            size_t row[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                valid[e] = item_row(cur, kb + e, rl[e], row[e]);
+                mv[e] = rv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (valid[e]) {
+                    mv[e] = *(const float4*)(mu_k + row[e] * D + 4 * qd);
+                    rv[e] = *(const float4*)(R + row[e] * D + 4 * qd);
                 }
-                uint4* ud = (uint4*)(U + row * D + c0);
-                uint4* md = (uint4*)(dmu + row * D + c0);
+            }
 #pragma unroll
-                for (int y = 0; y < 4; y++) {
-                    ud[y] = make_uint4(uhp[4 * y], uhp[4 * y + 1], uhp[4 * y + 2], uhp[4 * y + 3]);
-                    md[y] = make_uint4(mh[4 * y], mh[4 * y + 1], mh[4 * y + 2], mh[4 * y + 3]);
+            for (int e = 0; e < 4; e++) {
+                const float4 u4 = *(const float4*)(sXU + rl[e] * LDF + 4 * qd);
+                const float4 d4 = *(const float4*)(sXD + rl[e] * LDF + 4 * qd);
+                const uint32_t uh0 = pack_f16(u4.x, u4.y), uh1 = pack_f16(u4.z, u4.w);
+                float gr = mv[e].x * f16_lo(uh0);
+                gr = fmaf(mv[e].y, f16_hi(uh0), gr);
+                gr = fmaf(mv[e].z, f16_lo(uh1), gr);
+                gr = fmaf(mv[e].w, f16_hi(uh1), gr);
+                float gb = mv[e].x * u4.x;
+                gb = fmaf(mv[e].y, u4.y, gb);
+                gb = fmaf(mv[e].z, u4.z, gb);
+                gb = fmaf(mv[e].w, u4.w, gb);
+                float ru = rv[e].x * u4.x;
+                ru = fmaf(rv[e].y, u4.y, ru);
+                ru = fmaf(rv[e].z, u4.z, ru);
+                ru = fmaf(rv[e].w, u4.w, ru);
+                float xx = mv[e].x * -d4.x;
+                xx = fmaf(mv[e].y, -d4.y, xx);
+                xx = fmaf(mv[e].z, -d4.z, xx);
+                xx = fmaf(mv[e].w, -d4.w, xx);
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) {  // the row's sixteen threads (lanes 16-aligned)
+                    gr += __shfl_xor_sync(0xffffffffu, gr, o);
+                    gb += __shfl_xor_sync(0xffffffffu, gb, o);
+                    ru += __shfl_xor_sync(0xffffffffu, ru, o);
+                    xx += __shfl_xor_sync(0xffffffffu, xx, o);
+                }
+                if (valid[e]) {
+                    const size_t base = row[e] * D + 4 * qd;
+                    *(float4*)(dq_acc + base) = d4;
+                    *(uint2*)(U + base) = make_uint2(uh0, uh1);
+                    *(uint2*)(dmu + base) = make_uint2(pack_f16(-d4.x, -d4.y), pack_f16(-d4.z, -d4.w));
+                    if (qd == 0) {
+                        // paired row scalars {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o}
+                        const float eb = sEb[rl[e]];
+                        const float doo = eb + ru - gb * eb;
+                        const int r = cur.r0 + rl[e], tt = r % T, hp = tt & 1;
+                        float* prow = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + hp;
+                        prow[0] = -sL[rl[e]] * LOG2E;
+                        prow[2] = 1.f - gr;
+                        prow[4] = -eb;
+                        prow[6] = -(doo - gb * eb + xx);
+                    }
                 }
             }
         }
-        if (half == 1) sRed[rit] = make_float4(gr, gb, ru, xx);
-        __syncthreads();
-        if (half == 0 && valid) {
-            const float4 o = sRed[rit];
-            gr += o.x;
-            gb += o.y;
-            ru += o.z;
-            xx += o.w;
-            // paired row scalars {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o}
-            const float doo = eb + ru - gb * eb;
-            const int tt = r % T, hp = tt & 1;
-            float* pr = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + hp;
-            pr[0] = -lse[row] * LOG2E;
-            pr[2] = 1.f - gr;
-            pr[4] = -eb;
-            pr[6] = -(doo - gb * eb + xx);
-        }
-    }
-    // this CTA's dP_h partial: rows a = TMEM lanes 0..63 (quadrants 0 and 1),
-    // columns split between the two halves
-    if (ok && quad < 2) {
-        tc_fence_after();
-        float* dst = dp_partial + ((size_t)h * gridDim.x + blockIdx.x) * D * D + (size_t)rit * D + c0;
-        uint32_t v[32];
-        tmem_ld32(tDP + lrow + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-            *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        tc_fence_before();
+        __syncthreads();  // the fp32 tiles are read before the next tile's operands overwrite them
+        cur = next_tile(cur);
+        ntile++;
     }
     // teardown: every MMA issued must complete before the CTA releases TMEM
     if (warp == 0) {
@@ -2842,10 +2930,14 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         const int nchunks = (a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA;
         if (D == 64) {
             PLX_TRY(cudaFuncSetAttribute(tc_b2, cudaFuncAttributeMaxDynamicSharedMemorySize, B2T::SMEM));
+            int dev = 0, sms = 0;
+            PLX_TRY(cudaGetDevice(&dev));
+            PLX_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+            const int grid = std::min(2 * sms, nchunks * a.H);  // persistent: two CTAs per SM
             timing_begin(a.stream, "tc_bwd_b2");
-            tc_b2<<<dim3(nchunks, a.H), B2T::NT, B2T::SMEM, a.stream>>>(w.q16, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U,
-                                                                       w.dmu, w.dq_acc, w.rows, w.partial, a.B,
-                                                                       a.H, a.T, a.status);
+            tc_b2<<<grid, B2T::NT, B2T::SMEM, a.stream>>>(w.q16, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U, w.dmu,
+                                                          w.dq_acc, w.rows, w.partial, a.B, a.H, a.T, nchunks,
+                                                          a.status);
         } else {
             const size_t sm = R::smem(1);
             PLX_TRY(cudaFuncSetAttribute(tc_rows<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
