@@ -20,8 +20,9 @@
 //   dec1_chunk<D> : grid (chunks, B H), 128 threads (TPK = D/32 threads per
 //                   key, 32 features each), three CTAs per SM.  K and V tiles
 //                   of KT = 128 / TPK keys (8 KB each) arrive by TMA (128-byte
-//                   swizzle) in NS = 4 stages; thread 0 refills each stage two
-//                   tiles after its MMA was issued, so its wait is short.
+//                   swizzle) in NS = 4 stages; lane 0 of the last warp refills
+//                   each stage two tiles after its MMA was issued (so its wait
+//                   is short) while warp 0 issues the previous tile's MMA.
 //                   Per tile: scores, tile max (lazy rescale by 2^8), p, the
 //                   register sums, then p k and v are written back in place
 //                   as f16 and one thread issues M += V^T (p K) (A = V^T read
@@ -164,8 +165,11 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             tma_load_3d(sKV + (2 * s + 1) * C::TB + r * KT * 128, &tm_v, r * 64, k_begin + j * KT, bh, &full[s]);
         }
     };
-    int issued = 0;  // thread 0: tiles whose loads are issued
-    if (threadIdx.x == 0) {
+    // the loader is lane 0 of the last warp, so its refills overlap warp 0's
+    // MMA issue at the end of the previous tile
+    const bool loader = threadIdx.x == (NW - 1) * 32;
+    int issued = 0;  // loader: tiles whose loads are issued
+    if (loader) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         for (; issued < 2 && issued < nt; issued++) load_tile(issued);
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             // was issued two tiles ago, so the wait is short; tiles j, j + 1
             // and j + 2 are then loaded or in flight
             static_assert(NS == 4, "the refill distance assumes four stages");
-            if (threadIdx.x == 0 && ok && issued < nt && issued == j + 2) {
+            if (loader && ok && issued < nt && issued == j + 2) {
                 if (j < 2 || mbar_wait(&empty[(j - 2) % NS], ((j - 2) / NS) & 1, wd, 1)) {
                     load_tile(issued);
                     issued++;
@@ -324,9 +328,12 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
                 __syncwarp();
             }
         }
+        // the merge grid may now be scheduled (it waits for this grid's
+        // completion before it reads the partials)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // loads issued but not consumed (only after an abort) land before
         // stage 0 is reused below and before the CTA exits
-        if (threadIdx.x == 0)
+        if (loader)
             for (int jj = issued > NS ? issued - NS : 0; jj < issued; jj++) mbar_wait_drain(&full[jj % NS], (jj / NS) & 1);
         // ---- the chunk's partial (every worker agrees whether it is valid)
         ok = workers_and(ok, NW * 32);
@@ -406,9 +413,12 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
 // Merge the chunks of one head (only those holding keys of the sequence)
 // and finish the layer: lse, mu_k, mu_v, u = P_h (q - mu_k), gbar = mu_k . u,
 // o = mu_v + M u - gbar mu_v.  256 threads; the matrix-vector products (P_h
-// and each chunk's M) give four threads to a row (D/4 columns each) and
-// issue all their loads before using them, so each product is about one
-// memory latency.
+// and each chunk's M) give four threads to a row (D/4 columns each).  The
+// kernel is a chain of short dependent steps, so every load that does not
+// depend on an earlier step is issued at the start: this thread's P_h row
+// part, q, and its M row parts of the first kPre chunks (4 at d = 64, 1 at
+// d = 128, within the register budget), which then arrive
+// during the scalar steps instead of after them.
 constexpr int kMergeThreads = 256;
 
 template <int D>
@@ -420,19 +430,47 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
     using C = Dec1<D>;
     constexpr int NWM = kMergeThreads / 32;
     constexpr int RPP = kMergeThreads / 4;   // rows per pass, four threads per row
+    constexpr int NPASS = (D + RPP - 1) / RPP;
     constexpr int CQ = D / 4;                // columns per thread
-    __shared__ float s_d[D], s_mk[D], s_mv[D], s_u[D], s_red[NWM], s_w[2];
+    constexpr int kPre = D == 64 ? 4 : 1;    // chunks whose M rows are loaded up front
+    __shared__ float s_d[D], s_mk[D], s_mv[D], s_u[D], s_red[NWM], s_w[kPre];
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qr = tid & 3, rr = tid >> 2;   // column quarter, row within a pass
     const int len = seq_len1(lens, b, Lmax);
     const int nc = min(nchunk, (len + chunk - 1) / chunk);
     const float* pb = part + (size_t)bh * nchunk * C::PART;
+    // loads that depend on nothing computed here: P_h and q before the chunk
+    // kernel has finished (this grid may start early, as its programmatic
+    // dependent), the chunks' partials after
+    float4 pv[NPASS][CQ / 4], mpre[kPre][NPASS][CQ / 4];
+#pragma unroll
+    for (int ps = 0; ps < NPASS; ps++) {
+        const int a = ps * RPP + rr;
+#pragma unroll
+        for (int i = 0; i < CQ / 4; i++)
+            pv[ps][i] = a < D ? ((const float4*)(P + ((size_t)h * D + a) * D + qr * CQ))[i] : make_float4(0, 0, 0, 0);
+    }
+    const float qv = tid < D ? __bfloat162float(q[(size_t)bh * D + tid]) : 0.f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll
+    for (int ps = 0; ps < NPASS; ps++) {
+        const int a = ps * RPP + rr;
+#pragma unroll
+        for (int i = 0; i < CQ / 4; i++) {
+#pragma unroll
+            for (int c = 0; c < kPre; c++)
+                mpre[c][ps][i] = (a < D && c < nc)
+                                     ? ((const float4*)(pb + (size_t)c * C::PART + 4 + 2 * D + (size_t)a * D + qr * CQ))[i]
+                                     : make_float4(0, 0, 0, 0);
+        }
+    }
     float m = -INFINITY;
     for (int c = 0; c < nc; c++) m = fmaxf(m, pb[(size_t)c * C::PART]);
     float l = 0.f;
     for (int c = 0; c < nc; c++) l = fmaf(exp2f(pb[(size_t)c * C::PART] - m), pb[(size_t)c * C::PART + 1], l);
     const float inv = 1.f / l;
+    if (tid < kPre) s_w[tid] = tid < nc ? exp2f(pb[(size_t)tid * C::PART] - m) : 0.f;
     if (tid < D) {
         float mk = 0.f, mv = 0.f;
         for (int c = 0; c < nc; c++) {
@@ -443,23 +481,18 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
         }
         s_mk[tid] = mk * inv;
         s_mv[tid] = mv * inv;
-        s_d[tid] = __bfloat162float(q[(size_t)bh * D + tid]) - mk * inv;  // delta = q - mu_k
+        s_d[tid] = qv - mk * inv;  // delta = q - mu_k
     }
     __syncthreads();
     // u = P_h delta
-    for (int a0 = 0; a0 < D; a0 += RPP) {
-        const int a = a0 + rr;
+#pragma unroll
+    for (int ps = 0; ps < NPASS; ps++) {
+        const int a = ps * RPP + rr;
         float x = 0.f;
-        if (a < D) {
-            const float4* Pr = (const float4*)(P + ((size_t)h * D + a) * D + qr * CQ);
-            float4 pv[CQ / 4];
 #pragma unroll
-            for (int i = 0; i < CQ / 4; i++) pv[i] = Pr[i];
-#pragma unroll
-            for (int i = 0; i < CQ / 4; i++) {
-                const float* dd = s_d + qr * CQ + 4 * i;
-                x = fmaf(pv[i].x, dd[0], fmaf(pv[i].y, dd[1], fmaf(pv[i].z, dd[2], fmaf(pv[i].w, dd[3], x))));
-            }
+        for (int i = 0; i < CQ / 4; i++) {
+            const float* dd = s_d + qr * CQ + 4 * i;
+            x = fmaf(pv[ps][i].x, dd[0], fmaf(pv[ps][i].y, dd[1], fmaf(pv[ps][i].z, dd[2], fmaf(pv[ps][i].w, dd[3], x))));
         }
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
@@ -478,31 +511,42 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
 #pragma unroll
     for (int w = 0; w < NWM; w++) gbar += s_red[w];
     // o_e = mu_v,e + (sum_c w_c (M_c u)_e) / l - gbar mu_v,e
-    for (int e0 = 0; e0 < D; e0 += RPP) {
-        const int e = e0 + rr;
+#pragma unroll
+    for (int ps = 0; ps < NPASS; ps++) {
+        const int e = ps * RPP + rr;
         float x = 0.f;
-        if (e < D) {
-            for (int c = 0; c < nc; c++) {
-                const float* pc = pb + (size_t)c * C::PART;
+#pragma unroll
+        for (int c = 0; c < kPre; c++) {
+            float y = 0.f;
+#pragma unroll
+            for (int i = 0; i < CQ / 4; i++) {
+                const float* uu = s_u + qr * CQ + 4 * i;
+                const float4 mv4 = mpre[c][ps][i];
+                y = fmaf(mv4.x, uu[0], fmaf(mv4.y, uu[1], fmaf(mv4.z, uu[2], fmaf(mv4.w, uu[3], y))));
+            }
+            x = fmaf(s_w[c], y, x);
+        }
+        for (int c = kPre; c < nc; c++) {  // chunks beyond the first kPre, loaded here
+            const float* pc = pb + (size_t)c * C::PART;
+            float y = 0.f;
+            if (e < D) {
                 const float4* mr = (const float4*)(pc + 4 + 2 * D + (size_t)e * D + qr * CQ);
                 float4 mv4[CQ / 4];
 #pragma unroll
                 for (int i = 0; i < CQ / 4; i++) mv4[i] = mr[i];
-                float y = 0.f;
 #pragma unroll
                 for (int i = 0; i < CQ / 4; i++) {
                     const float* uu = s_u + qr * CQ + 4 * i;
                     y = fmaf(mv4[i].x, uu[0], fmaf(mv4[i].y, uu[1], fmaf(mv4[i].z, uu[2], fmaf(mv4[i].w, uu[3], y))));
                 }
-                x = fmaf(exp2f(pc[0] - m), y, x);
             }
+            x = fmaf(exp2f(pc[0] - m), y, x);
         }
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
         if (e < D && qr == 0) out[(size_t)bh * D + e] = __float2bfloat16_rn(s_mv[e] + x * inv - gbar * s_mv[e]);
     }
     if (tid == 0) lse[bh] = (m + __log2f(l)) * LN2;
-    (void)s_w;
 }
 
 // ----------------------------------------------------------------- host
@@ -576,8 +620,22 @@ cudaError_t decode_tc_impl(const DecodeArgs& a) {
     timing_end(a.stream);
     PLX_TRY(cudaGetLastError());
     timing_begin(a.stream, "dec_merge");
-    dec1_merge<D><<<BH, kMergeThreads, 0, a.stream>>>((const __nv_bfloat16*)a.q, a.lens, a.P, part, a.H, a.Lmax, chunk, nchunk,
-                                           a.lse, (__nv_bfloat16*)a.out);
+    {  // programmatic dependent launch: the merge's launch and its P_h and q
+       // loads overlap the chunk kernel's last CTAs
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(BH);
+        cfg.blockDim = dim3(kMergeThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = a.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        PLX_TRY(cudaLaunchKernelEx(&cfg, dec1_merge<D>, (const __nv_bfloat16*)a.q, (const int*)a.lens,
+                                   (const float*)a.P, (const float*)part, a.H, a.Lmax, chunk, nchunk, a.lse,
+                                   (__nv_bfloat16*)a.out));
+    }
     timing_end(a.stream);
     return cudaGetLastError();
 }
