@@ -69,16 +69,22 @@ def load_peaks():
 
 def measured_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu capture, or None
-    when there is none or the kernel source changed since it was taken."""
+    when there is none or the kernel's source changed since it was taken.  Each
+    entry names the source file and the two lines that bound the kernel's text;
+    the hash covers that text only, so editing another kernel of the same file
+    does not void it."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic_c4.json")
     try:
         with open(path) as f:
             doc = json.load(f)
-        with open(os.path.join(ROOT, doc["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != doc["source_sha256"]:
-                return None
         k = doc["kernels"][kernel]
+        with open(os.path.join(ROOT, k["source"])) as f:
+            src = f.read()
+        i0 = src.index(k["begin"])
+        i1 = src.index(k["end"], i0)
+        if hashlib.sha256(src[i0:i1].encode()).hexdigest() != k["sha256"]:
+            return None
         return k["read"] + k["write"]
     except (OSError, KeyError, ValueError):
         return None

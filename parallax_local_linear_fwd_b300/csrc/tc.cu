@@ -140,9 +140,10 @@ struct P1PP {
 template <int D>
 __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     tc_pass1_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_k16, const __nv_bfloat16* __restrict__ v_in,
-                const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ mu_k,
-                __half* __restrict__ U, float* __restrict__ gbar, __half* __restrict__ q16,
+                const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_mu,
+                const __grid_constant__ CUtensorMap tm_u, const __nv_bfloat16* __restrict__ v_in,
+                const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ gbar,
+                __half* __restrict__ q16,
                 __half* __restrict__ v16, int T, int H, int BH, int npairs, float scale_log2, unsigned* status) {
     using C = P1PP<D>;
     constexpr int NS = C::NS;
@@ -323,7 +324,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     } else if (warp >= 10) {
         // converters (warps 10-11): K tile j to f16 in place as soon as it
         // lands; P_h to f16 once the first stages are done (tile NS arrives
-        // only after tile 0's scores complete); then this pair's V rows
+        // only after tile 0's scores complete); then this pair's V rows,
+        // while the softmax warpgroups finish
         const int ct = threadIdx.x - 320;  // 0..63
         const int ph_at = min(nk, NS) - 1;
         bool ok = true;
@@ -376,11 +378,23 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             bulk_wait_all();
             if (ok) mbar_arrive(cdone);  // the K stages may now take delta
         }
-        if (ok) {  // V rows [q0a, q0a + 256) of head bh in f16
-            const int rows = min(2 * C::BM, T - q0a);
+        if (ok) {  // V rows [q0a, q0a + 256) of head bh in f16, eight 16-byte loads in flight per thread
+            const int c1 = min(2 * C::BM, T - q0a) * (D / 8);
             const uint4* src = (const uint4*)(v_in + ((size_t)bh * T + q0a) * D);
             uint4* dst = (uint4*)(v16 + ((size_t)bh * T + q0a) * D);
-            for (int c = ct; c < rows * (D / 8); c += 64) {
+            int c = ct;
+            for (; c + 7 * 64 < c1; c += 8 * 64) {
+                uint4 x[8];
+#pragma unroll
+                for (int u = 0; u < 8; u++) x[u] = src[c + u * 64];
+#pragma unroll
+                for (int u = 0; u < 8; u++)
+                    dst[c + u * 64] = make_uint4(pack_f16_sat(bf16_lo(x[u].x), bf16_hi(x[u].x)),
+                                                 pack_f16_sat(bf16_lo(x[u].y), bf16_hi(x[u].y)),
+                                                 pack_f16_sat(bf16_lo(x[u].z), bf16_hi(x[u].z)),
+                                                 pack_f16_sat(bf16_lo(x[u].w), bf16_hi(x[u].w)));
+            }
+            for (; c < c1; c += 64) {
                 const uint4 x = src[c];
                 dst[c] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
                                     pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
@@ -508,27 +522,22 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         // The four warps agree on ok before the projection (whose steps
         // synchronise on a named barrier): an abort anywhere skips it.
         ok = named_bar_and(1 + x, 128, ok);
+        // one thread of the warpgroup issues its tensor stores (mu_k, U)
+        const bool leader = qd == 0 && lane == 0;
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
             const size_t grow = (size_t)bh * T + t;
             uint8_t* sDhi = sK + (2 * x) * C::KB;
             uint8_t* sDlo = sK + (2 * x + 1) * C::KB;
-            // mu_k = Mu / l (output), delta = q - mu_k split into f16 hi + lo,
-            // written as the K-major A tile of the projection
+            // delta = q - mu_k (mu_k = Mu / l) split into f16 hi + lo, written
+            // as the K-major A tile of the projection; this thread's q row is
+            // read in full here, before its own mu_k row overwrites it below
 #pragma unroll 1
             for (int c = 0; c < D / 32; c++) {
                 uint32_t u[32];
                 tmem_ld32(tMu + lrow + c * 32, u);
                 tmem_wait_ld();
-                float mu[32];
-#pragma unroll
-                for (int i = 0; i < 32; i++) mu[i] = __uint_as_float(u[i]) * inv;
-                if (t < T) {
-                    float* dst = mu_k + grow * D + c * 32;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) *(float4*)(dst + i) = make_float4(mu[i], mu[i + 1], mu[i + 2], mu[i + 3]);
-                }
 #pragma unroll
                 for (int g = 0; g < 4; g++) {
                     const uint32_t off = sw_off(row, c * 32 + g * 8, C::BM);
@@ -537,8 +546,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
-                        const float d0 = f16_lo(qw[e]) - mu[g * 8 + 2 * e];
-                        const float d1 = f16_hi(qw[e]) - mu[g * 8 + 2 * e + 1];
+                        const float d0 = f16_lo(qw[e]) - __uint_as_float(u[g * 8 + 2 * e]) * inv;
+                        const float d1 = f16_hi(qw[e]) - __uint_as_float(u[g * 8 + 2 * e + 1]) * inv;
                         hi[e] = pack_f16(d0, d1);
                         lo[e] = pack_f16(d0 - f16_lo(hi[e]), d1 - f16_hi(hi[e]));
                     }
@@ -549,9 +558,49 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&proj_ready[x]);
+            // mu_k (output, fp32) through tile x's Q slot while the projection
+            // runs: 32-column boxes (128-byte swizzle), as many per round as
+            // the slot holds (D / 64), one tensor store per box; row t of a
+            // box lies in row t of the Q tile's own bytes, so each thread
+            // overwrites only its q row
+            constexpr int BPR = C::QB / (C::BM * 128);  // boxes per round
+            static_assert(BPR >= 1 && (D / 32) % BPR == 0, "the Q slot holds whole boxes");
+#pragma unroll 1
+            for (int r2 = 0; r2 < D / 32 / BPR; r2++) {
+                if (r2 > 0) {
+                    if (leader) bulk_wait_read_all();
+                    named_bar_sync(1 + x, 128);
+                }
+#pragma unroll 1
+                for (int b2 = 0; b2 < BPR; b2++) {
+                    uint32_t u[32];
+                    tmem_ld32(tMu + lrow + (r2 * BPR + b2) * 32, u);
+                    tmem_wait_ld();
+                    uint8_t* box = sQx + b2 * (C::BM * 128) + row * 128;
+#pragma unroll
+                    for (int y = 0; y < 8; y++)
+                        *(uint4*)(box + ((y ^ (row & 7)) << 4)) =
+                            make_uint4(__float_as_uint(__uint_as_float(u[4 * y]) * inv),
+                                       __float_as_uint(__uint_as_float(u[4 * y + 1]) * inv),
+                                       __float_as_uint(__uint_as_float(u[4 * y + 2]) * inv),
+                                       __float_as_uint(__uint_as_float(u[4 * y + 3]) * inv));
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + x, 128);
+                if (leader) {
+#pragma unroll
+                    for (int b2 = 0; b2 < BPR; b2++)
+                        tma_store_3d(&tm_mu, (r2 * BPR + b2) * 32, q0, bh, sQx + b2 * (C::BM * 128));
+                    bulk_commit();
+                }
+            }
             ok = mbar_wait(&proj_done[x], 0, wd, 12);
-            if (__all_sync(0xffffffffu, ok)) {
+            // the U stores below meet on the named barrier: agree first
+            ok = named_bar_and(1 + x, 128, ok);
+            if (ok) {
                 tc_fence_after();
+                if (leader) bulk_wait_read_all();  // the mu_k stores have read the Q slot
+                named_bar_sync(1 + x, 128);
                 float g = 0.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; c++) {
@@ -566,11 +615,18 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                         g = fmaf(__uint_as_float(vm[2 * i]) * inv, f16_lo(uh[i]), g);
                         g = fmaf(__uint_as_float(vm[2 * i + 1]) * inv, f16_hi(uh[i]), g);
                     }
-                    if (t < T) {
-                        uint4* dst = (uint4*)(U + grow * D + c * 32);
+                    // U (f16) in the Q tile's own layout, then one tensor store per 64 columns
 #pragma unroll
-                        for (int i = 0; i < 4; i++) dst[i] = make_uint4(uh[4 * i], uh[4 * i + 1], uh[4 * i + 2], uh[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 4; i++)
+                        *(uint4*)(sQx + sw_off(row, c * 32 + 8 * i, C::BM)) =
+                            make_uint4(uh[4 * i], uh[4 * i + 1], uh[4 * i + 2], uh[4 * i + 3]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + x, 128);
+                if (leader) {
+#pragma unroll
+                    for (int r = 0; r < D / 64; r++) tma_store_3d(&tm_u, r * 64, q0, bh, sQx + r * (C::BM * 128));
+                    bulk_commit();
                 }
                 if (t < T) {
                     lse[grow] = (m_use + __log2f(l)) * LN2;
@@ -578,6 +634,8 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                 }
             }
         }
+        // the tensor stores have read shared memory (and completed) before the CTA exits
+        if (leader) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -2809,6 +2867,19 @@ size_t tc_bwd_bytes(int B, int H, int T, int d) {
 
 // Row scalars: per head ceil(T/2) query pairs of 8 floats, viewed as 3-D
 // (8, pairs, BH) with a box of 8 x pairs_box x 1 (no swizzle).
+// fp32 [BH][T][D] in 32-column boxes of `rows` rows, 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, const void* base, int D, int T, int BH, int rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)T * D * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_rows_map(CUtensorMap* m, const void* base, int T, int BH, int pairs_box) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -2844,8 +2915,9 @@ cudaError_t fwd_impl(const FwdArgs& a) {
     TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
     // pass 1 reads the bf16 inputs (a 16-bit map copies the bytes as they
     // are) and writes the f16 copies of q, k, v that pass 2 reads
-    CUtensorMap mq_in, mk_in, mk16_128, mq128, mu128, mk64, mv64;
+    CUtensorMap mq_in, mk_in, mk16_128, mq128, mu128, mk64, mv64, mmu;
     if (!make_map(&mq_in, a.q, D, a.T, BH, 128) || !make_map(&mk_in, a.k, D, a.T, BH, 128) ||
+        !make_map_f32(&mmu, a.mu_k, D, a.T, BH, 128) ||
         !make_map(&mk16_128, w.k16, D, a.T, BH, 128) || !make_map(&mq128, w.q16, D, a.T, BH, 128) ||
         !make_map(&mu128, w.U, D, a.T, BH, 128) || !make_map(&mk64, w.k16, D, a.T, BH, 64) ||
         !make_map(&mv64, w.v16, D, a.T, BH, 64))
@@ -2857,7 +2929,7 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         PLX_TRY(cudaFuncSetAttribute(tc_pass1_pp<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass1");
         tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(
-            mq_in, mk_in, mk16_128, (const __nv_bfloat16*)a.v, a.P, a.lse, a.mu_k, w.U, w.gbar, w.q16, w.v16, a.T,
+            mq_in, mk_in, mk16_128, mmu, mu128, (const __nv_bfloat16*)a.v, a.P, a.lse, w.gbar, w.q16, w.v16, a.T,
             a.H, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
@@ -2958,17 +3030,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     if (D == 64) {  // B3: dK, dV, dQ (ping-pong form)
         using C = B3P;
         CUtensorMap mq32, mu32, mdmu32, mdo32, mrows32, mdq;
-        {
-            EncodeTiledFn fn = encode_fn();
-            cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.T, (cuuint64_t)BH};
-            cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)a.T * D * 4};
-            cuuint32_t box[3] = {32, (cuuint32_t)C::QT, 1};
-            cuuint32_t es[3] = {1, 1, 1};
-            if (!fn || fn(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, w.dq_acc, dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                return cudaErrorInvalidValue;
-        }
+        if (!make_map_f32(&mdq, w.dq_acc, D, a.T, BH, C::QT)) return cudaErrorInvalidValue;
         if (!make_map(&mq32, w.q16, D, a.T, BH, 32) || !make_map(&mu32, w.U, D, a.T, BH, 32) ||
             !make_map(&mdmu32, w.dmu, D, a.T, BH, 32) || !make_map(&mdo32, w.do16, D, a.T, BH, 32) ||
             !make_rows_map(&mrows32, w.rows, a.T, BH, 16))
