@@ -129,8 +129,8 @@ struct P1PP {
     static constexpr int KB = BN * D * 2;
     static constexpr int PB = D * D * 2;  // P_h in f16
     // q_full, k_full[NS], k_empty[NS], k16[NS], q16[2], s_full[2], p_full[2],
-    // o_done[2], kfree, cdone, ph_full, proj_ready[2], proj_done[2], drain
-    static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 2 + 1;
+    // o_done[2], kfree, cdone, ph_full, proj_ready[2], proj_done[2], drain, v_full
+    static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 2 + 2 + 1 + 1;
     static constexpr int SMEM = 1024 + 2 * QB + NS * KB + PB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 512;
     static_assert(NS >= 4 && KB == QB, "the projection of each tile takes two K stages");
@@ -141,10 +141,10 @@ template <int D>
 __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     tc_pass1_pp(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_k16, const __grid_constant__ CUtensorMap tm_mu,
-                const __grid_constant__ CUtensorMap tm_u, const __nv_bfloat16* __restrict__ v_in,
+                const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_q16,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v16,
                 const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ gbar,
-                __half* __restrict__ q16,
-                __half* __restrict__ v16, int T, int H, int BH, int npairs, float scale_log2, unsigned* status) {
+                int T, int H, int BH, int npairs, float scale_log2, unsigned* status) {
     using C = P1PP<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     uint64_t* proj_ready = ph_full + 1;  // [2] delta_x staged
     uint64_t* proj_done = proj_ready + 2;  // [2] U_x in TMEM
     uint64_t* drain = proj_done + 2;
+    uint64_t* v_full = drain + 1;        // the pair's V rows (bf16) are in K stages 0-1 (one phase)
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         mbar_init(cdone, 1);
         mbar_init(ph_full, 1);
         mbar_init(drain, 1);
+        mbar_init(v_full, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
@@ -378,28 +380,44 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             bulk_wait_all();
             if (ok) mbar_arrive(cdone);  // the K stages may now take delta
         }
-        if (ok) {  // V rows [q0a, q0a + 256) of head bh in f16, eight 16-byte loads in flight per thread
-            const int c1 = min(2 * C::BM, T - q0a) * (D / 8);
-            const uint4* src = (const uint4*)(v_in + ((size_t)bh * T + q0a) * D);
-            uint4* dst = (uint4*)(v16 + ((size_t)bh * T + q0a) * D);
-            int c = ct;
-            for (; c + 7 * 64 < c1; c += 8 * 64) {
-                uint4 x[8];
+        // V rows [q0a, q0a + 256) of head bh in f16, through K stages 0-1 once
+        // both projections have read their delta tiles there: one tensor load
+        // per 128 x 64 box, conversion in place, one tensor store per box
+        if (ok) ok = mbar_wait(&proj_done[0], 0, wd, 16);
+        if (ok && ntiles > 1) ok = mbar_wait(&proj_done[1], 0, wd, 16);
+        ok = named_bar_and(3, 64, ok);
+        if (ok) {
+            const int vt = min(2, (T - q0a + C::BM - 1) / C::BM);  // 128-row V tiles of this pair
+            if (ct == 0) {
+                mbar_expect_tx(v_full, vt * C::KB);
+                for (int rt = 0; rt < vt; rt++)
 #pragma unroll
-                for (int u = 0; u < 8; u++) x[u] = src[c + u * 64];
-#pragma unroll
-                for (int u = 0; u < 8; u++)
-                    dst[c + u * 64] = make_uint4(pack_f16_sat(bf16_lo(x[u].x), bf16_hi(x[u].x)),
-                                                 pack_f16_sat(bf16_lo(x[u].y), bf16_hi(x[u].y)),
-                                                 pack_f16_sat(bf16_lo(x[u].z), bf16_hi(x[u].z)),
-                                                 pack_f16_sat(bf16_lo(x[u].w), bf16_hi(x[u].w)));
+                    for (int r = 0; r < D / 64; r++)
+                        tma_load_3d(sK + rt * C::KB + r * C::BN * 128, &tm_v, r * 64, q0a + rt * C::BM, bh, v_full);
             }
-            for (; c < c1; c += 64) {
-                const uint4 x = src[c];
-                dst[c] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
-                                    pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
+            ok = named_bar_and(3, 64, mbar_wait(v_full, 0, wd, 17));
+            if (ok) {
+                uint4* tile = (uint4*)sK;
+#pragma unroll 4
+                for (int c = ct; c < vt * C::KB / 16; c += 64) {
+                    const uint4 x = tile[c];
+                    tile[c] = make_uint4(pack_f16_sat(bf16_lo(x.x), bf16_hi(x.x)), pack_f16_sat(bf16_lo(x.y), bf16_hi(x.y)),
+                                         pack_f16_sat(bf16_lo(x.z), bf16_hi(x.z)), pack_f16_sat(bf16_lo(x.w), bf16_hi(x.w)));
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(3, 64);
+                if (ct == 0) {
+                    for (int rt = 0; rt < vt; rt++)
+#pragma unroll
+                        for (int r = 0; r < D / 64; r++)
+                            tma_store_3d(&tm_v16, r * 64, q0a + rt * C::BM, bh, sK + rt * C::KB + r * C::BN * 128);
+                    bulk_commit();
+                }
+            } else if (ct == 0) {
+                mbar_wait_drain(v_full, 0);  // the loads land before the CTA exits
             }
         }
+        if (ct == 0) bulk_wait_all();
     } else if (warp >= 2) {
         // softmax / epilogue warpgroup x: thread <-> query row (TMEM lane)
         const int x = (warp - 2) >> 2;
@@ -414,11 +432,9 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
         float m_use = -INFINITY, l = 0.f;
         bool ok = my_nkt > 0;
         if (ok) {
-            // this thread's q row to f16: in place in the Q tile (the MMA
-            // operand) and in the copy pass 2 reads
+            // this thread's q row to f16, in place in the Q tile (the MMA operand)
             ok = mbar_wait(q_full, 0, wd, 14);
             if (__all_sync(0xffffffffu, ok)) {
-                const size_t grow = (size_t)bh * T + t;
 #pragma unroll 4
                 for (int c = 0; c < D / 8; c++) {
                     const uint32_t off = sw_off(row, 8 * c, C::BM);
@@ -428,10 +444,16 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                                                 pack_f16_sat(bf16_lo(x8.z), bf16_hi(x8.z)),
                                                 pack_f16_sat(bf16_lo(x8.w), bf16_hi(x8.w)));
                     *(uint4*)(sQx + off) = h8;
-                    if (t < T) *(uint4*)(q16 + grow * D + 8 * c) = h8;
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&q16r[x]);
+                // the f16 tile, once all its rows are converted, to the copy
+                // pass 2 reads: one tensor store per 64 columns
+                if (qd == 0 && lane == 0 && mbar_wait(&q16r[x], 0, wd, 18)) {
+#pragma unroll
+                    for (int r = 0; r < D / 64; r++) tma_store_3d(&tm_q16, r * 64, q0, bh, sQx + r * (C::BM * 128));
+                    bulk_commit();
+                }
             } else {
                 ok = false;
             }
@@ -567,10 +589,10 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
             static_assert(BPR >= 1 && (D / 32) % BPR == 0, "the Q slot holds whole boxes");
 #pragma unroll 1
             for (int r2 = 0; r2 < D / 32 / BPR; r2++) {
-                if (r2 > 0) {
-                    if (leader) bulk_wait_read_all();
-                    named_bar_sync(1 + x, 128);
-                }
+                // the previous tensor store from the slot (the f16 q copy, then
+                // the previous round) has read it
+                if (leader) bulk_wait_read_all();
+                named_bar_sync(1 + x, 128);
 #pragma unroll 1
                 for (int b2 = 0; b2 < BPR; b2++) {
                     uint32_t u[32];
@@ -2915,8 +2937,9 @@ cudaError_t fwd_impl(const FwdArgs& a) {
     TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
     // pass 1 reads the bf16 inputs (a 16-bit map copies the bytes as they
     // are) and writes the f16 copies of q, k, v that pass 2 reads
-    CUtensorMap mq_in, mk_in, mk16_128, mq128, mu128, mk64, mv64, mmu;
+    CUtensorMap mq_in, mk_in, mv_in, mk16_128, mv16_128, mq128, mu128, mk64, mv64, mmu;
     if (!make_map(&mq_in, a.q, D, a.T, BH, 128) || !make_map(&mk_in, a.k, D, a.T, BH, 128) ||
+        !make_map(&mv_in, a.v, D, a.T, BH, 128) || !make_map(&mv16_128, w.v16, D, a.T, BH, 128) ||
         !make_map_f32(&mmu, a.mu_k, D, a.T, BH, 128) ||
         !make_map(&mk16_128, w.k16, D, a.T, BH, 128) || !make_map(&mq128, w.q16, D, a.T, BH, 128) ||
         !make_map(&mu128, w.U, D, a.T, BH, 128) || !make_map(&mk64, w.k16, D, a.T, BH, 64) ||
@@ -2929,7 +2952,7 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         PLX_TRY(cudaFuncSetAttribute(tc_pass1_pp<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass1");
         tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(
-            mq_in, mk_in, mk16_128, mmu, mu128, (const __nv_bfloat16*)a.v, a.P, a.lse, w.gbar, w.q16, w.v16, a.T,
+            mq_in, mk_in, mk16_128, mmu, mu128, mq128, mv_in, mv16_128, a.P, a.lse, w.gbar, a.T,
             a.H, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
