@@ -686,6 +686,52 @@ __global__ void __launch_bounds__(256) tc_to_f16(CvtJob job, size_t n8) {
     }
 }
 
+// The dual-score pass's accumulator to global memory through shared memory,
+// by the four-warp group that owns TMEM lanes 0-127 (thread = row): MODE 0
+// writes out (bf16) in the A1 slot's 16-bit tile layout, MODE 1 writes R
+// (fp32) in 32-column boxes (128-byte swizzle) over the A1 and A2 slots, which
+// lie back to back; both slots are free once the accumulation has completed.
+// The group meets on named barrier `bar`, then `leader` issues one tensor
+// store per box (rows past T are not written).
+template <int D, int MODE>
+__device__ __forceinline__ void dual_store_acc(uint32_t tAcc, uint32_t lrow, int row, uint8_t* slot, int bar,
+                                               bool leader, const CUtensorMap* tm_out, int q0, int bh) {
+    constexpr int BM = 128;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; c++) {
+        uint32_t v[32];
+        tmem_ld32(tAcc + lrow + c * 32, v);
+        tmem_wait_ld();
+        if (MODE == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                *(uint4*)(slot + sw_off(row, c * 32 + 8 * i, BM)) =
+                    make_uint4(pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                               pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                               pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                               pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+        } else {
+            uint8_t* box = slot + c * (BM * 128) + row * 128;
+#pragma unroll
+            for (int y = 0; y < 8; y++)
+                *(uint4*)(box + ((y ^ (row & 7)) << 4)) = make_uint4(v[4 * y], v[4 * y + 1], v[4 * y + 2], v[4 * y + 3]);
+        }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(bar, 128);
+    if (leader) {
+        if (MODE == 0) {
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) tma_store_3d(tm_out, r * 64, q0, bh, slot + r * (BM * 128));
+        } else {
+#pragma unroll
+            for (int c = 0; c < D / 32; c++) tma_store_3d(tm_out, c * 32, q0, bh, slot + c * (BM * 128));
+        }
+        bulk_commit();
+        bulk_wait_all();  // the slot stays valid until the stores have read it
+    }
+}
+
 // ======================================================== dual-score pass
 // MODE 0 (forward pass 2): X = U K^T, W = p (x + 1 - gbar), Acc += W V, out = Acc.
 // MODE 1 (backward B1)   : X = dO V^T, W = p x,           Acc += W K, R = Acc,
@@ -705,8 +751,9 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 2)
     tc_dual(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-            const float* __restrict__ lse, const float* __restrict__ gbar, void* __restrict__ acc_out,
-            float* __restrict__ ebar_out, int T, int BH, int ntq, float scale_log2, unsigned* status) {
+            const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
+            const float* __restrict__ gbar, float* __restrict__ ebar_out, int T, int BH, int ntq, float scale_log2,
+            unsigned* status) {
     using C = DualCfg<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -875,35 +922,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             tc_fence_before();
             mbar_arrive(w_full);
         }
+        if (ok) ok = mbar_wait(acc_done, 0, wd, 8);
+        // the group meets on a named barrier in the store below: agree first
+        ok = named_bar_and(1, 128, ok);
         if (ok) {
-            ok = mbar_wait(acc_done, 0, wd, 8);
-            if (__all_sync(0xffffffffu, ok)) {
+            {
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(tAcc + lrow + c * 32, v);
-                    tmem_wait_ld();
-                    if (valid) {
-                        const size_t off = ((size_t)bh * T + t) * D + c * 32;
-                        if (MODE == 0) {
-                            uint4* dst = (uint4*)((__nv_bfloat16*)acc_out + off);
-#pragma unroll
-                            for (int i = 0; i < 4; i++)
-                                dst[i] = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
-                        } else {
-                            float* dst = (float*)acc_out + off;
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                        }
-                    }
-                }
+                dual_store_acc<D, MODE>(tAcc, lrow, row, sA1, 1, qd == 0 && lane == 0, &tm_out, q0, bh);
                 if (MODE == 1 && valid) {
                     const float2 r2 = uf2(rs2);
                     ebar_out[(size_t)bh * T + t] = r2.x + r2.y;
@@ -948,8 +973,9 @@ template <int D, int MODE>
 __global__ void __launch_bounds__(DualPP<D>::NT, 1)
     tc_dual_pp(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-               const float* __restrict__ lse, const float* __restrict__ gbar, void* __restrict__ acc_out,
-               float* __restrict__ ebar_out, int T, int BH, int npairs, float scale_log2, unsigned* status) {
+               const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
+               const float* __restrict__ gbar, float* __restrict__ ebar_out, int T, int BH, int npairs,
+               float scale_log2, unsigned* status) {
     using C = DualPP<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -1150,35 +1176,15 @@ __global__ void __launch_bounds__(DualPP<D>::NT, 1)
             tc_fence_before();
             mbar_arrive(&w_full[x]);
         }
+        if (ok) ok = mbar_wait(&acc_done[x], 0, wd, 8);
+        // the group meets on a named barrier in the store below: agree first
+        // (a group whose tile lies past T has no work and takes no part)
+        if (my_nkt > 0) ok = named_bar_and(1 + x, 128, ok);
         if (ok) {
-            ok = mbar_wait(&acc_done[x], 0, wd, 8);
-            if (__all_sync(0xffffffffu, ok)) {
+            {
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(tAcc + lrow + c * 32, v);
-                    tmem_wait_ld();
-                    if (valid) {
-                        const size_t off = ((size_t)bh * T + t) * D + c * 32;
-                        if (MODE == 0) {
-                            uint4* dst = (uint4*)((__nv_bfloat16*)acc_out + off);
-#pragma unroll
-                            for (int i = 0; i < 4; i++)
-                                dst[i] = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
-                        } else {
-                            float* dst = (float*)acc_out + off;
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *(float4*)(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                                  __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                        }
-                    }
-                }
+                dual_store_acc<D, MODE>(tAcc, lrow, row, sA + (2 * x) * C::AB, 1 + x, qd == 0 && lane == 0, &tm_out,
+                                        q0, bh);
                 if (MODE == 1 && valid) {
                     const float2 r2 = uf2(rs2);
                     ebar_out[(size_t)bh * T + t] = r2.x + r2.y;
@@ -2937,8 +2943,9 @@ cudaError_t fwd_impl(const FwdArgs& a) {
     TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
     // pass 1 reads the bf16 inputs (a 16-bit map copies the bytes as they
     // are) and writes the f16 copies of q, k, v that pass 2 reads
-    CUtensorMap mq_in, mk_in, mv_in, mk16_128, mv16_128, mq128, mu128, mk64, mv64, mmu;
+    CUtensorMap mq_in, mk_in, mv_in, mk16_128, mv16_128, mq128, mu128, mk64, mv64, mmu, mout;
     if (!make_map(&mq_in, a.q, D, a.T, BH, 128) || !make_map(&mk_in, a.k, D, a.T, BH, 128) ||
+        !make_map(&mout, a.out, D, a.T, BH, 128) ||
         !make_map(&mv_in, a.v, D, a.T, BH, 128) || !make_map(&mv16_128, w.v16, D, a.T, BH, 128) ||
         !make_map_f32(&mmu, a.mu_k, D, a.T, BH, 128) ||
         !make_map(&mk16_128, w.k16, D, a.T, BH, 128) || !make_map(&mq128, w.q16, D, a.T, BH, 128) ||
@@ -2962,9 +2969,8 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
         PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual_pp<D, 0><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, a.lse, w.gbar,
-                                                                     a.out, nullptr, a.T, BH, npairs, scale_log2,
-                                                                     a.status);
+        tc_dual_pp<D, 0><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, mout, a.lse, w.gbar,
+                                                                     nullptr, a.T, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // pass 2
@@ -2972,7 +2978,7 @@ cudaError_t fwd_impl(const FwdArgs& a) {
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual<D, 0><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, a.lse, w.gbar, a.out,
+        tc_dual<D, 0><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, mout, a.lse, w.gbar,
                                                                   nullptr, a.T, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
@@ -2987,8 +2993,9 @@ cudaError_t bwd_impl(const BwdArgs& a) {
     const float scale_log2 = LOG2E * scale;
     const size_t n = (size_t)BH * a.T * D;
     TcBwdWs w = tc_bwd_ws(a.ws, a.B, a.H, a.T, D);
-    CUtensorMap mq128, mdo128, mk64, mv64, mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows;
+    CUtensorMap mq128, mdo128, mk64, mv64, mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows, mR;
     if (!make_map(&mq128, w.q16, D, a.T, BH, 128) || !make_map(&mdo128, w.do16, D, a.T, BH, 128) ||
+        !make_map_f32(&mR, w.R, D, a.T, BH, 128) ||
         !make_map(&mk64, w.k16, D, a.T, BH, 64) || !make_map(&mv64, w.v16, D, a.T, BH, 64) ||
         !make_map(&mk128, w.k16, D, a.T, BH, 128) || !make_map(&mv128, w.v16, D, a.T, BH, 128) ||
         !make_map(&mq64, w.q16, D, a.T, BH, 64) || !make_map(&mu64, w.U, D, a.T, BH, 64) ||
@@ -3005,9 +3012,8 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
         PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b1");
-        tc_dual_pp<D, 1><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr,
-                                                                     w.R, w.ebar, a.T, BH, npairs, scale_log2,
-                                                                     a.status);
+        tc_dual_pp<D, 1><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, mR, a.lse, nullptr,
+                                                                     w.ebar, a.T, BH, npairs, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // B1: R = sum p e k, ebar = sum p e
@@ -3015,7 +3021,7 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b1");
-        tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, a.lse, nullptr, w.R,
+        tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, mR, a.lse, nullptr,
                                                                   w.ebar, a.T, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
