@@ -2463,7 +2463,8 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
 // E^T [96,128); dV [256,320), dK [320,384), dQ [384,448).
 struct B3P {
     static constexpr int D = 64, BK = 128, BQ = 32, QT = 128, NT = 320;
-    static constexpr int NS = 4;                   // operand stages
+    static constexpr int NS = 5;                   // operand stages (sub-chunk j in slot j % NS), loaded in pairs
+    static constexpr int NPB = 3;                  // pair barriers: at most three pairs are in flight
     static constexpr int KB = BK * D * 2;          // K or V tile
     static constexpr int SUB = BQ * 128;           // one 32-row operand tile
     static constexpr int DO_OFF = 3 * SUB;         // after the stacked [Q|U|dmu]
@@ -2551,12 +2552,12 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             mbar_expect_tx(kv_full, 2 * C::KB);
             tma_load_3d(sK, &tm_k, 0, k0, bh, kv_full);
             tma_load_3d(sV, &tm_v, 0, k0, bh, kv_full);
-            // sub-chunks load in pairs (2p, 2p + 1) onto one barrier, st_full[p & 1],
-            // so the MMA warp waits once per pair
+            // sub-chunks load in pairs (2p, 2p + 1) onto one barrier,
+            // st_full[p % NPB], so the MMA warp waits once per pair
             int issued = 0;
             for (int j = 0; j < nsub; j += 2) {
                 const int n2 = nsub - j < 2 ? nsub - j : 2;
-                uint64_t* bar = &st_full[(j >> 1) & 1];
+                uint64_t* bar = &st_full[(j >> 1) % C::NPB];
                 bool free_ok = true;
                 for (int e = 0; e < n2 && free_ok; e++) {
                     const int jj = j + e;
@@ -2576,9 +2577,10 @@ __global__ void __launch_bounds__(B3P::NT, 1)
                 issued = j + n2;
             }
             mbar_wait_drain(kv_full, 0);
-            // loads can be in flight for the last two pairs only (four slots)
+            // loads can be in flight for the last NPB pairs only (NS slots)
             const int npairs = (issued + 1) / 2;
-            for (int pq = npairs > 2 ? npairs - 2 : 0; pq < npairs; pq++) mbar_wait_drain(&st_full[pq & 1], (pq >> 1) & 1);
+            for (int pq = npairs > C::NPB ? npairs - C::NPB : 0; pq < npairs; pq++)
+                mbar_wait_drain(&st_full[pq % C::NPB], (pq / C::NPB) & 1);
         }
     } else if (warp == 1) {
         // The whole warp runs the loop, so the descriptors stay warp-uniform;
@@ -2594,7 +2596,8 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             if (j < nsub) {
                 const int s = j % NS, b = j & 1;
                 // the pair (j, j + 1) arrives on one barrier: wait at even j only
-                if ((j & 1) == 0 && !__all_sync(0xffffffffu, mbar_wait(&st_full[(j >> 1) & 1], (j >> 2) & 1, wd, 3)))
+                if ((j & 1) == 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait(&st_full[(j >> 1) % C::NPB], ((j >> 1) / C::NPB) & 1, wd, 3)))
                     break;
                 // buffer b's weight operands were read by the accumulation of j - 2,
                 // issued earlier by this thread: MMAs execute in issue order
@@ -2702,6 +2705,9 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             return __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
         };
         bool ok = true;
+        // warpgroup 1 reads dQ tile m after its next sub-chunk (4 m + 5), by
+        // when the dQ product has completed, instead of waiting for it
+        int pend = -1;
         for (int j = wg; j < nsub && ok; j += 2) {
             const int s = j % NS, m = j >> 2, x = m & 1;
             const int t0 = k0 + j * C::BQ;
@@ -2760,9 +2766,16 @@ __global__ void __launch_bounds__(B3P::NT, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&op_full[wg]);
-            if (wg == 1 && (j & 3) == 3) ok = read_dq(m);
+            if (wg == 1) {
+                if (pend >= 0) {
+                    ok = read_dq(pend);
+                    pend = -1;
+                }
+                if ((j & 3) == 3) pend = m;
+            }
         }
         // warpgroup 1 reads every dQ tile in order; the last one may be partial
+        if (ok && wg == 1 && pend >= 0) ok = read_dq(pend);
         if (ok && wg == 1 && ((nsub - 1) & 3) != 3) ok = read_dq((nsub - 1) >> 2);
         if (wg == 1 && warp == 6 && lane == 0) bulk_wait_all();  // staging must outlive its reduces
         if (ok) {
