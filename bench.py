@@ -438,6 +438,8 @@ def run_ours(args, world, rank):
     }
     if rank == 0 and world == 1 and not args.no_fwd_c3:
         line["decode"] = decode_workload(torch, plx, k, v, P, stream)
+        if k.dtype == torch.bfloat16:
+            line["decode_probe"] = decode_workload(torch, plx, k, v, P, stream, probe=True)
     if rank == 0 and world == 1 and path == "tc" and not args.no_fwd_c3:
         line["fwd_c3"] = forward_workload(torch, plx, "c3", dev, stream)
         line["fwd_probe_c3"] = probe_workload(torch, plx, "c3", dev, stream)
@@ -519,28 +521,36 @@ def forward_workload(torch, plx, name, dev, stream, iters=10, warmup=3):
     return res
 
 
-def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3):
+def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3, probe=False):
     """Decode step over the step's own keys and values as a KV cache (one new
     query per head, every sequence at full length).  HBM-bound: the roofline
     is the measured copy bandwidth; the algorithmic bytes are the cache (K and
-    V read once each), although the kernels read K twice."""
+    V read once each).  probe=True times the given-probe form
+    (parallax_decode_probe, a probe rho per head) instead of the projector's."""
     B, H, L, d = (int(x) for x in k.shape)
     gen = torch.Generator(device="cpu").manual_seed(17)
     q = torch.randn((B, H, d), generator=gen).to(k.dtype).to(k.device)
+    rho = (0.3 * torch.randn((B, H, d), generator=gen)).to(k.dtype).to(k.device)
     out = torch.empty_like(q)
     lse = torch.empty((B, H), dtype=torch.float32, device=k.device)
     dtc = plx.PLX_BF16 if k.dtype == torch.bfloat16 else plx.PLX_FP32
-    ws = torch.empty(max(256, plx.parallax_decode_workspace_bytes(B, H, L, d, dtc)), dtype=torch.uint8,
-                     device=k.device)
+    wsb = (plx.parallax_decode_probe_workspace_bytes if probe else plx.parallax_decode_workspace_bytes)(B, H, L, d, dtc)
+    ws = torch.empty(max(256, wsb), dtype=torch.uint8, device=k.device)
+
+    def call(st):
+        if probe:
+            plx.parallax_decode_probe(q, k, v, rho, out=out, lse=lse, workspace=ws, stream=st)
+        else:
+            plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=st)
     for _ in range(warmup):
-        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=stream)
+        call(stream)
     # timed without the library's per-kernel events: at this microsecond
     # scale their host work per launch would be measured too
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(iters):
-        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=stream)
+        call(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_eager = e0.elapsed_time(e1) / iters
@@ -550,7 +560,7 @@ def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3):
     cs.wait_stream(stream)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cs):
-        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=cs)
+        call(cs)
     for _ in range(warmup):
         graph.replay()
     # the cache (2 x 67 MB) barely exceeds L2 (126 MB): every timed replay
@@ -572,15 +582,16 @@ def decode_workload(torch, plx, k, v, P, stream, iters=20, warmup=3):
     plx.parallax_timing_reset()
     plx.parallax_timing_enable(True)
     for _ in range(iters):
-        plx.parallax_decode(q, k, v, P, out=out, lse=lse, workspace=ws, stream=stream)
+        call(stream)
     torch.cuda.synchronize()
     plx.parallax_timing_enable(False)
     kt = plx.kernel_times()
     cache_bytes = 2 * k.numel() * k.element_size()
     peaks = load_peaks()
     gbs = cache_bytes / (ms / 1e3) / 1e9
+    form = "given probe rho per head" if probe else "probe formed by the projector P_h"
     return {"workload": f"decode, {str(k.dtype).replace('torch.', '')}, B{B} H{H} cache {L} d{d}, "
-                        "one new query per head", "us": ms * 1e3, "timing": "CUDA-graph replay of the call, L2 flushed before each",
+                        f"one new query per head, {form}", "us": ms * 1e3, "timing": "CUDA-graph replay of the call, L2 flushed before each",
             "us_eager": ms_eager * 1e3, "tokens_per_s": B / (ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": cache_bytes,
@@ -706,7 +717,8 @@ def run_case(args):
         inp = plx_synth.generate_workload("c4")
         k, v, P = (torch.from_numpy(inp[x].view(np.int16)).view(torch.bfloat16).to(dev) if inp[x].dtype == np.uint16
                    else torch.from_numpy(inp[x]).to(dev) for x in ("k", "v", "P"))
-        res = decode_workload(torch, plx, k, v, P, stream, iters=args.steps, warmup=args.warmup)
+        res = decode_workload(torch, plx, k, v, P, stream, iters=args.steps, warmup=args.warmup,
+                              probe=args.case == "decode_probe")
     code, detail = plx.parallax_last_device_error(stream)
     if code != plx.PLX_OK:
         raise RuntimeError(f"device watchdog: {plx.parallax_strerror(code)} detail={detail:#x}")
@@ -726,7 +738,7 @@ def main(argv=None):
     ap.add_argument("--shard", default="heads", choices=["heads", "batch"],
                     help="heads: every rank runs its own independent set of heads (no collective); batch: "
                          "the ranks split one problem's batch and all-reduce dP_h each step")
-    ap.add_argument("--case", default="step", choices=["step", "fwd_c3", "probe_c3", "decode"],
+    ap.add_argument("--case", default="step", choices=["step", "fwd_c3", "probe_c3", "decode", "decode_probe"],
                     help="step: the benchmark (default). The others run one of the extra workloads alone "
                          "and print its figures (used for profiling a single kernel family)")
     args = ap.parse_args(argv)

@@ -205,6 +205,37 @@ PLX_API int parallax_decode(const void* q, const void* k_cache, const void* v_ca
 PLX_API size_t parallax_decode_workspace_bytes(int B, int H, int Lmax, int d, int dtype);
 
 /*
+ * Decode step with a given probe: one new query per (sequence, head) against
+ * a KV cache, in the form the paper states the layer ("Parallax:
+ * Parameterized Local Linear Attention for Language Modeling", technical
+ * summary, "Core mechanism"): o = o^SA - Sigma_KV rho, with the probe rho
+ * supplied by the caller.  With r_i = k_i . rho every term is a softmax-
+ * weighted sum over the keys,
+ *     o = mu_v - sum_i p_i r_i v_i + (sum_i p_i r_i) mu_v,
+ * so the keys and values are read once, in one pass, as the paper's own
+ * decode kernel runs both branches over one KV stream ("Hardware-aware
+ * algorithm").  Row len-1 of parallax_fwd_probe with that row's probe; with
+ * rho = -P_h (q - mu_k) it is parallax_decode.
+ *   q, rho: device, [B][H][d] bf16 (PLX_BF16 only; PLX_FP32 returns
+ *           PLX_ERR_UNSUPPORTED).
+ *   k_cache, v_cache: device, [B][H][Lmax][d] bf16.
+ *   lens: device int32 [B] (1 <= lens[b] <= Lmax; values outside are
+ *         clamped), or NULL for Lmax.  Cache rows at or past lens[b] are
+ *         ignored, whatever they hold.
+ *   out: device, [B][H][d] bf16.  lse: device, [B][H] float32.
+ *   workspace: device, >= parallax_decode_probe_workspace_bytes(), 256-byte
+ *              aligned, or NULL to allocate it stream-ordered.
+ * Returns PLX_OK, PLX_ERR_INVALID_ARG (null or misaligned pointer, bad
+ * sizes), PLX_ERR_UNSUPPORTED or PLX_ERR_CUDA; asynchronous on `stream`.
+ */
+PLX_API int parallax_decode_probe(const void* q, const void* k_cache, const void* v_cache, const int* lens,
+                          const void* rho, void* out, float* lse, void* workspace,
+                          int B, int H, int Lmax, int d, int dtype, void* stream);
+
+/* Bytes of device workspace parallax_decode_probe needs (0 on bad or unsupported args). */
+PLX_API size_t parallax_decode_probe_workspace_bytes(int B, int H, int Lmax, int d, int dtype);
+
+/*
  * Forward and backward of the layer from HOST buffers, with the copies
  * overlapped with the compute.  The paper has no counterpart: this entry
  * serves callers whose tensors live in host memory.  The heads are split into

@@ -43,7 +43,10 @@ def _load():
         lib.plx_oracle_bwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i,
                                        ctypes.POINTER(ctypes.c_int32), i, dp, dp, dp, dp, i]
         lib.plx_oracle_fwd_probe.argtypes = [dp, dp, dp, dp, i, i, i, i, dp, dp, i]
-        for f in (lib.plx_oracle_fwd, lib.plx_oracle_fwd_rows, lib.plx_oracle_bwd, lib.plx_oracle_fwd_probe):
+        lib.plx_oracle_fwd_probe_rows.argtypes = [dp, dp, dp, dp, i, i, i, i,
+                                                  ctypes.POINTER(ctypes.c_int64), i, dp, dp, i]
+        for f in (lib.plx_oracle_fwd, lib.plx_oracle_fwd_rows, lib.plx_oracle_bwd, lib.plx_oracle_fwd_probe,
+                  lib.plx_oracle_fwd_probe_rows):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -113,6 +116,22 @@ def forward_probe(q, k, v, rho, nthreads: int | None = None):
                                       nthreads or default_threads())
     if rc:
         raise RuntimeError(f"plx_oracle_fwd_probe failed ({rc})")
+    return out, lse
+
+
+def forward_probe_rows(q, k, v, rho, rows, nthreads: int | None = None):
+    """The given-probe form at selected (b, h, t) rows: returns (out [n,d], lse [n])."""
+    q, k, v, rho = _f64(q), _f64(k), _f64(v), _f64(rho)
+    B, H, T, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.empty((n, d))
+    lse = np.empty((n,))
+    rc = _load().plx_oracle_fwd_probe_rows(_p(q), _p(k), _p(v), _p(rho), B, H, T, d,
+                                           rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+                                           _p(out), _p(lse), nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"plx_oracle_fwd_probe_rows failed ({rc})")
     return out, lse
 
 

@@ -374,6 +374,45 @@ int plx_oracle_fwd_probe(const double *q, const double *k, const double *v, cons
     return run_pool(&pool, nthreads) ? 2 : 0;
 }
 
+/* The given-probe form at selected rows only: rows is n triples (b, h, t);
+ * rho is still [B][H][T][d] (only the selected rows' probes are read). */
+typedef struct {
+    const plx_in_t *in;
+    const double *rho;
+    const int64_t *rows;
+    double *out, *lse;
+} probe_rows_ctx_t;
+
+static void probe_rows_job(void *vctx, int job, scratch_t *w, double *unused) {
+    (void)unused;
+    probe_rows_ctx_t *ctx = (probe_rows_ctx_t *)vctx;
+    const int b = (int)ctx->rows[3 * job], h = (int)ctx->rows[3 * job + 1];
+    const int t = (int)ctx->rows[3 * job + 2], d = ctx->in->d;
+    const double L = probe_query(ctx->in, ctx->rho, b, h, t, w);
+    if (ctx->lse) ctx->lse[job] = L;
+    for (int j = 0; j < d; j++)
+        if (ctx->out) ctx->out[(size_t)job * d + j] = w->o[j];
+}
+
+int plx_oracle_fwd_probe_rows(const double *q, const double *k, const double *v, const double *rho, int B, int H,
+                              int T, int d, const int64_t *rows, int n, double *out, double *lse, int nthreads) {
+    if (B < 1 || H < 1 || T < 1 || d < 1 || n < 0 || !q || !k || !v || !rho || (n && !rows)) return 1;
+    for (int r = 0; r < n; r++) {
+        if (rows[3 * r] < 0 || rows[3 * r] >= B || rows[3 * r + 1] < 0 || rows[3 * r + 1] >= H ||
+            rows[3 * r + 2] < 0 || rows[3 * r + 2] >= T)
+            return 1;
+    }
+    plx_in_t in = {q, k, v, NULL, NULL, B, H, T, d, 0};
+    probe_rows_ctx_t ctx = {&in, rho, rows, out, lse};
+    pool_t pool;
+    memset(&pool, 0, sizeof(pool));
+    pool.in = &in;
+    pool.njobs = n;
+    pool.run = probe_rows_job;
+    pool.ctx = &ctx;
+    return run_pool(&pool, nthreads) ? 2 : 0;
+}
+
 /* ----------------------------------------------------------------- backward */
 
 typedef struct {

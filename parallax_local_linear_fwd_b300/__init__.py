@@ -24,7 +24,8 @@ __all__ = [
     "parallax_bwd_workspace_bytes", "parallax_last_device_error", "parallax_set_path",
     "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
     "parallax_timing_get", "parallax_timing_reset", "kernel_times",
-    "parallax_decode", "parallax_decode_workspace_bytes",
+    "parallax_decode", "parallax_decode_workspace_bytes", "parallax_decode_probe",
+    "parallax_decode_probe_workspace_bytes",
     "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes", "parallax_set_wait_limit",
 ]
 
@@ -58,6 +59,8 @@ _SIGNATURES = {
     "parallax_timing_reset": (None, []),
     "parallax_decode": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "parallax_decode_probe": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_decode_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_fwd_probe": (_i, [_vp] * 7 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_step_host": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _i, _vp]),
@@ -331,6 +334,37 @@ def parallax_decode(q, k_cache, v_cache, P, lens=None, out=None, lse=None, works
         _check(lib().parallax_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(P), _ptr(out),
                                      _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
                "parallax_decode")
+    return out, lse
+
+
+def parallax_decode_probe_workspace_bytes(B, H, Lmax, d, dtype) -> int:
+    return int(lib().parallax_decode_probe_workspace_bytes(B, H, Lmax, d, dtype))
+
+
+def parallax_decode_probe(q, k_cache, v_cache, rho, lens=None, out=None, lse=None, workspace=None, stream=None):
+    """Decode step with a given probe rho [B,H,d]: q [B,H,d] against caches
+    [B,H,Lmax,d] (bf16, CUDA), o = o^SA - Sigma_KV rho in one pass over the
+    keys and values; lens: int32 [B] (None: Lmax).  Returns (out, lse)."""
+    if not isinstance(k_cache, torch.Tensor) or k_cache.dim() != 4:
+        raise ValueError("the caches must be [B, H, Lmax, d] tensors")
+    B, H, Lmax, d = (int(x) for x in k_cache.shape)
+    dt = _dtype_code(k_cache)
+    dev = k_cache.device
+    _expect("q", q, (B, H, d), k_cache.dtype, dev)
+    _expect("rho", rho, (B, H, d), k_cache.dtype, dev)
+    _expect("v_cache", v_cache, (B, H, Lmax, d), k_cache.dtype, dev)
+    _expect("lens", lens, (B,), torch.int32, dev, optional=True)
+    _expect("out", out, (B, H, d), k_cache.dtype, dev, optional=True)
+    _expect("lse", lse, (B, H), torch.float32, dev, optional=True)
+    _cuda_device(k_cache)
+    if workspace is not None:
+        _expect_workspace(workspace, parallax_decode_probe_workspace_bytes(B, H, Lmax, d, dt), dev)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    with _on(k_cache):
+        _check(lib().parallax_decode_probe(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(rho), _ptr(out),
+                                           _ptr(lse), _ptr(workspace), B, H, Lmax, d, dt, _stream_ptr(stream)),
+               "parallax_decode_probe")
     return out, lse
 
 

@@ -347,6 +347,40 @@ int parallax_decode(const void* q, const void* k_cache, const void* v_cache, con
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
+size_t parallax_decode_probe_workspace_bytes(int B, int H, int Lmax, int d, int dtype) {
+    if (check_sizes(B, H, Lmax, d, dtype) || dtype != PLX_BF16) return 0;
+    return plx::decode_probe_ws_bytes(B, H, Lmax, d);
+}
+
+int parallax_decode_probe(const void* q, const void* k_cache, const void* v_cache, const int* lens, const void* rho,
+                          void* out, float* lse, void* workspace, int B, int H, int Lmax, int d, int dtype,
+                          void* stream) {
+    int rc = check_sizes(B, H, Lmax, d, dtype);
+    if (rc) return rc;
+    if (dtype != PLX_BF16) return PLX_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !rho || !out || !lse) return PLX_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k_cache, v_cache, rho, out, lse};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
+    if (lens && ((uintptr_t)lens & 3u)) return PLX_ERR_INVALID_ARG;
+    if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool own = workspace == nullptr;
+    void* ws = workspace;
+    if (own && cudaMallocAsync(&ws, plx::decode_probe_ws_bytes(B, H, Lmax, d), s) != cudaSuccess) return PLX_ERR_CUDA;
+    plx::DecodeArgs a{q, k_cache, v_cache, lens, nullptr, out, lse, ws, B, H, Lmax, d, dtype, s, status, rho};
+    cudaError_t e = plx::decode_probe(a);
+    if (own) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e == cudaErrorNotSupported) return PLX_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
 int parallax_step_host(const void* q, const void* k, const void* v, const float* P, const void* dout, void* out,
                        float* lse, float* mu_k, void* dq, void* dk, void* dv, float* dP, int chunks, int B, int H,
                        int T, int d, int dtype, void* stream) {

@@ -57,13 +57,14 @@ struct DecodeArgs {
     const void* k;     // [B,H,Lmax,d] key cache
     const void* v;     // [B,H,Lmax,d] value cache
     const int* lens;   // [B] valid keys per sequence (device), or nullptr = Lmax
-    const float* P;    // [H,d,d]
+    const float* P;    // [H,d,d] (the committed probe form)
     void* out;         // [B,H,d]
     float* lse;        // [B,H]
-    void* ws;          // decode_ws_bytes()
+    void* ws;          // decode_ws_bytes() or decode_probe_ws_bytes()
     int B, H, Lmax, d, dtype;
     cudaStream_t stream;
     unsigned* status;  // device watchdog word
+    const void* rho = nullptr;  // [B,H,d] the given probe (decode_probe), same dtype as q
 };
 
 struct ProbeArgs {
@@ -113,6 +114,8 @@ bool tc_make_map(void* map, const void* base, int D, int T, int BH, int rows);
 // One-pass decode for bf16 caches (tensor-core M = V^T diag(p) K per chunk).
 size_t decode_tc_ws_bytes(int B, int H, int Lmax, int d);
 cudaError_t decode_tc(const DecodeArgs& a);
+size_t decode_probe_ws_bytes(int B, int H, int Lmax, int d);
+cudaError_t decode_probe(const DecodeArgs& a);
 size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
 cudaError_t tc_fwd(const FwdArgs& a);

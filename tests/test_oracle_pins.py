@@ -190,6 +190,13 @@ def test_rows_and_head_subsets_agree_with_full(oracle_mod):
         np.testing.assert_array_equal(o_r[j], out[b, h, t])
         np.testing.assert_array_equal(l_r[j], lse[b, h, t])
         np.testing.assert_array_equal(m_r[j], mu[b, h, t])
+    # the given-probe form at selected rows is its full form at those rows
+    rho = _rand(rng, B, H, T, d) * 0.3
+    po, pl = oracle_mod.forward_probe(q, k, v, rho, nthreads=3)
+    po_r, pl_r = oracle_mod.forward_probe_rows(q, k, v, rho, rows, nthreads=2)
+    for j, (b, h, t) in enumerate(rows):
+        np.testing.assert_array_equal(po_r[j], po[b, h, t])
+        np.testing.assert_array_equal(pl_r[j], pl[b, h, t])
     dq, dk, dv, dP = oracle_mod.backward(q, k, v, P, do, nthreads=3)
     sub = [(0, 1), (1, 1)]
     dq2, dk2, dv2, dP2 = oracle_mod.backward(q, k, v, P, do, heads=sub, nthreads=2)
