@@ -194,6 +194,25 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
         for (int i = 0; i < 16; i++) ak[i] = av[i] = 0;
         float l = 0.f, m_run = -INFINITY;
         const uint32_t idM = idesc_mma(128, D, true, true);
+        // M += V^T (p K) for tile jt: A = V^T (MN-major: features contiguous),
+        // B = p K (MN-major), K dimension = the tile's keys in steps of 16.
+        // Issued by warp 0 at the next tile's max barrier (or after the loop
+        // for the last tile), which every write-back of tile jt precedes, so a
+        // tile needs one barrier
+        auto issue_mma = [&](int jt) {
+            const int st = jt % NS;
+            const uint32_t va = smem_u32(sKV + (2 * st + 1) * C::TB), kb = smem_u32(sKV + (2 * st) * C::TB);
+            const uint32_t lboA = D == 64 ? (uint32_t)(smem_u32(sZ) - va) : (uint32_t)(KT * 128);
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < KT / 16; kk++)
+                    mma_ss(tM, desc_mn_lbo(va, kk, lboA), desc_mnmajor(kb, KT, kk), idM, (jt > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&empty[st]);
+                mma_commit(mma_done);
+            }
+            __syncwarp();
+        };
         bool ok = true;
         for (int j = 0; j < nt; j++) {
             const int s = j % NS;
@@ -243,6 +262,7 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
                 ok = false;
                 break;
             }
+            if (warp == 0 && j >= 1) issue_mma(j - 1);
             float tm = wmax[0];
 #pragma unroll
             for (int w = 1; w < NW; w++) tm = fmaxf(tm, wmax[w]);
@@ -311,22 +331,6 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
                 *(uint4*)(sv + off) = vo;
             }
             fence_proxy_async_smem();
-            workers_sync(NW * 32);
-            if (warp == 0) {
-                // M += V^T (p K): A = V^T (MN-major: features contiguous), B = p K
-                // (MN-major), K dimension = the tile's 64 keys in steps of 16
-                tc_fence_after();
-                const uint32_t va = smem_u32(sv), kb = smem_u32(sk);
-                const uint32_t lboA = D == 64 ? (uint32_t)(smem_u32(sZ) - va) : (uint32_t)(KT * 128);
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < KT / 16; kk++)
-                        mma_ss(tM, desc_mn_lbo(va, kk, lboA), desc_mnmajor(kb, KT, kk), idM, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&empty[s]);
-                    mma_commit(mma_done);
-                }
-                __syncwarp();
-            }
         }
         // the merge grid may now be scheduled (it waits for this grid's
         // completion before it reads the partials)
@@ -337,6 +341,7 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             for (int jj = issued > NS ? issued - NS : 0; jj < issued; jj++) mbar_wait_drain(&full[jj % NS], (jj / NS) & 1);
         // ---- the chunk's partial (every worker agrees whether it is valid)
         ok = workers_and(ok, NW * 32);
+        if (ok && warp == 0) issue_mma(nt - 1);  // the last tile's write-back preceded the barrier above
         float* dst = part + ((size_t)bh * gridDim.x + blockIdx.x) * C::PART;
         // l, sum p k, sum p v: reduce over the keys (lanes of one feature part
         // first, then the worker warps through shared memory, reusing stage 0)
