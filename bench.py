@@ -338,9 +338,12 @@ def run_ours(args, world, rank):
     plx.parallax_set_path(plx.PLX_PATH_AUTO)
     path = "tc" if _tc_ws(plx, B, H, T, d, dtc) > 0 else "simt"
 
+    sws = torch.empty(max(256, plx.parallax_fwd_bwd_workspace_bytes(B, H, T, d, dtc)), dtype=torch.uint8, device=dev)
+
     def step():
-        plx.parallax_fwd_ws(q, k, v, P, out, lse, mu, fws, stream=stream)
-        plx.parallax_bwd(q, k, v, P, lse, mu, do, dq, dk, dv, dP, workspace=bws, stream=stream)
+        # one training step through the fused entry point (one workspace, the
+        # backward reusing the forward's f16 operand copies)
+        plx.parallax_fwd_bwd(q, k, v, P, do, out, lse, mu, dq, dk, dv, dP, workspace=sws, stream=stream)
         if args.shard == "batch" and world > 1:
             from parallax_local_linear_fwd_b300.shard import allreduce_dP
             allreduce_dP(dP)

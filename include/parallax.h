@@ -151,6 +151,23 @@ PLX_API int parallax_bwd(const void* q, const void* k, const void* v, const floa
                  int B, int H, int T, int d, int dtype, void* stream);
 
 /*
+ * Forward and backward of one training step in one call: parallax_fwd's
+ * outputs (out, lse, mu_k) and parallax_bwd's (dq, dk, dv, dP), with the
+ * same arguments, layouts and errors as those two.  One workspace serves
+ * both, so the backward reuses the f16 operand copies of q, k and v that the
+ * forward's pass 1 writes (it converts dO only).  Equal, bit for bit, to
+ * parallax_fwd followed by parallax_bwd.
+ *   workspace: device, >= parallax_fwd_bwd_workspace_bytes(), 256-byte
+ *              aligned, or NULL to allocate it stream-ordered.
+ */
+PLX_API int parallax_fwd_bwd(const void* q, const void* k, const void* v, const float* P, const void* dout,
+                     void* out, float* lse, float* mu_k, void* dq, void* dk, void* dv, float* dP,
+                     void* workspace, int B, int H, int T, int d, int dtype, void* stream);
+
+/* Bytes of device workspace parallax_fwd_bwd needs (0 on bad args). */
+PLX_API size_t parallax_fwd_bwd_workspace_bytes(int B, int H, int T, int d, int dtype);
+
+/*
  * One-pass forward with a given probe: the layer in the form the paper states
  * it ("Parallax: Parameterized Local Linear Attention for Language Modeling",
  * technical summary, "Core mechanism"), with the probe rho supplied by the

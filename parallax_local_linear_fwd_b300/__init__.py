@@ -24,6 +24,7 @@ __all__ = [
     "parallax_bwd_workspace_bytes", "parallax_last_device_error", "parallax_set_path",
     "parallax_strerror", "parallax_launch_count", "parallax_timing_enable", "parallax_timing_collect",
     "parallax_timing_get", "parallax_timing_reset", "kernel_times",
+    "parallax_fwd_bwd", "parallax_fwd_bwd_workspace_bytes",
     "parallax_decode", "parallax_decode_workspace_bytes", "parallax_decode_probe",
     "parallax_decode_probe_workspace_bytes",
     "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes", "parallax_set_wait_limit",
@@ -60,6 +61,8 @@ _SIGNATURES = {
     "parallax_decode": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_decode_probe": (_i, [_vp] * 8 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_bwd": (_i, [_vp] * 13 + [_i, _i, _i, _i, _i, _vp]),
+    "parallax_fwd_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_decode_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "parallax_fwd_probe": (_i, [_vp] * 7 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_fwd_probe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -279,6 +282,43 @@ def parallax_bwd(q, k, v, P, lse, mu_k, dout, dq=None, dk=None, dv=None, dP=None
                                   _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
                                   B, H, T, d, dt, _stream_ptr(stream)), "parallax_bwd")
     return dq, dk, dv, dP
+
+
+def parallax_fwd_bwd_workspace_bytes(B, H, T, d, dtype) -> int:
+    return int(lib().parallax_fwd_bwd_workspace_bytes(B, H, T, d, dtype))
+
+
+def parallax_fwd_bwd(q, k, v, P, dout, out=None, lse=None, mu_k=None, dq=None, dk=None, dv=None, dP=None,
+                     workspace=None, stream=None):
+    """Forward and backward of one step in one call (one workspace: the
+    backward reuses the forward's f16 operand copies).  Returns
+    (out, lse, mu_k, dq, dk, dv, dP), equal to parallax_fwd then parallax_bwd."""
+    B, H, T, d = _shape(q)
+    dt = _dtype_code(q)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _expect(name, t, (B, H, T, d), q.dtype, dev)
+    _expect("P", P, (H, d, d), torch.float32, dev)
+    for name, t in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(name, t, (B, H, T, d), q.dtype, dev, optional=True)
+    _expect("lse", lse, (B, H, T), torch.float32, dev, optional=True)
+    _expect("mu_k", mu_k, (B, H, T, d), torch.float32, dev, optional=True)
+    _expect("dP", dP, (H, d, d), torch.float32, dev, optional=True)
+    _cuda_device(q)
+    if workspace is not None:
+        _expect_workspace(workspace, parallax_fwd_bwd_workspace_bytes(B, H, T, d, dt), dev)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev) if lse is None else lse
+    mu_k = torch.empty((B, H, T, d), dtype=torch.float32, device=dev) if mu_k is None else mu_k
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dP = torch.empty_like(P) if dP is None else dP
+    with _on(q):
+        _check(lib().parallax_fwd_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(P), _ptr(dout), _ptr(out), _ptr(lse),
+                                      _ptr(mu_k), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dP), _ptr(workspace),
+                                      B, H, T, d, dt, _stream_ptr(stream)), "parallax_fwd_bwd")
+    return out, lse, mu_k, dq, dk, dv, dP
 
 
 def parallax_fwd_probe_workspace_bytes(B, H, T, d, dtype) -> int:

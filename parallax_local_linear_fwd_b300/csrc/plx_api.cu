@@ -285,6 +285,51 @@ int parallax_bwd(const void* q, const void* k, const void* v, const float* P, co
     return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
 }
 
+size_t parallax_fwd_bwd_workspace_bytes(int B, int H, int T, int d, int dtype) {
+    if (check_sizes(B, H, T, d, dtype)) return 0;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return 0;
+    const size_t f = fwd_ws_for(fam, B, H, T, d), b = bwd_ws_for(fam, B, H, T, d);
+    return f > b ? f : b;
+}
+
+int parallax_fwd_bwd(const void* q, const void* k, const void* v, const float* P, const void* dout, void* out,
+                     float* lse, float* mu_k, void* dq, void* dk, void* dv, float* dP, void* workspace, int B, int H,
+                     int T, int d, int dtype, void* stream) {
+    int rc = check_sizes(B, H, T, d, dtype);
+    if (rc) return rc;
+    if (!q || !k || !v || !P || !dout || !out || !lse || !mu_k || !dq || !dk || !dv || !dP)
+        return PLX_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, P, dout, out, lse, mu_k, dq, dk, dv, dP};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PLX_ERR_INVALID_ARG;
+    if (workspace && ((uintptr_t)workspace & 255u)) return PLX_ERR_INVALID_ARG;
+    const int fam = pick_family(dtype);
+    if (fam < 0) return -fam;
+    unsigned* status = nullptr;
+    rc = device_state(&status);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool own = workspace == nullptr;
+    void* ws = workspace;
+    if (own && cudaMallocAsync(&ws, parallax_fwd_bwd_workspace_bytes(B, H, T, d, dtype), s) != cudaSuccess)
+        return PLX_ERR_CUDA;
+    plx::FwdArgs fa{q, k, v, P, out, lse, mu_k, ws, B, H, T, d, dtype, s, status};
+    plx::BwdArgs ba{q, k, v, P, lse, mu_k, dout, dq, dk, dv, dP, ws, B, H, T, d, dtype, s, status};
+    cudaError_t e;
+    if (fam == 2) {
+        e = plx::tc_fwd_bwd(fa, ba);
+    } else {
+        e = plx::simt_fwd(fa);
+        if (e == cudaSuccess) e = plx::simt_bwd(ba);
+    }
+    if (own) {
+        cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? PLX_OK : PLX_ERR_CUDA;
+}
+
 size_t parallax_fwd_probe_workspace_bytes(int B, int H, int T, int d, int dtype) {
     if (check_sizes(B, H, T, d, dtype) || dtype != PLX_BF16 || !plx::tc_available()) return 0;
     return plx::tc_probe_ws_bytes(B, H, T, d);
@@ -463,11 +508,14 @@ int parallax_step_host(const void* q, const void* k, const void* v, const float*
         const float* Pc = Pd + (size_t)h0[c] * d * d;
         plx::FwdArgs fa{dev(c, Q), dev(c, K), dev(c, V), Pc, dev(c, OUT), (float*)dev(c, LSE), (float*)dev(c, MU),
                         ws, B, nh[c], T, d, dtype, s, status};
-        if (!chk(fam == 2 ? plx::tc_fwd(fa) : plx::simt_fwd(fa))) break;
         plx::BwdArgs ba{dev(c, Q), dev(c, K), dev(c, V), Pc, (const float*)dev(c, LSE), (const float*)dev(c, MU),
                         dev(c, DO), dev(c, DQ), dev(c, DK), dev(c, DV), dPd + (size_t)h0[c] * d * d, ws,
                         B, nh[c], T, d, dtype, s, status};
-        if (!chk(fam == 2 ? plx::tc_bwd(ba) : plx::simt_bwd(ba))) break;
+        if (fam == 2) {  // one workspace: the backward reuses the forward's f16 copies
+            if (!chk(plx::tc_fwd_bwd(fa, ba))) break;
+        } else {
+            if (!chk(plx::simt_fwd(fa)) || !chk(plx::simt_bwd(ba))) break;
+        }
         if (!chk(cudaEventRecord(e_comp[c], s)) || !chk(cudaStreamWaitEvent(s_out, e_comp[c], 0))) break;
         void* dst[4] = {out, dq, dk, dv};
         for (int t = OUT; t <= DV; t++)

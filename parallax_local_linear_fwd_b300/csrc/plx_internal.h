@@ -120,6 +120,7 @@ size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
 cudaError_t tc_fwd(const FwdArgs& a);
 cudaError_t tc_bwd(const BwdArgs& a);
+cudaError_t tc_fwd_bwd(const FwdArgs& f, const BwdArgs& b);
 // One-pass forward with a given probe (o = o^SA - Sigma_KV rho), bf16.
 size_t tc_probe_ws_bytes(int B, int H, int T, int d);
 cudaError_t tc_probe(const ProbeArgs& a);

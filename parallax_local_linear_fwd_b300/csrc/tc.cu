@@ -2949,11 +2949,10 @@ cudaError_t to_f16(const void* const* src, __half* const* dst, int count, size_t
 }
 
 template <int D>
-cudaError_t fwd_impl(const FwdArgs& a) {
+cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w) {
     const int BH = a.B * a.H;
     const float scale_log2 = LOG2E / sqrtf((float)D);
     const size_t n = (size_t)BH * a.T * D;
-    TcFwdWs w = tc_fwd_ws(a.ws, a.B, a.H, a.T, D);
     // pass 1 reads the bf16 inputs (a 16-bit map copies the bytes as they
     // are) and writes the f16 copies of q, k, v that pass 2 reads
     CUtensorMap mq_in, mk_in, mv_in, mk16_128, mv16_128, mq128, mu128, mk64, mv64, mmu, mout;
@@ -3000,7 +2999,7 @@ cudaError_t fwd_impl(const FwdArgs& a) {
 }
 
 template <int D>
-cudaError_t bwd_impl(const BwdArgs& a) {
+cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready) {
     const int BH = a.B * a.H;
     const float scale = 1.f / sqrtf((float)D);
     const float scale_log2 = LOG2E * scale;
@@ -3015,7 +3014,11 @@ cudaError_t bwd_impl(const BwdArgs& a) {
         !make_map(&mdmu64, w.dmu, D, a.T, BH, 64) || !make_map(&mdo64, w.do16, D, a.T, BH, 64) ||
         !make_rows_map(&mrows, w.rows, a.T, BH, 32))
         return cudaErrorInvalidValue;
-    {
+    if (copies_ready) {  // the forward of the same step made the copies of q, k, v
+        const void* src[1] = {a.dout};
+        __half* dst[1] = {w.do16};
+        PLX_TRY(to_f16(src, dst, 1, n, a.stream));
+    } else {
         const void* src[4] = {a.q, a.k, a.v, a.dout};
         __half* dst[4] = {w.q16, w.k16, w.v16, w.do16};
         PLX_TRY(to_f16(src, dst, 4, n, a.stream));
@@ -3151,7 +3154,30 @@ size_t tc_bwd_ws_bytes(int B, int H, int T, int d) { return tc_bwd_bytes(B, H, T
 
 cudaError_t tc_fwd(const FwdArgs& a) {
     if (a.dtype != 1) return cudaErrorNotSupported;
-    return a.d == 64 ? fwd_impl<64>(a) : fwd_impl<128>(a);
+    if (a.d == 64) return fwd_impl<64>(a, tc_fwd_ws(a.ws, a.B, a.H, a.T, 64));
+    return fwd_impl<128>(a, tc_fwd_ws(a.ws, a.B, a.H, a.T, 128));
+}
+
+// Forward and backward of one step in one workspace (the backward's): the
+// forward's f16 copies of q, k and v are written where the backward reads
+// them, and its U and gbar in the backward's U and ebar regions (B2 and B1
+// rewrite those only after pass 2 has read them), so the backward converts
+// dO alone.
+cudaError_t tc_fwd_bwd(const FwdArgs& f, const BwdArgs& b) {
+    if (f.dtype != 1) return cudaErrorNotSupported;
+    const TcBwdWs w = tc_bwd_ws(b.ws, b.B, b.H, b.T, b.d);
+    TcFwdWs fw;
+    fw.q16 = w.q16;
+    fw.k16 = w.k16;
+    fw.v16 = w.v16;
+    fw.U = w.U;
+    fw.gbar = w.ebar;
+    if (f.d == 64) {
+        PLX_TRY(fwd_impl<64>(f, fw));
+        return bwd_impl<64>(b, true);
+    }
+    PLX_TRY(fwd_impl<128>(f, fw));
+    return bwd_impl<128>(b, true);
 }
 
 size_t tc_probe_ws_bytes(int B, int H, int T, int d) {
@@ -3166,7 +3192,7 @@ cudaError_t tc_probe(const ProbeArgs& a) {
 
 cudaError_t tc_bwd(const BwdArgs& a) {
     if (a.dtype != 1) return cudaErrorNotSupported;
-    return a.d == 64 ? bwd_impl<64>(a) : bwd_impl<128>(a);
+    return a.d == 64 ? bwd_impl<64>(a, false) : bwd_impl<128>(a, false);
 }
 
 }  // namespace plx

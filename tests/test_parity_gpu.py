@@ -238,6 +238,36 @@ def test_backward_full_size_c4_head_subset():
         assert np.isfinite(g).all()
 
 
+@pytest.mark.parametrize("path", ["simt", "tc"])
+@pytest.mark.parametrize("B,H,T,d,dtype", [(2, 2, 130, 64, "bf16"), (1, 2, 257, 128, "bf16"), (1, 2, 100, 64, "fp32")])
+def test_fused_step_equals_separate_calls(path, B, H, T, d, dtype):
+    # parallax_fwd_bwd shares one workspace between the passes (the backward
+    # reads the forward's f16 copies): every output equals parallax_fwd then
+    # parallax_bwd bit for bit, and stays inside its tensor
+    _use_path(path, dtype)
+    inp = plx_synth.generate(B, H, T, d, dtype, seed=11 * T + d, p_std=0.3 / np.sqrt(d), backward=True)
+    q, k, v, P, do = (to_device(inp[x]) for x in ("q", "k", "v", "P", "dout"))
+    out, lse, mu = plx.parallax_fwd(q, k, v, P)
+    sep = (out, lse, mu) + tuple(plx.parallax_bwd(q, k, v, P, lse, mu, do))
+    shapes = {"out": ((B, H, T, d), q.dtype), "lse": ((B, H, T), torch.float32), "mu": ((B, H, T, d), torch.float32),
+              "dq": ((B, H, T, d), q.dtype), "dk": ((B, H, T, d), q.dtype), "dv": ((B, H, T, d), q.dtype),
+              "dP": ((H, d, d), torch.float32)}
+    g = {n: guarded_empty(sh, dt) for n, (sh, dt) in shapes.items()}
+    fused = plx.parallax_fwd_bwd(q, k, v, P, do, out=g["out"][1], lse=g["lse"][1], mu_k=g["mu"][1], dq=g["dq"][1],
+                                 dk=g["dk"][1], dv=g["dv"][1], dP=g["dP"][1])
+    code, detail = plx.parallax_last_device_error()
+    assert code == plx.PLX_OK, (code, hex(detail))
+    for n, a_, b_ in zip(shapes, sep, fused):
+        assert torch.equal(a_, b_), n
+        assert guards_intact(g[n][0], shapes[n][0]), f"{n}: a store landed outside the tensor"
+    # and the fused step agrees with the oracle
+    f = inputs_f64(inp)
+    ref = oracle.backward(f["q"], f["k"], f["v"], f["P"], f["dout"])
+    tol = TOL_FP32 if dtype == "fp32" else TOL_BF16_GRAD
+    for name, got, r in zip(("dq", "dk", "dv", "dP"), fused[3:], ref):
+        assert rel_err(to_host64(got), r, dtype if name != "dP" else "fp32") < tol, name
+
+
 def test_dp_is_bitwise_reproducible():
     plx.parallax_set_path(plx.PLX_PATH_AUTO)
     inp = plx_synth.generate(2, 2, 300, 64, "bf16", seed=5, p_std=0.05, backward=True)
