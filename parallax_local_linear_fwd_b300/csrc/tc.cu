@@ -29,6 +29,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <functional>
 #include <mutex>
 
 #include "plx_internal.h"
@@ -2949,7 +2950,7 @@ cudaError_t to_f16(const void* const* src, __half* const* dst, int count, size_t
 }
 
 template <int D>
-cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w) {
+cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cudaError_t()>& after_pass1 = {}) {
     const int BH = a.B * a.H;
     const float scale_log2 = LOG2E / sqrtf((float)D);
     const size_t n = (size_t)BH * a.T * D;
@@ -2976,6 +2977,7 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
+    if (after_pass1) PLX_TRY(after_pass1());
     if constexpr (D == 128) {  // pass 2: two query tiles per CTA sharing the K|V stages
         using C = DualPP<D>;
         const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
@@ -2999,7 +3001,8 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w) {
 }
 
 template <int D>
-cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready) {
+// parts: 1 = the dO (or all) operand copies and B1, 2 = B2 onwards, 3 = all.
+cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready, int parts = 3) {
     const int BH = a.B * a.H;
     const float scale = 1.f / sqrtf((float)D);
     const float scale_log2 = LOG2E * scale;
@@ -3014,7 +3017,8 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready) {
         !make_map(&mdmu64, w.dmu, D, a.T, BH, 64) || !make_map(&mdo64, w.do16, D, a.T, BH, 64) ||
         !make_rows_map(&mrows, w.rows, a.T, BH, 32))
         return cudaErrorInvalidValue;
-    if (copies_ready) {  // the forward of the same step made the copies of q, k, v
+    if (!(parts & 1)) {
+    } else if (copies_ready) {  // the forward of the same step made the copies of q, k, v
         const void* src[1] = {a.dout};
         __half* dst[1] = {w.do16};
         PLX_TRY(to_f16(src, dst, 1, n, a.stream));
@@ -3023,7 +3027,8 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready) {
         __half* dst[4] = {w.q16, w.k16, w.v16, w.do16};
         PLX_TRY(to_f16(src, dst, 4, n, a.stream));
     }
-    if constexpr (D == 128) {  // B1: R = sum p e k, ebar = sum p e (two query tiles per CTA)
+    if (!(parts & 1)) {
+    } else if constexpr (D == 128) {  // B1: R = sum p e k, ebar = sum p e (two query tiles per CTA)
         using C = DualPP<D>;
         const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
         PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
@@ -3042,6 +3047,7 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
+    if (!(parts & 2)) return cudaSuccess;
     {  // B2: row math and the dP_h partials
         using R = RowCfg<D>;
         const int nchunks = (a.B * a.T + R::ROWS_PER_CTA - 1) / R::ROWS_PER_CTA;
@@ -3160,24 +3166,60 @@ cudaError_t tc_fwd(const FwdArgs& a) {
 
 // Forward and backward of one step in one workspace (the backward's): the
 // forward's f16 copies of q, k and v are written where the backward reads
-// them, and its U and gbar in the backward's U and ebar regions (B2 and B1
-// rewrite those only after pass 2 has read them), so the backward converts
-// dO alone.
-cudaError_t tc_fwd_bwd(const FwdArgs& f, const BwdArgs& b) {
-    if (f.dtype != 1) return cudaErrorNotSupported;
-    const TcBwdWs w = tc_bwd_ws(b.ws, b.B, b.H, b.T, b.d);
+// them, its U in the backward's U region (B2 rewrites it after pass 2 has read
+// it) and its gbar in the dq accumulator's (written from B2 on), so the
+// backward converts dO alone.  B1 needs only pass 1's results, so it runs on a
+// second stream beside pass 2 (the two kernels each leave the tensor pipe
+// partly idle); B2 waits for both.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t side_stream(SideStream** out, std::unique_lock<std::mutex>* lock) {
+    static SideStream cache[64];
+    static std::mutex mu[64];
+    int dev = 0;
+    PLX_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    *lock = std::unique_lock<std::mutex>(mu[dev]);  // the events are reused: one caller enqueues at a time
+    SideStream& x = cache[dev];
+    if (!x.s) {
+        PLX_TRY(cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking));
+        PLX_TRY(cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming));
+        PLX_TRY(cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming));
+    }
+    *out = &x;
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t fwd_bwd_impl(const FwdArgs& f, const BwdArgs& b) {
+    const TcBwdWs w = tc_bwd_ws(b.ws, b.B, b.H, b.T, D);
     TcFwdWs fw;
     fw.q16 = w.q16;
     fw.k16 = w.k16;
     fw.v16 = w.v16;
     fw.U = w.U;
-    fw.gbar = w.ebar;
-    if (f.d == 64) {
-        PLX_TRY(fwd_impl<64>(f, fw));
-        return bwd_impl<64>(b, true);
-    }
-    PLX_TRY(fwd_impl<128>(f, fw));
-    return bwd_impl<128>(b, true);
+    fw.gbar = w.dq_acc;
+    SideStream* ss = nullptr;
+    std::unique_lock<std::mutex> lock;
+    PLX_TRY(side_stream(&ss, &lock));
+    auto b1_beside = [&]() -> cudaError_t {
+        PLX_TRY(cudaEventRecord(ss->fork, f.stream));
+        PLX_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+        BwdArgs b1 = b;
+        b1.stream = ss->s;
+        PLX_TRY(bwd_impl<D>(b1, true, 1));
+        return cudaEventRecord(ss->join, ss->s);
+    };
+    PLX_TRY(fwd_impl<D>(f, fw, b1_beside));
+    PLX_TRY(cudaStreamWaitEvent(b.stream, ss->join, 0));
+    return bwd_impl<D>(b, true, 2);
+}
+
+cudaError_t tc_fwd_bwd(const FwdArgs& f, const BwdArgs& b) {
+    if (f.dtype != 1) return cudaErrorNotSupported;
+    return f.d == 64 ? fwd_bwd_impl<64>(f, b) : fwd_bwd_impl<128>(f, b);
 }
 
 size_t tc_probe_ws_bytes(int B, int H, int T, int d) {
