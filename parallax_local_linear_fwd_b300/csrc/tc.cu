@@ -737,15 +737,19 @@ __device__ __forceinline__ void dual_store_acc(uint32_t tAcc, uint32_t lrow, int
 // MODE 0 (forward pass 2): X = U K^T, W = p (x + 1 - gbar), Acc += W V, out = Acc.
 // MODE 1 (backward B1)   : X = dO V^T, W = p x,           Acc += W K, R = Acc,
 //                          ebar = sum_i W (fp32, before rounding).
+// The weights W have TMEM columns of their own, so the MMA thread issues the
+// next key tile's S and X as soon as the elementwise warps have read this
+// tile's (before they have formed W), and the accumulation of W after them:
+// the scores of tile j + 1 run while tile j's weights are formed.
 template <int D>
 struct DualCfg {
     static constexpr int BM = 128, BN = 64;
     static constexpr int NS = D == 64 ? 4 : 1;  // K+V stages
     static constexpr int AB = BM * D * 2;       // one A tile (Q, U or dO)
     static constexpr int KB = BN * D * 2;       // one K or V tile
-    static constexpr int NBAR = 1 + 2 * NS + 4;
+    static constexpr int NBAR = 1 + 2 * NS + 4 + 2;  // + sx_free, w_free
     static constexpr int SMEM = 1024 + 2 * AB + NS * 2 * KB + NBAR * 8 + 16;
-    static constexpr unsigned TMEM_COLS = 256;  // S [0,64) (W aliases [0,32)), X [64,128), Acc [128,128+D)
+    static constexpr unsigned TMEM_COLS = 256;  // S [0,64), X [64,128), W [128,160), Acc [160,160+D)
 };
 
 template <int D, int MODE>
@@ -757,6 +761,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             unsigned* status) {
     using C = DualCfg<D>;
     constexpr int NS = C::NS;
+    static_assert(D == 64, "the TMEM plan holds S, X, W and Acc for d = 64");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* sA1 = sm;
@@ -770,6 +775,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint64_t* w_full = s_full + 1;
     uint64_t* acc_done = s_full + 2;
     uint64_t* drain = s_full + 3;
+    uint64_t* sx_free = s_full + 4;  // the elementwise warps have read S and X of the tile (128 arrivals)
+    uint64_t* w_free = s_full + 5;   // the accumulation has read W of the tile
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
@@ -792,6 +799,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mbar_init(w_full, 128);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
+        mbar_init(sx_free, 128);
+        mbar_init(w_free, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
@@ -799,7 +808,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
-    const uint32_t tS = tmem, tX = tmem + 64, tAcc = tmem + 128;
+    const uint32_t tS = tmem, tX = tmem + 64, tW = tmem + 128, tAcc = tmem + 160;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -836,38 +845,45 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const uint32_t idS = idesc_mma(128, C::BN, false, false);
         const uint32_t idA = idesc_mma(128, D, false, true);
         const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
-        if (__all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2))) {
-            for (int j = 0; j < nkt; j++) {
-                const int s = j % NS;
-                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3))) break;
-                // S aliases the previous tile's weights; tcgen05.mma ops issued by
-                // one thread execute in issue order, so no wait for that MMA here.
-                tc_fence_after();
-                const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
-                const uint32_t vaddr = kaddr + C::KB;
-                const uint32_t xb = MODE == 0 ? kaddr : vaddr;  // B of the second score product
-                const uint32_t ab = MODE == 0 ? vaddr : kaddr;  // B of the accumulation
-                if (elect_one()) {
+        auto scores = [&](int j) {  // S = A1 K_j^T, X = A2 (K or V)_j^T
+            const uint32_t kaddr = smem_u32(sKV + (j % NS) * 2 * C::KB);
+            const uint32_t xb = MODE == 0 ? kaddr : kaddr + C::KB;  // B of the second score product
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++)
-                        mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++)
-                        mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
-                    mma_commit(s_full);
-                }
-                __syncwarp();
-                if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
-                tc_fence_after();
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; kk++)
-                        mma_ts(tAcc, tS + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                    if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
-                    mma_commit(&kv_empty[s]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
+                mma_commit(s_full);
             }
+            __syncwarp();
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2)) &&
+                  __all_sync(0xffffffffu, mbar_wait(&kv_full[0], 0, wd, 3));
+        if (ok) scores(0);
+        for (int j = 0; ok && j < nkt; j++) {
+            const int s = j % NS;
+            if (j + 1 < nkt) {
+                // tile j's S and X have been read: tile j + 1's may overwrite them
+                if (!__all_sync(0xffffffffu, mbar_wait(sx_free, j & 1, wd, 9))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
+                scores(j + 1);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+            tc_fence_after();
+            const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
+            const uint32_t ab = MODE == 0 ? kaddr + C::KB : kaddr;  // B of the accumulation
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; kk++)
+                    mma_ts(tAcc, tW + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
+                mma_commit(w_free);
+                mma_commit(&kv_empty[s]);
+            }
+            __syncwarp();
         }
         if (elect_one()) mma_commit(drain);
         __syncwarp();
@@ -899,6 +915,10 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 tmem_ld32(tS + lrow + c * 32, vs);
                 tmem_ld32(tX + lrow + c * 32, vx);
                 tmem_wait_ld();
+                if (c == C::BN / 32 - 1) {  // S and X of the tile are in registers
+                    tc_fence_before();
+                    mbar_arrive(sx_free);
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
@@ -917,11 +937,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     // R - ebar mu_k = sum_i w_i (k_i - mu_k) holds for them.
                     if (MODE == 1) rs2 = fadd2(rs2, f2(f16_lo(pk[i]), f16_hi(pk[i])));
                 }
-                tmem_st16(tS + lrow + c * 16, pk);
+                if (c == 0 && j > 0) {  // the previous tile's accumulation has read W
+                    ok = mbar_wait(w_free, (j - 1) & 1, wd, 10);
+                    tc_fence_after();
+                }
+                tmem_st16(tW + lrow + c * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(w_full);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
         }
         if (ok) ok = mbar_wait(acc_done, 0, wd, 8);
         // the group meets on a named barrier in the store below: agree first
