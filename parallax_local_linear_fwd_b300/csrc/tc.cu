@@ -2839,6 +2839,363 @@ __global__ void __launch_bounds__(B3P::NT, 1)
     }
 }
 
+// ------------------------------------------------ B3, d = 64: 64-query sub-chunks
+// The same mathematics as tc_bwd_b3 with 64-query sub-chunks: the score
+// product [S|G|Y]^T = K [Q|U|dmu]^T is one N = 192 MMA per 16 of d, and E^T one
+// N = 64 MMA.  One TMEM score region serves every sub-chunk.  The two
+// elementwise warpgroups (queries [0,32) and [32,64) of each sub-chunk) load
+// their scores into registers and arrive on sx_free; the MMA thread then
+// issues the next sub-chunk's scores while they form the weights.  The weights
+// have storage of their own: a | dg in TMEM, ds and p in shared memory (ds in
+// the 128-query tile the dQ product reads as well), so the accumulation of
+// sub-chunk j reads them while the scores of j + 1 occupy the score region.
+// dQ of each 128-query tile is read after the elementwise step of the next
+// tile's first sub-chunk, by when its product has completed; it is staged in
+// the ds tile that product has read (one 32-column box per warpgroup) and
+// added into the fp32 accumulator by one tensor reduce-add per box.  The next
+// writer of that ds tile, a sub-chunk later, waits until both reduces have
+// read their boxes.
+// TMEM columns: S^T [0,64) G^T [64,128) Y^T [128,192) E^T [192,256),
+// a|dg [256,320), dV [320,384), dK [384,448), dQ [448,512).
+struct B3Q {
+    static constexpr int D = 64, BK = 128, BQ = 64, QT = 128, NT = 320;
+    static constexpr int NS = 3;                            // operand stages
+    static constexpr int KB = BK * D * 2;                   // K or V tile
+    static constexpr int SUB = BQ * 128;                    // one 64-row operand tile
+    static constexpr int DO_OFF = 3 * SUB;                  // after the stacked [Q|U|dmu]
+    static constexpr int ROWS_OFF = 4 * SUB;
+    static constexpr int STAGE = ROWS_OFF + (BQ / 2) * 32;  // + the row scalars of 32 query pairs
+    static constexpr int DSB = BK * QT * 2;                 // one ds tile, f16 [keys][128 queries]
+    static constexpr int PB = BK * BQ * 2;                  // the p tile, f16 [keys][64 queries]
+    static constexpr int NBAR = 1 + 2 * NS + 12;
+    static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + PB + NS * STAGE + NBAR * 8 + 16;
+    static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+};
+
+__global__ void __launch_bounds__(B3Q::NT, 1)
+    tc_bwd_b3_q64(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
+                  const __grid_constant__ CUtensorMap tm_dmu, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_dq,
+                  __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T, int BH, int nkt,
+                  float scale, float scale_log2, unsigned* status) {
+    using C = B3Q;
+    constexpr int NS = C::NS, D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sK = sm;
+    uint8_t* sV = sK + C::KB;
+    uint8_t* sDS = sV + C::KB;       // two ds tiles (128-query tiles m and m + 1)
+    uint8_t* sP = sDS + 2 * C::DSB;  // p of one sub-chunk
+    uint8_t* sSt = sP + C::PB;       // stage s: Q, U, dmu, dO (64 rows each), row scalars
+    uint64_t* bars = (uint64_t*)(sSt + NS * C::STAGE);
+    uint64_t* kv_full = bars;
+    uint64_t* st_full = bars + 1;
+    uint64_t* st_empty = st_full + NS;
+    uint64_t* sc_full = st_empty + NS;  // the sub-chunk's scores are in TMEM
+    uint64_t* sx_free = sc_full + 1;    // both warpgroups have loaded them (256 arrivals)
+    uint64_t* w_full = sc_full + 2;     // the sub-chunk's weights are written (256 arrivals)
+    uint64_t* w_free = sc_full + 3;     // the accumulation has read a|dg and p
+    uint64_t* stg_read = sc_full + 4;   // [2], per ds tile: both dQ reduces staged there have read it (2 arrivals)
+    uint64_t* stg_ready = sc_full + 6;  // [2], per warpgroup: its dQ box is staged (128 arrivals)
+    uint64_t* dq_full = sc_full + 8;
+    uint64_t* dq_free = sc_full + 9;    // both warpgroups have read the dQ tile (256 arrivals)
+    uint64_t* drain = sc_full + 10;
+    uint64_t* fin = sc_full + 11;       // the last accumulation has completed (one phase)
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int kt, bh;
+    work_item(blockIdx.x, BH, nkt, &kt, &bh);  // key tiles with the most queries first
+    const int k0 = kt * C::BK;
+    const int nsub = (T - k0 + C::BQ - 1) / C::BQ;  // sub-chunk j: queries [k0 + 64 j, k0 + 64 j + 64)
+    const Watchdog wd{status, abortf, KID_TC_BWD_B3, wait_limit(status)};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&st_full[s], 1);
+            mbar_init(&st_empty[s], 1);
+        }
+        mbar_init(sc_full, 1);
+        mbar_init(sx_free, 256);
+        mbar_init(w_full, 256);
+        mbar_init(w_free, 1);
+        for (int x = 0; x < 2; x++) {
+            mbar_init(&stg_read[x], 2);
+            mbar_init(&stg_ready[x], 128);
+        }
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, 256);
+        mbar_init(drain, 1);
+        mbar_init(fin, 1);
+        fence_barrier_init();
+    }
+    // ds tiles start at zero: the last tile of a key tile may have one
+    // sub-chunk only, and the dQ product reads all 128 query rows (the rows
+    // past T are discarded).
+    for (int i = threadIdx.x; i < 2 * C::DSB / 16; i += C::NT) ((uint4*)sDS)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 1) tmem_alloc(holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tSc = tmem, tW = tmem + 256, tDV = tmem + 320, tDK = tmem + 384, tDQ = tmem + 448;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(kv_full, 2 * C::KB);
+            tma_load_3d(sK, &tm_k, 0, k0, bh, kv_full);
+            tma_load_3d(sV, &tm_v, 0, k0, bh, kv_full);
+            int issued = 0;
+            for (int j = 0; j < nsub; j++) {
+                const int s = j % NS, t0 = k0 + j * C::BQ;
+                if (j >= NS && !mbar_wait(&st_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&st_full[s], C::STAGE);
+                uint8_t* st = sSt + s * C::STAGE;
+                tma_load_3d(st, &tm_q, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::SUB, &tm_u, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + 2 * C::SUB, &tm_dmu, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::DO_OFF, &tm_do, 0, t0, bh, &st_full[s]);
+                tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, &st_full[s]);
+                issued = j + 1;
+            }
+            mbar_wait_drain(kv_full, 0);
+            for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&st_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        // The whole warp runs the loop, so the descriptors stay warp-uniform;
+        // the elected lane (lane 0 of the converged warp) issues every tcgen05
+        // instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T
+        const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
+        const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK
+        const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ
+        const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS), paddr = smem_u32(sP);
+        auto scores = [&](int j) {
+            const uint32_t st = smem_u32(sSt + (j % NS) * C::STAGE);
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++) {
+                    mma_ss(tSc, desc_kmajor(kaddr, C::BK, kk), desc_kmajor(st, 3 * C::BQ, kk), idS3, kk > 0);
+                    mma_ss(tSc + 192, desc_kmajor(vaddr, C::BK, kk), desc_kmajor(st + C::DO_OFF, C::BQ, kk), idS,
+                           kk > 0);
+                }
+                mma_commit(sc_full);
+            }
+            __syncwarp();
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, wd, 2)) &&
+                  __all_sync(0xffffffffu, mbar_wait(&st_full[0], 0, wd, 3));
+        if (ok) scores(0);
+        for (int j = 0; ok && j < nsub; j++) {
+            const int s = j % NS;
+            if (j + 1 < nsub) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&st_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
+                // sub-chunk j's scores are in registers: the region takes j + 1's
+                if (!__all_sync(0xffffffffu, mbar_wait(sx_free, j & 1, wd, 4))) break;
+                scores(j + 1);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+            tc_fence_after();
+            const uint32_t st = smem_u32(sSt + s * C::STAGE);
+            const uint32_t dsb = dsaddr + ((j >> 1) & 1) * C::DSB + (j & 1) * (C::BK * 128);  // ds of sub-chunk j
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BQ / 16; kk++) {
+                    const uint32_t first = (j == 0 && kk == 0) ? 0u : 1u;
+                    mma_ts(tDV, tW + 16 * kk, desc_mnmajor(st + C::DO_OFF, C::BQ, kk), idA, first);
+                    mma_ts(tDK, tW + 16 * kk + 8, desc_mnmajor(st + C::SUB, C::BQ, kk), idA, first);
+                    mma_ss(tDK, desc_kmajor(dsb, C::BK, kk), desc_mnmajor(st, C::BQ, kk), idA, 1u);
+                    mma_ss(tDK, desc_kmajor(paddr, C::BK, kk), desc_mnmajor(st + 2 * C::SUB, C::BQ, kk), idA, 1u);
+                }
+                mma_commit(w_free);
+                mma_commit(&st_empty[s]);
+                if (j == nsub - 1) mma_commit(fin);
+            }
+            __syncwarp();
+            if ((j & 1) == 1 || j == nsub - 1) {  // the 128-query tile m is complete: dQ = ds^T K
+                const int m = j >> 1, x = m & 1;
+                if (m >= 1 && !__all_sync(0xffffffffu, mbar_wait(dq_free, (m - 1) & 1, wd, 6))) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; kk++)
+                        mma_ss(tDQ, desc_mnmajor(dsaddr + x * C::DSB, C::BK, kk), desc_mnmajor(kaddr, C::BK, kk), idQ,
+                               kk > 0);
+                    mma_commit(dq_full);
+                }
+                __syncwarp();
+            }
+        }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
+    } else {
+        const int wg = (warp - 2) >> 2;  // queries [32 wg, 32 wg + 32) of every sub-chunk
+        const int qd = warp & 3;
+        const int i = qd * 32 + lane;  // key row (and, for dQ, query row)
+        const int key = k0 + i;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        const bool leader = qd == 0 && lane == 0;  // issues this warpgroup's dQ reduces
+        // dQ tile m: this warpgroup adds columns [32 wg, 32 wg + 32) of query
+        // row i, staged as one 32-column box in block wg of ds tile m & 1
+        int ndq = 0;  // dQ tiles this warpgroup has read
+        auto read_dq = [&](int m) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(dq_full, m & 1, wd, 9))) return false;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(tDQ + lrow + 32 * wg, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(dq_free);
+            uint8_t* box = sDS + (m & 1) * C::DSB + wg * (C::BK * 128);
+#pragma unroll
+            for (int y = 0; y < 8; y++)
+                *(uint4*)(box + i * 128 + ((y ^ (i & 7)) << 4)) = make_uint4(v[4 * y], v[4 * y + 1], v[4 * y + 2], v[4 * y + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(&stg_ready[wg]);
+            bool done = true;
+            if (leader) {  // every thread's staging writes are visible to the reduce
+                done = mbar_wait(&stg_ready[wg], ndq & 1, wd, 12);
+                if (done) {
+                    tma_reduce_add_3d(&tm_dq, 32 * wg, k0 + m * C::QT, bh, box);
+                    bulk_commit();
+                }
+            }
+            ndq++;
+            return __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
+        };
+        bool ok = true;
+        int nread = 0;  // dQ tiles read so far
+        for (int j = 0; j < nsub && ok; j++) {
+            const int s = j % NS, m = j >> 1, x = m & 1;
+            const int t0 = k0 + j * C::BQ;
+            ok = mbar_wait(sc_full, j & 1, wd, 7);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* rows = (const float*)(sSt + s * C::STAGE + C::ROWS_OFF);  // 8 floats per query pair
+            const bool need_mask = t0 < k0 + C::BK || t0 + C::BQ > T;
+            uint8_t* dsrow = sDS + x * C::DSB + (j & 1) * (C::BK * 128) + i * 128;
+            uint8_t* prow = sP + i * 128;
+            // chunk h's scores, loaded into registers; the second load comes right
+            // after the first chunk's arithmetic, so the region can take the next
+            // sub-chunk's scores before this one's weights are stored
+            uint32_t vs[16], vg[16], vy[16], ve[16];
+            auto load = [&](int c) {
+                tmem_ld16(tSc + lrow + 16 * c, vs);
+                tmem_ld16(tSc + lrow + 64 + 16 * c, vg);
+                tmem_ld16(tSc + lrow + 128 + 16 * c, vy);
+                tmem_ld16(tSc + lrow + 192 + 16 * c, ve);
+                tmem_wait_ld();
+            };
+            auto weights = [&](int c, uint32_t(&o1)[16], uint32_t(&o2)[16]) {  // o1: a | dg, o2: ds | p
+                if (need_mask) {
+                    // query t = t0 + 16 c + qq is valid iff key <= t and t < T
+                    const int qlo = max(key - (t0 + 16 * c), 0);
+                    const int qhi = T - (t0 + 16 * c);
+                    b3_chunk<true>(vs, vg, vy, ve, rows + 64 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
+                    if (qhi < 16) {
+#pragma unroll
+                        for (int y = 0; y < 8; y++) {
+                            const uint32_t keep = (2 * y + 1 < qhi) ? 0xFFFFFFFFu : (2 * y < qhi ? 0xFFFFu : 0u);
+                            o1[y] &= keep;
+                            o1[8 + y] &= keep;
+                            o2[y] &= keep;
+                            o2[8 + y] &= keep;
+                        }
+                    }
+                } else {
+                    b3_chunk<false>(vs, vg, vy, ve, rows + 64 * c, 0, scale, scale_log2, o1, o2);
+                }
+            };
+            // ds and p rows into the swizzled [keys][queries] tiles: the 16-query
+            // chunk c is the 16-byte chunks 2c and 2c + 1 of the 128-byte row
+            auto store = [&](int c, const uint32_t(&o1)[16], const uint32_t(&o2)[16]) {
+                const int ch = 2 * c;
+                tmem_st16(tW + lrow + 16 * c, o1);
+                *(uint4*)(dsrow + ((ch ^ (i & 7)) << 4)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                *(uint4*)(dsrow + (((ch + 1) ^ (i & 7)) << 4)) = make_uint4(o2[4], o2[5], o2[6], o2[7]);
+                *(uint4*)(prow + ((ch ^ (i & 7)) << 4)) = make_uint4(o2[8], o2[9], o2[10], o2[11]);
+                *(uint4*)(prow + (((ch + 1) ^ (i & 7)) << 4)) = make_uint4(o2[12], o2[13], o2[14], o2[15]);
+            };
+            uint32_t o1[16], o2[16];
+            load(2 * wg);
+            weights(2 * wg, o1, o2);
+            load(2 * wg + 1);
+            tc_fence_before();
+            mbar_arrive(sx_free);  // every score of the sub-chunk this thread needs is in registers
+            // the accumulation of j - 1 has read a|dg and p
+            if (j > 0) ok = mbar_wait(w_free, (j - 1) & 1, wd, 10);
+            if ((j & 1) == 0 && m >= 2) {
+                // ds tile x held the staged dQ of tile m - 2: both reduces have read it
+                if (leader) {
+                    bulk_wait_read_all();
+                    mbar_arrive(&stg_read[x]);
+                }
+                if (ok) ok = mbar_wait(&stg_read[x], ((m >> 1) - 1) & 1, wd, 8);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            store(2 * wg, o1, o2);
+            weights(2 * wg + 1, o1, o2);
+            store(2 * wg + 1, o1, o2);
+            if (!ok) break;
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(w_full);
+            // the dQ product of tile m - 1 was issued before this sub-chunk's accumulation
+            if ((j & 1) == 0 && m >= 1) {
+                ok = read_dq(m - 1);
+                nread = m;
+            }
+        }
+        // the remaining dQ tiles; the last one may hold one sub-chunk only
+        for (int mm = nread; ok && mm < (nsub + 1) / 2; mm++) ok = read_dq(mm);
+        if (leader) bulk_wait_all();  // the staging outlives its reduces
+        if (ok) {
+            ok = mbar_wait(fin, 0, wd, 11);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                const uint32_t tsrc = wg == 0 ? tDV : tDK;  // warpgroup 0 writes dV, 1 writes dK
+                __nv_bfloat16* dst_base = wg == 0 ? dv : dk;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t v[32];
+                    tmem_ld32(tsrc + lrow + 32 * c, v);
+                    tmem_wait_ld();
+                    if (key < T) {
+                        uint4* pv = (uint4*)(dst_base + ((size_t)bh * T + key) * D + 32 * c);
+#pragma unroll
+                        for (int y = 0; y < 4; y++)
+                            pv[y] = make_uint4(pack_bf16(__uint_as_float(v[8 * y]), __uint_as_float(v[8 * y + 1])),
+                                               pack_bf16(__uint_as_float(v[8 * y + 2]), __uint_as_float(v[8 * y + 3])),
+                                               pack_bf16(__uint_as_float(v[8 * y + 4]), __uint_as_float(v[8 * y + 5])),
+                                               pack_bf16(__uint_as_float(v[8 * y + 6]), __uint_as_float(v[8 * y + 7])));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 x = src[i];
@@ -3106,20 +3463,16 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready, int parts = 3) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
-    if (D == 64) {  // B3: dK, dV, dQ (ping-pong form)
-        using C = B3P;
-        CUtensorMap mq32, mu32, mdmu32, mdo32, mrows32, mdq;
+    if (D == 64) {  // B3: dK, dV, dQ (64-query sub-chunks)
+        using C = B3Q;
+        CUtensorMap mdq;
         if (!make_map_f32(&mdq, w.dq_acc, D, a.T, BH, C::QT)) return cudaErrorInvalidValue;
-        if (!make_map(&mq32, w.q16, D, a.T, BH, 32) || !make_map(&mu32, w.U, D, a.T, BH, 32) ||
-            !make_map(&mdmu32, w.dmu, D, a.T, BH, 32) || !make_map(&mdo32, w.do16, D, a.T, BH, 32) ||
-            !make_rows_map(&mrows32, w.rows, a.T, BH, 16))
-            return cudaErrorInvalidValue;
         const int nkt = (a.T + C::BK - 1) / C::BK;
-        PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3_pp, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        PLX_TRY(cudaFuncSetAttribute(tc_bwd_b3_q64, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b3");
-        tc_bwd_b3_pp<<<nkt * BH, C::NT, C::SMEM, a.stream>>>(mk128, mv128, mq32, mu32, mdmu32, mdo32, mrows32,
-                                                              mdq, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
-                                                              a.T, BH, nkt, scale, scale_log2, a.status);
+        tc_bwd_b3_q64<<<nkt * BH, C::NT, C::SMEM, a.stream>>>(mk128, mv128, mq64, mu64, mdmu64, mdo64, mrows,
+                                                               mdq, (__nv_bfloat16*)a.dk, (__nv_bfloat16*)a.dv,
+                                                               a.T, BH, nkt, scale, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // B3: dK, dV, dQ
