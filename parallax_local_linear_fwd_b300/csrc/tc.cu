@@ -2482,363 +2482,6 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
     }
 }
 
-// ------------------------------------------------ B3, d = 64: ping-pong form
-// The same mathematics as tc_bwd_b3 with queries in sub-chunks of 32 and two
-// TMEM score buffers: warpgroup 0 takes the even sub-chunks, warpgroup 1 the
-// odd ones, and the MMA thread issues scores(j), then the accumulation of
-// sub-chunk j - 1 (and dQ when a 128-query tile is complete), so the tensor
-// core works on one sub-chunk while the other warpgroup runs the elementwise
-// step.  TMEM columns: buffer b at 128 b = S^T [0,32) G^T [32,64) Y^T [64,96)
-// E^T [96,128); dV [256,320), dK [320,384), dQ [384,448).
-struct B3P {
-    static constexpr int D = 64, BK = 128, BQ = 32, QT = 128, NT = 320;
-    static constexpr int NS = 5;                   // operand stages (sub-chunk j in slot j % NS), loaded in pairs
-    static constexpr int NPB = 3;                  // pair barriers: at most three pairs are in flight
-    static constexpr int KB = BK * D * 2;          // K or V tile
-    static constexpr int SUB = BQ * 128;           // one 32-row operand tile
-    static constexpr int DO_OFF = 3 * SUB;         // after the stacked [Q|U|dmu]
-    static constexpr int ROWS_OFF = 4 * SUB;
-    static constexpr int STAGE_BYTES = ROWS_OFF + BQ * 16;
-    static constexpr int STAGE = 17 * 1024;        // stage stride (1024-aligned)
-    static constexpr int DSB = BK * QT * 2;        // one ds tile, f16 [keys][128 queries]
-    static constexpr int DQB = QT * D * 4;         // dQ staging: two 32-column boxes, 128-byte swizzle
-    static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 6;
-    static constexpr int SMEM = 1024 + 2 * KB + 2 * DSB + DQB + NS * STAGE + NBAR * 8 + 16;
-};
-
-__global__ void __launch_bounds__(B3P::NT, 1)
-    tc_bwd_b3_pp(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_u,
-                 const __grid_constant__ CUtensorMap tm_dmu, const __grid_constant__ CUtensorMap tm_do,
-                 const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_dq,
-                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T, int BH, int nkt, float scale,
-                 float scale_log2, unsigned* status) {
-    using C = B3P;
-    constexpr int NS = C::NS, D = C::D;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = align1024(smem_raw);
-    uint8_t* sK = sm;
-    uint8_t* sV = sK + C::KB;
-    uint8_t* sDS = sV + C::KB;  // two ds tiles
-    uint8_t* sDQ = sDS + 2 * C::DSB;  // dQ staging for the tensor reduce-add
-    uint8_t* sSt = sDQ + C::DQB;
-    uint64_t* bars = (uint64_t*)(sSt + NS * C::STAGE);
-    uint64_t* kv_full = bars;
-    uint64_t* st_full = bars + 1;
-    uint64_t* st_empty = st_full + NS;
-    uint64_t* sc_full = st_empty + NS;   // [2], per score buffer
-    uint64_t* op_full = sc_full + 2;     // [2]
-    uint64_t* ds_free = op_full + 2;     // [2], per ds tile
-    uint64_t* dq_full = ds_free + 2;
-    uint64_t* dq_free = dq_full + 1;
-    uint64_t* drain = dq_free + 1;
-    uint64_t* fin = drain + 1;           // the last accumulation has completed (one phase)
-    uint64_t* st_free = fin + 1;         // dQ staging may be overwritten (warpgroup 1)
-    uint64_t* st_ready = st_free + 1;    // dQ staging is written (warpgroup 1)
-    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
-    volatile int* abortf = (volatile int*)(holder + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int kt, bh;
-    work_item(blockIdx.x, BH, nkt, &kt, &bh);
-    const int k0 = kt * C::BK;
-    const int nsub = (T - k0 + C::BQ - 1) / C::BQ;  // sub-chunk j: queries [k0 + 32 j, k0 + 32 j + 32)
-    const Watchdog wd{status, abortf, KID_TC_BWD_B3, wait_limit(status)};
-
-    if (threadIdx.x == 0) {
-        *abortf = 0;
-        mbar_init(kv_full, 1);
-        for (int s = 0; s < NS; s++) {
-            mbar_init(&st_full[s], 1);
-            mbar_init(&st_empty[s], 1);
-        }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(&sc_full[b], 1);
-            mbar_init(&op_full[b], 128);
-            mbar_init(&ds_free[b], 1);
-        }
-        mbar_init(dq_full, 1);
-        mbar_init(dq_free, 128);
-        mbar_init(drain, 1);
-        mbar_init(fin, 1);
-        mbar_init(st_free, 128);
-        mbar_init(st_ready, 128);
-        fence_barrier_init();
-    }
-    // ds tiles start at zero: a tile cut by T leaves part unwritten, and the dQ
-    // MMA must not read uninitialised bits (its rows past T are discarded).
-    for (int i = threadIdx.x; i < 2 * C::DSB / 16; i += C::NT) ((uint4*)sDS)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    if (warp == 1) tmem_alloc(holder, 512);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *holder;
-    const uint32_t tDV = tmem + 256, tDK = tmem + 320, tDQ = tmem + 384;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            mbar_expect_tx(kv_full, 2 * C::KB);
-            tma_load_3d(sK, &tm_k, 0, k0, bh, kv_full);
-            tma_load_3d(sV, &tm_v, 0, k0, bh, kv_full);
-            // sub-chunks load in pairs (2p, 2p + 1) onto one barrier,
-            // st_full[p % NPB], so the MMA warp waits once per pair
-            int issued = 0;
-            for (int j = 0; j < nsub; j += 2) {
-                const int n2 = nsub - j < 2 ? nsub - j : 2;
-                uint64_t* bar = &st_full[(j >> 1) % C::NPB];
-                bool free_ok = true;
-                for (int e = 0; e < n2 && free_ok; e++) {
-                    const int jj = j + e;
-                    if (jj >= NS && !mbar_wait(&st_empty[jj % NS], ((jj / NS) - 1) & 1, wd, 1)) free_ok = false;
-                }
-                if (!free_ok) break;
-                mbar_expect_tx(bar, n2 * C::STAGE_BYTES);
-                for (int e = 0; e < n2; e++) {
-                    const int jj = j + e, t0 = k0 + jj * C::BQ;
-                    uint8_t* st = sSt + (jj % NS) * C::STAGE;
-                    tma_load_3d(st, &tm_q, 0, t0, bh, bar);
-                    tma_load_3d(st + C::SUB, &tm_u, 0, t0, bh, bar);
-                    tma_load_3d(st + 2 * C::SUB, &tm_dmu, 0, t0, bh, bar);
-                    tma_load_3d(st + C::DO_OFF, &tm_do, 0, t0, bh, bar);
-                    tma_load_3d(st + C::ROWS_OFF, &tm_rows, 0, t0 / 2, bh, bar);
-                }
-                issued = j + n2;
-            }
-            mbar_wait_drain(kv_full, 0);
-            // loads can be in flight for the last NPB pairs only (NS slots)
-            const int npairs = (issued + 1) / 2;
-            for (int pq = npairs > C::NPB ? npairs - C::NPB : 0; pq < npairs; pq++)
-                mbar_wait_drain(&st_full[pq % C::NPB], (pq / C::NPB) & 1);
-        }
-    } else if (warp == 1) {
-        // The whole warp runs the loop, so the descriptors stay warp-uniform;
-        // the elected lane (lane 0 of the converged warp) issues every tcgen05
-        // instruction, so one thread issues all MMAs, in order.
-        const uint32_t idS3 = idesc_mma(128, 3 * C::BQ, false, false);  // [S|G|Y]^T
-        const uint32_t idS = idesc_mma(128, C::BQ, false, false);       // E^T
-        const uint32_t idA = idesc_mma(128, D, false, true);            // dV, dK
-        const uint32_t idQ = idesc_mma(128, D, true, true);             // dQ
-        const uint32_t kaddr = smem_u32(sK), vaddr = smem_u32(sV), dsaddr = smem_u32(sDS);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, wd, 2));
-        for (int j = 0; ok && j <= nsub; j++) {
-            if (j < nsub) {
-                const int s = j % NS, b = j & 1;
-                // the pair (j, j + 1) arrives on one barrier: wait at even j only
-                if ((j & 1) == 0 &&
-                    !__all_sync(0xffffffffu, mbar_wait(&st_full[(j >> 1) % C::NPB], ((j >> 1) / C::NPB) & 1, wd, 3)))
-                    break;
-                // buffer b's weight operands were read by the accumulation of j - 2,
-                // issued earlier by this thread: MMAs execute in issue order
-                tc_fence_after();
-                const uint32_t st = smem_u32(sSt + s * C::STAGE);
-                const uint32_t tb = tmem + 128 * b;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++) {
-                        mma_ss(tb, desc_kmajor(kaddr, C::BK, kk), desc_kmajor(st, 3 * C::BQ, kk), idS3, kk > 0);
-                        mma_ss(tb + 96, desc_kmajor(vaddr, C::BK, kk), desc_kmajor(st + C::DO_OFF, C::BQ, kk), idS,
-                               kk > 0);
-                    }
-                    mma_commit(&sc_full[b]);
-                }
-                __syncwarp();
-            }
-            if (j >= 1) {
-                const int jp = j - 1, bp = jp & 1, sp = jp % NS;
-                if (!__all_sync(0xffffffffu, mbar_wait(&op_full[bp], (jp >> 1) & 1, wd, 5))) break;
-                tc_fence_after();
-                const uint32_t st = smem_u32(sSt + sp * C::STAGE);
-                const uint32_t tb = tmem + 128 * bp;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BQ / 16; kk++) {
-                        const uint32_t first = (jp == 0 && kk == 0) ? 0u : 1u;
-                        mma_ts(tDV, tb + 16 * kk, desc_mnmajor(st + C::DO_OFF, C::BQ, kk), idA, first);
-                        mma_ts(tDK, tb + 16 * kk + 8, desc_mnmajor(st + C::SUB, C::BQ, kk), idA, first);
-                        mma_ts(tDK, tb + 32 + 16 * kk, desc_mnmajor(st, C::BQ, kk), idA, 1u);
-                        mma_ts(tDK, tb + 32 + 16 * kk + 8, desc_mnmajor(st + 2 * C::SUB, C::BQ, kk), idA, 1u);
-                    }
-                    mma_commit(&st_empty[sp]);
-                    if (jp == nsub - 1) mma_commit(fin);
-                }
-                __syncwarp();
-                if ((jp & 3) == 3 || jp == nsub - 1) {
-                    const int m = jp >> 2, x = m & 1;
-                    if (m >= 1 && !__all_sync(0xffffffffu, mbar_wait(dq_free, (m - 1) & 1, wd, 6))) break;
-                    tc_fence_after();
-                    const uint32_t dsx = dsaddr + x * C::DSB;
-                    if (elect_one()) {
-#pragma unroll
-                        for (int kk = 0; kk < C::BK / 16; kk++)
-                            mma_ss(tDQ, desc_mnmajor(dsx, C::BK, kk), desc_mnmajor(kaddr, C::BK, kk), idQ, kk > 0);
-                        mma_commit(dq_full);
-                        mma_commit(&ds_free[x]);
-                    }
-                    __syncwarp();
-                }
-            }
-        }
-        if (elect_one()) mma_commit(drain);
-        __syncwarp();
-        mbar_wait_drain(drain, 0);
-    } else {
-        const int wg = (warp - 2) >> 2;  // owns score buffer wg and the sub-chunks j = wg (mod 2)
-        const int qd = warp & 3;
-        const int i = qd * 32 + lane;  // key row (and, for dQ, query row)
-        const int key = k0 + i;
-        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
-        const uint32_t tb = tmem + 128 * wg;
-        // dQ of the 128-query tile m: thread = query row i; reduced into dq_acc
-        // dQ of the 128-query tile m (thread = query row i): staged in shared
-        // memory and added into the fp32 accumulator by one tensor reduce-add
-        // per 32-column box (rows past T are clipped by the tensor map).
-        // The warpgroup meets on two mbarriers (st_free, st_ready; one phase
-        // per call, parity = calls so far) rather than on a named barrier:
-        // their waits are bounded and see the abort flag, so a warp that
-        // left after a timed-out wait cannot strand the others.
-        int ndq = 0;
-        auto read_dq = [&](int m) -> bool {
-            const bool got = mbar_wait(dq_full, m & 1, wd, 9);
-            if (!__all_sync(0xffffffffu, got)) return false;
-            tc_fence_after();
-            const bool leader = warp == 6 && lane == 0;
-            if (leader) bulk_wait_read_all();  // the previous tile's reduce has read the staging
-            mbar_arrive(st_free);
-            if (!__all_sync(0xffffffffu, mbar_wait(st_free, ndq & 1, wd, 11))) return false;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; c++) {
-                uint32_t v[32];
-                tmem_ld32(tDQ + lrow + 32 * c, v);
-                tmem_wait_ld();
-                uint8_t* box = sDQ + c * (C::QT * 128) + i * 128;
-#pragma unroll
-                for (int y = 0; y < 8; y++)
-                    *(uint4*)(box + ((y ^ (i & 7)) << 4)) = make_uint4(v[4 * y], v[4 * y + 1], v[4 * y + 2], v[4 * y + 3]);
-            }
-            tc_fence_before();
-            mbar_arrive(dq_free);
-            fence_proxy_async_smem();
-            mbar_arrive(st_ready);
-            bool done = true;
-            if (leader) {  // every thread's staging writes are visible to the reduce
-                done = mbar_wait(st_ready, ndq & 1, wd, 12);
-                if (done) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; c++)
-                        tma_reduce_add_3d(&tm_dq, 32 * c, k0 + m * C::QT, bh, sDQ + c * (C::QT * 128));
-                    bulk_commit();
-                }
-            }
-            ndq++;
-            return __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
-        };
-        bool ok = true;
-        // warpgroup 1 reads dQ tile m after its next sub-chunk (4 m + 5), by
-        // when the dQ product has completed, instead of waiting for it
-        int pend = -1;
-        for (int j = wg; j < nsub && ok; j += 2) {
-            const int s = j % NS, m = j >> 2, x = m & 1;
-            const int t0 = k0 + j * C::BQ;
-            // first write of ds tile m by this warpgroup: dQ(m - 2) must have read the buffer
-            if ((j & 3) == wg && m >= 2) {
-                ok = mbar_wait(&ds_free[x], ((m >> 1) - 1) & 1, wd, 7);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-            }
-            ok = mbar_wait(&sc_full[wg], (j >> 1) & 1, wd, 8);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float* rows = (const float*)(sSt + s * C::STAGE + C::ROWS_OFF);  // 8 floats per query pair
-            // ds row segment of this sub-chunk: column block (j & 3) >> 1, 16-byte
-            // chunks 4 (j & 1) + 2 c + {0, 1} of the 128-byte row
-            uint8_t* dsrow = sDS + x * C::DSB + ((j & 3) >> 1) * (C::BK * 128) + i * 128;
-            const bool need_mask = t0 < k0 + C::BK || t0 + C::BQ > T;
-#pragma unroll 1
-            for (int c = 0; c < 2; c++) {
-                uint32_t vs[16], vg[16], vy[16], ve[16];
-                tmem_ld16(tb + lrow + 16 * c, vs);
-                tmem_ld16(tb + lrow + 32 + 16 * c, vg);
-                tmem_ld16(tb + lrow + 64 + 16 * c, vy);
-                tmem_ld16(tb + lrow + 96 + 16 * c, ve);
-                tmem_wait_ld();
-                uint32_t o1[16], o2[16];  // o1: a | dg, o2: ds | p (f16 pairs)
-                if (need_mask) {
-                    const int qlo = max(key - (t0 + 16 * c), 0);
-                    const int qhi = T - (t0 + 16 * c);
-                    b3_chunk<true>(vs, vg, vy, ve, rows + 64 * c, qhi <= 0 ? 16 : qlo, scale, scale_log2, o1, o2);
-                    if (qhi < 16) {
-#pragma unroll
-                        for (int y = 0; y < 8; y++) {
-                            const uint32_t keep = (2 * y + 1 < qhi) ? 0xFFFFFFFFu : (2 * y < qhi ? 0xFFFFu : 0u);
-                            o1[y] &= keep;
-                            o1[8 + y] &= keep;
-                            o2[y] &= keep;
-                            o2[8 + y] &= keep;
-                        }
-                    }
-                } else {
-                    b3_chunk<false>(vs, vg, vy, ve, rows + 64 * c, 0, scale, scale_log2, o1, o2);
-                }
-                tmem_st16(tb + lrow + 16 * c, o1);
-                tmem_st16(tb + lrow + 32 + 16 * c, o2);
-                const int ch = 4 * (j & 1) + 2 * c;
-                *(uint4*)(dsrow + ((ch ^ (i & 7)) << 4)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-                *(uint4*)(dsrow + (((ch + 1) ^ (i & 7)) << 4)) = make_uint4(o2[4], o2[5], o2[6], o2[7]);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&op_full[wg]);
-            if (wg == 1) {
-                if (pend >= 0) {
-                    ok = read_dq(pend);
-                    pend = -1;
-                }
-                if ((j & 3) == 3) pend = m;
-            }
-        }
-        // warpgroup 1 reads every dQ tile in order; the last one may be partial
-        if (ok && wg == 1 && pend >= 0) ok = read_dq(pend);
-        if (ok && wg == 1 && ((nsub - 1) & 3) != 3) ok = read_dq((nsub - 1) >> 2);
-        if (wg == 1 && warp == 6 && lane == 0) bulk_wait_all();  // staging must outlive its reduces
-        if (ok) {
-            ok = mbar_wait(fin, 0, wd, 10);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-                const uint32_t tsrc = wg == 0 ? tDV : tDK;  // warpgroup 0 writes dV, 1 writes dK
-                __nv_bfloat16* dst_base = wg == 0 ? dv : dk;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t v[32];
-                    tmem_ld32(tsrc + lrow + 32 * c, v);
-                    tmem_wait_ld();
-                    if (key < T) {
-                        uint4* pv = (uint4*)(dst_base + ((size_t)bh * T + key) * D + 32 * c);
-#pragma unroll
-                        for (int y = 0; y < 4; y++)
-                            pv[y] = make_uint4(pack_bf16(__uint_as_float(v[8 * y]), __uint_as_float(v[8 * y + 1])),
-                                               pack_bf16(__uint_as_float(v[8 * y + 2]), __uint_as_float(v[8 * y + 3])),
-                                               pack_bf16(__uint_as_float(v[8 * y + 4]), __uint_as_float(v[8 * y + 5])),
-                                               pack_bf16(__uint_as_float(v[8 * y + 6]), __uint_as_float(v[8 * y + 7])));
-                    }
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
-}
-
 // ------------------------------------------------ B3, d = 64: 64-query sub-chunks
 // The same mathematics as tc_bwd_b3 with 64-query sub-chunks: the score
 // product [S|G|Y]^T = K [Q|U|dmu]^T is one N = 192 MMA per 16 of d, and E^T one
@@ -3463,7 +3106,7 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready, int parts = 3) {
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
-    if (D == 64) {  // B3: dK, dV, dQ (64-query sub-chunks)
+    if constexpr (D == 64) {  // B3: dK, dV, dQ (64-query sub-chunks)
         using C = B3Q;
         CUtensorMap mdq;
         if (!make_map_f32(&mdq, w.dq_acc, D, a.T, BH, C::QT)) return cudaErrorInvalidValue;
