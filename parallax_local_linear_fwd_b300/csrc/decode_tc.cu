@@ -566,9 +566,16 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
 // softmax-weighted sum over the keys: one pass over K and V, as the pages'
 // decode kernel runs both branches over one KV stream ("Hardware-aware
 // algorithm").  No matrix product remains, so the chunk kernel runs on the
-// CUDA cores: each CTA streams its chunk of keys once (TMA, four stages) and
-// keeps, with an online softmax, l = sum p, sum p r, sum p v and sum p r v.
-// A second kernel merges the chunks of a head by their log-sum-exp.
+// CUDA cores and keeps, with an online softmax, l = sum p, sum p r, sum p v
+// and sum p r v.
+// Work split: the keys of all heads form one sequence of KT-key tiles, head
+// after head (ntile = ceil(Lmax / KT) tiles per head, G = B H ntile in all).
+// CTA c of N takes tiles [c G / N, (c + 1) G / N), so every CTA streams the
+// same number of bytes, and with N = MIN_CTAS CTAs per SM so does every SM
+// (whole heads per CTA would leave some SMs a third more work than others).
+// A CTA writes one partial per head its range touches, into slot c + h
+// (distinct for every overlapping pair); a second kernel merges the partials
+// of a head by their log-sum-exp.
 template <int D>
 struct DecP {
     static constexpr int TPK = D / 32;       // threads per key (32 features each)
@@ -579,9 +586,11 @@ struct DecP {
     static constexpr int TB = KT * D * 2;    // one K or V tile: 8 KB
     static constexpr int QS = 34;            // stride of a 32-feature part of q and rho in shared memory
     static constexpr int NBAR = NS;          // full[NS]
-    static constexpr int SMEM = 1024 + NS * 2 * TB + NBAR * 8 + 16 + 8 * 4 + 2 * TPK * QS * 4 + 16;
+    static constexpr int RED = NW * (2 * D + 2);  // per-warp sums of one partial
+    static constexpr int SMEM = 1024 + NS * 2 * TB + NBAR * 8 + 16 + 2 * NW * 4 + 2 * TPK * QS * 4 + RED * 4 + 16;
     static_assert(MIN_CTAS * (SMEM + 1024) <= 233472, "MIN_CTAS CTAs fit an SM's shared memory");
-    // partial of one chunk: {m, l, sum p r, pad}, sum p v [D], sum p r v [D]
+    static_assert(2 * NW <= 8, "the two tile-parity copies of the warp maxima fit their slot");
+    // partial of one (CTA, head): {m, l, sum p r, pad}, sum p v [D], sum p r v [D]
     static constexpr int PART = 4 + 2 * D;
 };
 
@@ -589,55 +598,71 @@ template <int D>
 __global__ void __launch_bounds__(DecP<D>::NT, DecP<D>::MIN_CTAS)
     decp_chunk(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ rho,
-               const int* __restrict__ lens, int H, int Lmax, int chunk, float scale_log2,
+               const int* __restrict__ lens, int H, int Lmax, int ntile, long long G, float scale_log2,
                float* __restrict__ part, unsigned* status) {
     using C = DecP<D>;
-    constexpr int NS = C::NS, KT = C::KT, TPK = C::TPK, NW = C::NW;
+    constexpr int NS = C::NS, KT = C::KT, TPK = C::TPK, NW = C::NW, NT = C::NT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sKV = sm;  // stage s: K at 2 s TB, V at (2 s + 1) TB
     uint64_t* full = (uint64_t*)(sKV + NS * 2 * C::TB);
     uint32_t* holder = (uint32_t*)(full + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
-    float* wmax = (float*)(holder + 4);  // [NW]
+    float* wmax = (float*)(holder + 4);  // [2][NW]: tile max per warp, by tile parity
     float* sq = wmax + 8;                // q, fp32, parts of 32 at stride QS
     float* sr = sq + TPK * C::QS;        // rho likewise
+    float* red = sr + TPK * C::QS;       // [NW][2 D + 2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y, b = bh / H;
-    const int len = seq_len1(lens, b, Lmax);
-    const int k_begin = blockIdx.x * chunk;
-    const int k_end = min(k_begin + chunk, len);
-    if (k_begin >= k_end) return;  // no keys of this sequence in this chunk (uniform per CTA)
-    const int nt = (k_end - k_begin + KT - 1) / KT;
+    const long long N = gridDim.x, cta = blockIdx.x;
+    const long long g0 = cta * G / N, g1 = (cta + 1) * G / N;  // this CTA's tiles
+    const int h0 = (int)(g0 / ntile), h1 = (int)((g1 - 1) / ntile);
     const Watchdog wd{status, abortf, KID_DECODE, wait_limit(status)};
+    // the merge may be launched now: it waits for this whole grid to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         *abortf = 0;
         for (int s = 0; s < NS; s++) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < D; i += NW * 32) {
-        sq[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(q[(size_t)bh * D + i]);
-        sr[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(rho[(size_t)bh * D + i]);
-    }
     __syncthreads();
 
-    auto load_tile = [&](int j) {
-        const int s = j % NS;
+    // tiles [tb, tv) of head h lie in this CTA's range and hold keys of the sequence
+    auto range = [&](int h, int& tb, int& tv) {
+        const long long hb = (long long)h * ntile;
+        tb = (int)(max(g0, hb) - hb);
+        const int te = (int)(min(g1, hb + ntile) - hb);
+        const int len = seq_len1(lens, h / H, Lmax);
+        tv = max(tb, min(te, (len + KT - 1) / KT));
+    };
+    int total = 0;  // tiles this CTA streams
+    for (int h = h0; h <= h1; h++) {
+        int tb, tv;
+        range(h, tb, tv);
+        total += tv - tb;
+    }
+    // The loader (lane 0 of the last warp) walks the same tiles, NS ahead of
+    // the workers: tile n of the walk goes to stage n % NS.
+    const bool loader = threadIdx.x == (NW - 1) * 32;
+    int lh = h0, lt = 0, le = 0, issued = 0;
+    if (loader) range(lh, lt, le);
+    auto load_next = [&]() {
+        while (lt >= le) range(++lh, lt, le);  // issued < total: a head with tiles follows
+        const int s = issued % NS;
         mbar_expect_tx(&full[s], 2 * C::TB);
 #pragma unroll
         for (int r = 0; r < D / 64; r++) {
-            tma_load_3d(sKV + (2 * s) * C::TB + r * KT * 128, &tm_k, r * 64, k_begin + j * KT, bh, &full[s]);
-            tma_load_3d(sKV + (2 * s + 1) * C::TB + r * KT * 128, &tm_v, r * 64, k_begin + j * KT, bh, &full[s]);
+            tma_load_3d(sKV + (2 * s) * C::TB + r * KT * 128, &tm_k, r * 64, lt * KT, lh, &full[s]);
+            tma_load_3d(sKV + (2 * s + 1) * C::TB + r * KT * 128, &tm_v, r * 64, lt * KT, lh, &full[s]);
         }
+        lt++;
+        issued++;
     };
-    const bool loader = threadIdx.x == (NW - 1) * 32;
-    int issued = 0;
     if (loader) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        for (; issued < NS && issued < nt; issued++) load_tile(issued);
+        while (issued < NS && issued < total) load_next();
     }
     // lane = fp * KW + kl: thread = (key r of the tile, feature part fp)
     constexpr int KW = 32 / TPK;
@@ -646,165 +671,213 @@ __global__ void __launch_bounds__(DecP<D>::NT, DecP<D>::MIN_CTAS)
     const int f0 = fp * 32;
     const float* qf = sq + fp * C::QS;
     const float* rf = sr + fp * C::QS;
-    uint64_t av[16], arv[16];  // sum p v, sum p r v over this thread's keys, as f32x2 pairs
-#pragma unroll
-    for (int i = 0; i < 16; i++) av[i] = arv[i] = 0;
-    float l = 0.f, lr = 0.f, m_run = -INFINITY;
     bool ok = true;
-    for (int j = 0; j < nt; j++) {
-        const int s = j % NS;
-        ok = mbar_wait(&full[s], (j / NS) & 1, wd, 2) && ok;
-        if (!__all_sync(0xffffffffu, ok)) ok = false;
-        const uint8_t* sk = sKV + (2 * s) * C::TB;
-        const uint8_t* sv = sKV + (2 * s + 1) * C::TB;
-        const int key = k_begin + j * KT + r;
-        const bool valid = key < k_end;
-        // q . k and rho . k over this thread's 32 features, summed over the key's threads
-        uint64_t dq[2] = {0, 0}, dr[2] = {0, 0};
+    int n = 0;  // tiles consumed
+    for (int h = h0; h <= h1 && ok; h++) {
+        int tb, tv;
+        range(h, tb, tv);
+        const int len = seq_len1(lens, h / H, Lmax);
+        workers_sync(NT);  // every read of the previous head's q, rho and partial sums is done
+        for (int i = threadIdx.x; i < D; i += NT) {
+            sq[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(q[(size_t)h * D + i]);
+            sr[(i >> 5) * C::QS + (i & 31)] = __bfloat162float(rho[(size_t)h * D + i]);
+        }
+        workers_sync(NT);
+        uint64_t av[16], arv[16];  // sum p v, sum p r v over this thread's keys, as f32x2 pairs
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-            const uint4 kc = *(const uint4*)(sk + swz(r, f0 + 8 * c, KT));
-            const uint32_t w[4] = {kc.x, kc.y, kc.z, kc.w};
+        for (int i = 0; i < 16; i++) av[i] = arv[i] = 0;
+        float l = 0.f, lr = 0.f, m_run = -INFINITY;
+        for (int t = tb; t < tv; t++, n++) {
+            const int s = n % NS;
+            ok = mbar_wait(&full[s], (n / NS) & 1, wd, 2) && ok;
+            if (!__all_sync(0xffffffffu, ok)) ok = false;
+            const uint8_t* sk = sKV + (2 * s) * C::TB;
+            const uint8_t* sv = sKV + (2 * s + 1) * C::TB;
+            const int key = t * KT + r;
+            const bool valid = key < len;
+            // q . k and rho . k over this thread's 32 features, summed over the key's threads
+            uint64_t dq[2] = {0, 0}, dr[2] = {0, 0};
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const uint64_t kk = f2(bf16_lo(w[e]), bf16_hi(w[e]));
-                const float2 qq = *(const float2*)(qf + 8 * c + 2 * e);
-                const float2 rr = *(const float2*)(rf + 8 * c + 2 * e);
-                dq[c & 1] = ffma2(f2(qq.x, qq.y), kk, dq[c & 1]);
-                dr[c & 1] = ffma2(f2(rr.x, rr.y), kk, dr[c & 1]);
+            for (int c = 0; c < 4; c++) {
+                const uint4 kc = *(const uint4*)(sk + swz(r, f0 + 8 * c, KT));
+                const uint32_t w[4] = {kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const uint64_t kk = f2(bf16_lo(w[e]), bf16_hi(w[e]));
+                    const float2 qq = *(const float2*)(qf + 8 * c + 2 * e);
+                    const float2 rr = *(const float2*)(rf + 8 * c + 2 * e);
+                    dq[c & 1] = ffma2(f2(qq.x, qq.y), kk, dq[c & 1]);
+                    dr[c & 1] = ffma2(f2(rr.x, rr.y), kk, dr[c & 1]);
+                }
+            }
+            const float2 q01 = uf2(fadd2(dq[0], dq[1])), r01 = uf2(fadd2(dr[0], dr[1]));
+            float dot = q01.x + q01.y, rk = r01.x + r01.y;
+#pragma unroll
+            for (int o = KW; o < 32; o <<= 1) {
+                dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                rk += __shfl_xor_sync(0xffffffffu, rk, o);
+            }
+            const float sc = valid ? dot * scale_log2 : -INFINITY;
+            float tmax = sc;
+#pragma unroll
+            for (int o = 1; o < KW; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            // two copies by tile parity: a warp that runs ahead writes the next
+            // tile's maximum while a slower one may still read this tile's
+            float* wm = wmax + (n & 1) * NW;
+            if (lane == 0) wm[warp] = tmax;
+            // every worker has finished tile n - 1 past this barrier: its stage
+            // takes tile n - 1 + NS
+            if (!workers_and(ok, NT)) {
+                ok = false;
+                break;
+            }
+            if (loader && n >= 1 && issued < total && issued == n - 1 + NS) {
+                fence_proxy_async_smem();
+                load_next();
+            }
+            float tm = wm[0];
+#pragma unroll
+            for (int w = 1; w < NW; w++) tm = fmaxf(tm, wm[w]);
+            const float m_new = fmaxf(m_run, tm);
+            if (m_new > m_run + RESCALE_TH) {  // uniform across the CTA
+                const float alpha = fast_exp2_dec(m_run - m_new);
+                m_run = m_new;
+                l *= alpha;
+                lr *= alpha;
+                const uint64_t A2 = f2(alpha, alpha);
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    av[i] = fmul2(av[i], A2);
+                    arv[i] = fmul2(arv[i], A2);
+                }
+            }
+            const float p = valid ? fast_exp2_dec(sc - m_run) : 0.f;
+            const float pr = valid ? p * rk : 0.f;  // a key past the sequence adds nothing (its row may hold anything)
+            if (fp == 0) {
+                l += p;
+                lr += pr;
+            }
+            const uint64_t P2 = f2(p, p), PR2 = f2(pr, pr);
+#pragma unroll
+            for (int c = 0; c < 4 && valid; c++) {  // a row past the sequence may hold NaN: not read
+                const uint4 vc = *(const uint4*)(sv + swz(r, f0 + 8 * c, KT));
+                const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const uint64_t vv = f2(bf16_lo(vw[e]), bf16_hi(vw[e]));
+                    av[4 * c + e] = ffma2(P2, vv, av[4 * c + e]);
+                    arv[4 * c + e] = ffma2(PR2, vv, arv[4 * c + e]);
+                }
             }
         }
-        const float2 q01 = uf2(fadd2(dq[0], dq[1])), r01 = uf2(fadd2(dr[0], dr[1]));
-        float dot = q01.x + q01.y, rk = r01.x + r01.y;
+        if (!ok) break;
+        // the partial of (this CTA, head h): sums over the KW key threads of
+        // each warp by a reduce-scatter (each round a lane keeps half of its
+        // values and adds the partner's copy of that half: 64 - 64 / KW
+        // shuffles in all), then over the warps in shared memory.  Value j of
+        // the 64 (sum p v of feature f0 + j, then sum p r v) ends in lane
+        // kl = j / (64 / KW).
+        float x[64];
 #pragma unroll
-        for (int o = KW; o < 32; o <<= 1) {
-            dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            rk += __shfl_xor_sync(0xffffffffu, rk, o);
+        for (int i = 0; i < 16; i++) {
+            const float2 a2 = uf2(av[i]), b2 = uf2(arv[i]);
+            x[2 * i] = a2.x;
+            x[2 * i + 1] = a2.y;
+            x[32 + 2 * i] = b2.x;
+            x[32 + 2 * i + 1] = b2.y;
         }
-        const float sc = valid ? dot * scale_log2 : -INFINITY;
-        float tmax = sc;
 #pragma unroll
-        for (int o = 1; o < KW; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-        if (lane == 0) wmax[warp] = tmax;
-        // every worker has finished tile j - 1 past this barrier: its stage
-        // takes tile j - 1 + NS
-        if (!workers_and(ok, NW * 32)) {
-            ok = false;
-            break;
-        }
-        if (loader && j >= 1 && issued < nt && issued == j - 1 + NS) {
-            fence_proxy_async_smem();
-            load_tile(issued);
-            issued++;
-        }
-        float tm = wmax[0];
+        for (int o = KW / 2, hs = 32; o >= 1; o >>= 1, hs >>= 1) {
+            const bool upper = (kl & o) != 0;  // this lane keeps the upper half
 #pragma unroll
-        for (int w = 1; w < NW; w++) tm = fmaxf(tm, wmax[w]);
-        const float m_new = fmaxf(m_run, tm);
-        if (m_new > m_run + RESCALE_TH) {  // uniform across the CTA
-            const float alpha = fast_exp2_dec(m_run - m_new);
-            m_run = m_new;
-            l *= alpha;
-            lr *= alpha;
-            const uint64_t A2 = f2(alpha, alpha);
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                av[i] = fmul2(av[i], A2);
-                arv[i] = fmul2(arv[i], A2);
+            for (int i = 0; i < hs; i++) {
+                const float send = upper ? x[i] : x[i + hs];
+                const float keep = upper ? x[i + hs] : x[i];
+                x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
         }
-        const float p = valid ? fast_exp2_dec(sc - m_run) : 0.f;
-        const float pr = valid ? p * rk : 0.f;  // a key past the sequence adds nothing (its row may hold anything)
-        if (fp == 0) {
-            l += p;
-            lr += pr;
+#pragma unroll
+        for (int o = 1; o < KW; o <<= 1) {
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+            lr += __shfl_xor_sync(0xffffffffu, lr, o);
         }
-        const uint64_t P2 = f2(p, p), PR2 = f2(pr, pr);
+        {
+            constexpr int PER = 64 / KW;  // values per lane after the reduce-scatter
+            float* rw = red + warp * (2 * D + 2);
 #pragma unroll
-        for (int c = 0; c < 4 && valid; c++) {  // a row past the sequence may hold NaN: not read
-            const uint4 vc = *(const uint4*)(sv + swz(r, f0 + 8 * c, KT));
-            const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const uint64_t vv = f2(bf16_lo(vw[e]), bf16_hi(vw[e]));
-                av[4 * c + e] = ffma2(P2, vv, av[4 * c + e]);
-                arv[4 * c + e] = ffma2(PR2, vv, arv[4 * c + e]);
+            for (int i = 0; i < PER; i++) {
+                const int j = PER * kl + i;
+                rw[(j < 32 ? f0 + j : D + f0 + j - 32)] = x[i];
+            }
+            if (lane == 0) {
+                rw[2 * D] = l;
+                rw[2 * D + 1] = lr;
             }
         }
-    }
-    // loads issued but not consumed (only after an abort) land before
-    // stage 0 is reused below and before the CTA exits
-    if (loader) {
-        const int consumed = ok ? nt : 0;
-        for (int jj = consumed > issued - NS ? consumed : (issued > NS ? issued - NS : 0); jj < issued; jj++)
-            mbar_wait_drain(&full[jj % NS], (jj / NS) & 1);
-    }
-    ok = workers_and(ok, NW * 32);
-    float* dst = part + ((size_t)bh * gridDim.x + blockIdx.x) * C::PART;
-    float avf[32], arf[32];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const float2 a2 = uf2(av[i]), b2 = uf2(arv[i]);
-        avf[2 * i] = a2.x;
-        avf[2 * i + 1] = a2.y;
-        arf[2 * i] = b2.x;
-        arf[2 * i + 1] = b2.y;
-    }
-#pragma unroll
-    for (int o = 1; o < KW; o <<= 1) {
-        l += __shfl_xor_sync(0xffffffffu, l, o);
-        lr += __shfl_xor_sync(0xffffffffu, lr, o);
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-            avf[i] += __shfl_xor_sync(0xffffffffu, avf[i], o);
-            arf[i] += __shfl_xor_sync(0xffffffffu, arf[i], o);
+        workers_sync(NT);
+        float* dst = part + (size_t)(cta + h) * C::PART;
+        for (int e = threadIdx.x; e < 2 * D + 2; e += NT) {
+            float x = 0.f;
+            for (int w = 0; w < NW; w++) x += red[w * (2 * D + 2) + e];
+            if (e < 2 * D) dst[4 + e] = x;
+            else dst[1 + (e - 2 * D)] = x;  // l, then sum p r
         }
+        if (threadIdx.x == 0) dst[0] = m_run;
     }
-    float* red = (float*)sKV;  // [NW][2 D + 2], stage 0 (every load has landed and been read)
-    if (ok && kl == 0) {
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-            red[warp * (2 * D + 2) + f0 + i] = avf[i];
-            red[warp * (2 * D + 2) + D + f0 + i] = arf[i];
-        }
-        if (lane == 0) {
-            red[warp * (2 * D + 2) + 2 * D] = l;
-            red[warp * (2 * D + 2) + 2 * D + 1] = lr;
-        }
-    }
-    workers_sync(NW * 32);
-    for (int e = threadIdx.x; ok && e < 2 * D + 2; e += NW * 32) {
-        float x = 0.f;
-        for (int w = 0; w < NW; w++) x += red[w * (2 * D + 2) + e];
-        if (e < 2 * D) dst[4 + e] = x;
-        else dst[1 + (e - 2 * D)] = x;  // l, then sum p r
-    }
-    if (threadIdx.x == 0) dst[0] = ok ? m_run : -INFINITY;  // an aborted chunk weighs 0 in the merge
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // an aborted CTA's partials weigh 0 in the merge
+    if (!ok && threadIdx.x == 0)
+        for (int h = h0; h <= h1; h++) part[(size_t)(cta + h) * C::PART] = -INFINITY;
+    // loads issued but not consumed (only after an abort) land before the CTA exits
+    if (loader)
+        for (int jj = issued > NS ? issued - NS : 0; jj < issued; jj++) mbar_wait_drain(&full[jj % NS], (jj / NS) & 1);
 }
 
-// Merge the chunks of one head: m = max m_c, weights 2^(m_c - m), then
-// o = mu_v - (sum p r v) / l + ((sum p r) / l) mu_v and lse.  One thread per feature.
+// Merge the partials of one head: m = max m_c, weights 2^(m_c - m), then
+// o = mu_v - (sum p r v) / l + ((sum p r) / l) mu_v and lse.  One thread per
+// feature.  The partials of head h are those of CTAs c(h ntile) .. c(h ntile +
+// ntile - 1), where c(g) = ((g + 1) N - 1) / G is the CTA whose range holds tile g.
 template <int D>
-__global__ void __launch_bounds__(D) decp_merge(const int* __restrict__ lens, const float* __restrict__ part, int H,
-                                                int Lmax, int chunk, int nchunk, float* __restrict__ lse,
-                                                __nv_bfloat16* __restrict__ out) {
+__global__ void __launch_bounds__(D) decp_merge(const float* __restrict__ part, int ntile, long long G, int N,
+                                                float* __restrict__ lse, __nv_bfloat16* __restrict__ out) {
     using C = DecP<D>;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int bh = blockIdx.x, b = bh / H, e = threadIdx.x;
-    const int len = seq_len1(lens, b, Lmax);
-    const int nc = min(nchunk, (len + chunk - 1) / chunk);
-    const float* pb = part + (size_t)bh * nchunk * C::PART;
-    float m = -INFINITY;
-    for (int c = 0; c < nc; c++) m = fmaxf(m, pb[(size_t)c * C::PART]);
-    float l = 0.f, lr = 0.f, pv = 0.f, prv = 0.f;
-    for (int c = 0; c < nc; c++) {
-        const float* pc = pb + (size_t)c * C::PART;
-        const float w = exp2f(pc[0] - m);
-        l = fmaf(w, pc[1], l);
-        lr = fmaf(w, pc[2], lr);
-        pv = fmaf(w, pc[4 + e], pv);
-        prv = fmaf(w, pc[4 + D + e], prv);
+    const int bh = blockIdx.x, e = threadIdx.x;
+    const long long ga = (long long)bh * ntile, gb = ga + ntile - 1;
+    const int ca = (int)(((ga + 1) * N - 1) / G), cb = (int)(((gb + 1) * N - 1) / G);
+    // every load of a partial is issued before any of them is used: a few
+    // partials per head, so the merge costs one round trip
+    constexpr int MAXP = 8;
+    float pm[MAXP], pl[MAXP], plr[MAXP], ppv[MAXP], pprv[MAXP];
+    float m = -INFINITY, l = 0.f, lr = 0.f, pv = 0.f, prv = 0.f;
+    for (int c0 = ca; c0 <= cb; c0 += MAXP) {
+#pragma unroll
+        for (int i = 0; i < MAXP; i++) {
+            const float* pc = part + (size_t)(c0 + i + bh) * C::PART;
+            const bool in = c0 + i <= cb;
+            pm[i] = in ? pc[0] : -INFINITY;
+            pl[i] = in ? pc[1] : 0.f;
+            plr[i] = in ? pc[2] : 0.f;
+            ppv[i] = in ? pc[4 + e] : 0.f;
+            pprv[i] = in ? pc[4 + D + e] : 0.f;
+        }
+        float mm = m;
+#pragma unroll
+        for (int i = 0; i < MAXP; i++) mm = fmaxf(mm, pm[i]);
+        const float a = m == -INFINITY ? 0.f : exp2f(m - mm);  // rescale what is summed so far
+        l *= a;
+        lr *= a;
+        pv *= a;
+        prv *= a;
+#pragma unroll
+        for (int i = 0; i < MAXP; i++) {
+            if (pm[i] == -INFINITY) continue;  // no keys of this head in that CTA
+            const float w = exp2f(pm[i] - mm);
+            l = fmaf(w, pl[i], l);
+            lr = fmaf(w, plr[i], lr);
+            pv = fmaf(w, ppv[i], pv);
+            prv = fmaf(w, pprv[i], prv);
+        }
+        m = mm;
     }
     const float inv = 1.f / l;
     const float mv = pv * inv;
@@ -905,8 +978,6 @@ cudaError_t decode_tc_impl(const DecodeArgs& a) {
 
 
 // ---- given-probe decode
-size_t decp_nchunk_max(size_t BH, int Lmax) { return dec1_nchunk_max(BH, Lmax); }
-
 template <int D>
 cudaError_t decode_probe_impl(const DecodeArgs& a) {
     using C = DecP<D>;
@@ -927,27 +998,22 @@ cudaError_t decode_probe_impl(const DecodeArgs& a) {
         }
         sms = sms_cache[dev];
     }
-    // one wave of resident CTAs: chunks per head, rounded to whole tiles
-    const size_t cap = decp_nchunk_max(BH, a.Lmax);
-    size_t per_head = (size_t)sms * C::MIN_CTAS / BH;
-    if (per_head < 1) per_head = 1;
-    if (per_head > cap) per_head = cap;
-    int chunk = (int)((a.Lmax + per_head - 1) / per_head);
-    chunk = (chunk + C::KT - 1) / C::KT * C::KT;
-    const int nchunk = (a.Lmax + chunk - 1) / chunk;
+    // the tiles of all heads split evenly over one wave of resident CTAs
+    const int ntile = (a.Lmax + C::KT - 1) / C::KT;
+    const long long G = (long long)BH * ntile;
+    const int N = (int)std::min<long long>(std::min<long long>((long long)sms * C::MIN_CTAS, G), kMaxCtas);
     CUtensorMap mk, mv;
     if (!tc_make_map(&mk, a.k, D, a.Lmax, BH, C::KT) || !tc_make_map(&mv, a.v, D, a.Lmax, BH, C::KT))
         return cudaErrorInvalidValue;
     const float scale_log2 = LOG2E / sqrtf((float)D);
     float* part = (float*)a.ws;
     timing_begin(a.stream, "decp_chunk");
-    decp_chunk<D><<<dim3(nchunk, BH), C::NT, C::SMEM, a.stream>>>(mk, mv, (const __nv_bfloat16*)a.q,
-                                                                   (const __nv_bfloat16*)a.rho, a.lens, a.H, a.Lmax,
-                                                                   chunk, scale_log2, part, a.status);
+    decp_chunk<D><<<N, C::NT, C::SMEM, a.stream>>>(mk, mv, (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.rho,
+                                                   a.lens, a.H, a.Lmax, ntile, G, scale_log2, part, a.status);
     timing_end(a.stream);
     PLX_TRY(cudaGetLastError());
     timing_begin(a.stream, "decp_merge");
-    {  // programmatic dependent launch, as for the committed-probe merge
+    {  // programmatic dependent launch: the chunk kernel releases it at its start
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(BH);
         cfg.blockDim = dim3(D);
@@ -958,8 +1024,8 @@ cudaError_t decode_probe_impl(const DecodeArgs& a) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        PLX_TRY(cudaLaunchKernelEx(&cfg, decp_merge<D>, (const int*)a.lens, (const float*)part, a.H, a.Lmax, chunk,
-                                   nchunk, a.lse, (__nv_bfloat16*)a.out));
+        PLX_TRY(cudaLaunchKernelEx(&cfg, decp_merge<D>, (const float*)part, ntile, G, N, a.lse,
+                                   (__nv_bfloat16*)a.out));
     }
     timing_end(a.stream);
     return cudaGetLastError();
@@ -978,9 +1044,10 @@ cudaError_t decode_tc(const DecodeArgs& a) {
 }
 
 size_t decode_probe_ws_bytes(int B, int H, int Lmax, int d) {
+    (void)Lmax;
     const size_t BH = (size_t)B * H;
     const size_t part = d == 64 ? (size_t)DecP<64>::PART : (size_t)DecP<128>::PART;
-    return align256(BH * decp_nchunk_max(BH, Lmax) * part * sizeof(float));
+    return align256((kMaxCtas + BH) * part * sizeof(float));  // slots c + h, c < kMaxCtas
 }
 
 cudaError_t decode_probe(const DecodeArgs& a) {
