@@ -1520,7 +1520,8 @@ __global__ void __launch_bounds__(ProbeCfg<D>::NT, ProbeCfg<D>::MIN_BLOCKS)
 //          gbar = mu_k . U (from the rounded U, so that sum_i p_i (g_i - gbar)
 //          vanishes for the values pass 2's MMA sees).
 //   MODE 1 (backward B2): the same u, du = R - ebar mu_k, ddelta = P_h^T du,
-//          dq_acc = ddelta, dmu = f16(-ddelta), the row scalars B3 needs
+//          dq_acc = ddelta, z = f16(dmu - ebar U) with dmu = -ddelta (B3's
+//          operand in place of dmu: k . z = y - ebar g), the row scalars B3 needs
 //          {-lse log2 e, 1 - mu_k . U, -ebar, -D} (stored by query pairs) with
 //          D = do.o - gbar ebar + mu_k . dmu and do.o = ebar + R.u - gbar ebar
 //          (rebuilt from B1's fp32 sums, gbar = mu_k . u in fp32), and this
@@ -1726,9 +1727,12 @@ __global__ void __launch_bounds__(256) tc_rows(const __nv_bfloat16* __restrict__
                 else
                     *(uint4*)&U[off] = make_uint4(uh[0], uh[1], uh[2], uh[3]);
                 if (MODE) {
+                    const float eb = ebar[row];
                     uint32_t mh[NC / 2];
 #pragma unroll
-                    for (int j = 0; j < NC; j += 2) mh[j / 2] = pack_f16(-dd[i][j], -dd[i][j + 1]);
+                    for (int j = 0; j < NC; j += 2)
+                        mh[j / 2] = pack_f16(fmaf(-eb, f16_lo(uh[j / 2]), -dd[i][j]),
+                                             fmaf(-eb, f16_hi(uh[j / 2]), -dd[i][j + 1]));
                     if (NC == 4)
                         *(uint2*)&dmu[off] = make_uint2(mh[0], mh[1]);
                     else
@@ -2041,8 +2045,9 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
                                                   __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
         }
         __syncthreads();
-        // per item: U (f16), dmu = -ddelta (f16), dq_acc = ddelta, and the row
-        // sums gr = mu_k . f16(U), gb = mu_k . U, ru = R . U, xx = -mu_k . ddelta
+        // per item: U (f16), z = dmu - ebar U (f16, dmu = -ddelta), dq_acc =
+        // ddelta, and the row sums gr = mu_k . f16(U), gb = mu_k . U, ru = R . U,
+        // xx = mu_k . dmu
 #pragma unroll 2
         for (int kb = 0; kb < C::ITEMS; kb += 4) {
             float4 mv[4], rv[4];
@@ -2090,10 +2095,12 @@ __global__ void __launch_bounds__(B2T::NT, 2) tc_b2(const __half* __restrict__ q
                     const size_t base = row[e] * D + 4 * qd;
                     *(float4*)(dq_acc + base) = d4;
                     *(uint2*)(U + base) = make_uint2(uh0, uh1);
-                    *(uint2*)(dmu + base) = make_uint2(pack_f16(-d4.x, -d4.y), pack_f16(-d4.z, -d4.w));
+                    const float eb = sEb[rl[e]];
+                    *(uint2*)(dmu + base) =
+                        make_uint2(pack_f16(fmaf(-eb, f16_lo(uh0), -d4.x), fmaf(-eb, f16_hi(uh0), -d4.y)),
+                                   pack_f16(fmaf(-eb, f16_lo(uh1), -d4.z), fmaf(-eb, f16_hi(uh1), -d4.w)));
                     if (qd == 0) {
                         // paired row scalars {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o}
-                        const float eb = sEb[rl[e]];
                         const float doo = eb + ru - gb * eb;
                         const int r = cur.r0 + rl[e], tt = r % T, hp = tt & 1;
                         float* prow = rowpack + (((size_t)(r / T) * H + h) * ((T + 1) / 2) + tt / 2) * 8 + hp;
@@ -2145,11 +2152,13 @@ __global__ void __launch_bounds__(256) tc_dp_reduce(const float4* __restrict__ p
 // ============================================================ backward B3
 // CTA = one tile of 128 keys of one head; queries stream in sub-chunks of 64.
 // Per sub-chunk (TMEM lanes = keys i, columns = queries t):
-//   [S^T | G^T | Y^T] = K [Q | U | dmu]^T   (one N = 192 MMA: K is read once)
+//   [S^T | G^T | Y^T] = K [Q | U | z]^T     (one N = 192 MMA: K is read once)
 //   E^T = V dO^T
-//   p = exp(c s - lse_t), w1 = 1 + g - gbar_t, a = p w1, dg = p (e - ebar_t),
-//   ds = c p (e w1 - g ebar_t + y - D_t)
-//   dV += a dO, dK += dg U + ds Q + p dmu      (A operands f16 in TMEM)
+//   p = exp(c s - lse_t), w1 = 1 + g - gbar_t, a = p w1, pe = p e,
+//   ds = c p (e w1 + y - D_t)      (y = k . z = k . dmu - g ebar_t)
+//   dV += a dO, dK += pe U + ds Q + p z        (A operands f16 in TMEM)
+// The dK sum is p (e - ebar_t) U + ds Q + p dmu written with z = dmu - ebar_t U,
+// which B2 stores in place of dmu: the ebar_t terms leave the per-element step.
 // and per 128 queries dQ += ds^T K (A = ds from shared memory), added into the
 // fp32 dq accumulator with vector reductions.  Two warpgroups split the
 // elementwise work by query columns.
@@ -2180,7 +2189,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // The elementwise step for 16 queries (one 16-column chunk) of one key row,
 // two queries per f32x2 instruction.  rp points at the chunk's first query
 // pair: {-L_e, -L_o, g1_e, g1_o, -ebar_e, -ebar_o, -D_e, -D_o} per pair, with
-// L = lse log2 e and g1 = 1 - gbar.
+// L = lse log2 e and g1 = 1 - gbar (-ebar is not needed here: see z above).
 template <bool MASK>
 __device__ __forceinline__ void b3_chunk(const uint32_t (&vs)[16], const uint32_t (&vg)[16], const uint32_t (&vy)[16],
                                          const uint32_t (&ve)[16], const float* rp, int qlo, float scale,
@@ -2190,7 +2199,7 @@ __device__ __forceinline__ void b3_chunk(const uint32_t (&vs)[16], const uint32_
     for (int q2 = 0; q2 < 8; q2++) {
         const float4 ra = *(const float4*)(rp + 8 * q2);
         const float4 rb = *(const float4*)(rp + 8 * q2 + 4);
-        const uint64_t nL = f2(ra.x, ra.y), g1 = f2(ra.z, ra.w), nE = f2(rb.x, rb.y), nD = f2(rb.z, rb.w);
+        const uint64_t nL = f2(ra.x, ra.y), g1 = f2(ra.z, ra.w), nD = f2(rb.z, rb.w);
         const uint64_t sv = f2(__uint_as_float(vs[2 * q2]), __uint_as_float(vs[2 * q2 + 1]));
         const uint64_t g = f2(__uint_as_float(vg[2 * q2]), __uint_as_float(vg[2 * q2 + 1]));
         const uint64_t y = f2(__uint_as_float(vy[2 * q2]), __uint_as_float(vy[2 * q2 + 1]));
@@ -2204,13 +2213,12 @@ __device__ __forceinline__ void b3_chunk(const uint32_t (&vs)[16], const uint32_
         const uint64_t p = f2(p0, p1);
         const uint64_t w1 = fadd2(g, g1);                    // 1 + g - gbar
         const float2 a = uf2(fmul2(p, w1));                  // p w1
-        const float2 dg = uf2(fmul2(p, fadd2(e, nE)));       // p (e - ebar)
-        uint64_t tt = fadd2(y, nD);                          // y - D
-        tt = ffma2(g, nE, tt);                               // - g ebar
+        const float2 pe = uf2(fmul2(p, e));                  // p e
+        uint64_t tt = fadd2(y, nD);                          // k.z - D
         tt = ffma2(e, w1, tt);                               // + e w1
         const float2 ds = uf2(fmul2(fmul2(p, SC), tt));      // c p (...)
         o1[q2] = pack_f16(a.x, a.y);
-        o1[8 + q2] = pack_f16(dg.x, dg.y);
+        o1[8 + q2] = pack_f16(pe.x, pe.y);
         o2[q2] = pack_f16(ds.x, ds.y);
         o2[8 + q2] = pack_f16(p0, p1);
     }
@@ -2391,7 +2399,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
                 tmem_ld16(tY + lrow + 16 * c, vy);
                 tmem_ld16(tE + lrow + 16 * c, ve);
                 tmem_wait_ld();
-                uint32_t o1[16], o2[16];  // o1: a | dg, o2: ds | p (f16 pairs)
+                uint32_t o1[16], o2[16];  // o1: a | pe, o2: ds | p (f16 pairs)
                 if (need_mask) {
                     // query t = t0 + 16 c + qq is valid iff key <= t and t < T
                     const int qlo = max(key - (t0 + 16 * c), 0);
@@ -2489,7 +2497,7 @@ __global__ void __launch_bounds__(B3Cfg<D>::NT, 1)
 // elementwise warpgroups (queries [0,32) and [32,64) of each sub-chunk) load
 // their scores into registers and arrive on sx_free; the MMA thread then
 // issues the next sub-chunk's scores while they form the weights.  The weights
-// have storage of their own: a | dg in TMEM, ds and p in shared memory (ds in
+// have storage of their own: a | pe in TMEM, ds and p in shared memory (ds in
 // the 128-query tile the dQ product reads as well), so the accumulation of
 // sub-chunk j reads them while the scores of j + 1 occupy the score region.
 // dQ of each 128-query tile is read after the elementwise step of the next
@@ -2739,7 +2747,7 @@ __global__ void __launch_bounds__(B3Q::NT, 1)
                 tmem_ld16(tSc + lrow + 192 + 16 * c, ve);
                 tmem_wait_ld();
             };
-            auto weights = [&](int c, uint32_t(&o1)[16], uint32_t(&o2)[16]) {  // o1: a | dg, o2: ds | p
+            auto weights = [&](int c, uint32_t(&o1)[16], uint32_t(&o2)[16]) {  // o1: a | pe, o2: ds | p
                 if (need_mask) {
                     // query t = t0 + 16 c + qq is valid iff key <= t and t < T
                     const int qlo = max(key - (t0 + 16 * c), 0);
