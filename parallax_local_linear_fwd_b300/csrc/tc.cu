@@ -2854,6 +2854,274 @@ __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src
     }
 }
 
+// ============================================ pass 2 at d = 128, 128-key tiles
+// Forward pass 2 with key tiles of 128, so S = c Q K^T and G = U K^T are
+// N = 128 MMAs (the full tensor rate) and Acc += W V is one N = 128 chain of
+// eight.  One 128-row query tile per CTA; TMEM holds S [0,128), X [128,256),
+// the f16 weights W [256,320) and Acc [320,448) in columns of their own, so
+// the MMA thread issues the next key tile's S and X as soon as the
+// elementwise warps hold this tile's (before they have formed W), and the
+// accumulation after them.  Two elementwise warpgroups split each tile's keys
+// (64 each).  K and V have rings of their own: K(j) is free once S(j), X(j)
+// have run, V(j) once Acc += W(j) V(j) has, so each is refilled as early as
+// its last reader allows.
+struct DualW {
+    static constexpr int D = 128, BM = 128, BN = 128, NT = 320;
+    static constexpr int AB = BM * D * 2;  // one A tile (Q or U): 32 KB
+    static constexpr int KB = BN * D * 2;  // one K or V tile: 32 KB
+    static constexpr int NS = 2;           // K stages, and V stages
+    static constexpr int NBAR = 1 + 4 * NS + 6;
+    static constexpr int SMEM = 1024 + 2 * AB + 2 * NS * KB + NBAR * 8 + 16;
+    static constexpr unsigned TMEM_COLS = 512;  // S [0,128), X [128,256), W [256,320), Acc [320,448)
+    static_assert(SMEM <= 232448, "one CTA per SM must fit");
+};
+
+__global__ void __launch_bounds__(DualW::NT, 1)
+    tc_dual_w(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
+              const float* __restrict__ gbar, int T, int BH, int ntq, float scale_log2, unsigned* status) {
+    using C = DualW;
+    constexpr int NS = C::NS, D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* sA1 = sm;
+    uint8_t* sA2 = sA1 + C::AB;
+    uint8_t* sK = sA2 + C::AB;          // K stage s at s KB
+    uint8_t* sV = sK + NS * C::KB;      // V stage s at s KB
+    uint64_t* bars = (uint64_t*)(sV + NS * C::KB);
+    uint64_t* a_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + NS;
+    uint64_t* v_full = k_empty + NS;
+    uint64_t* v_empty = v_full + NS;
+    uint64_t* s_full = v_empty + NS;    // S and X of the tile are in TMEM
+    uint64_t* sx_free = s_full + 1;     // the elementwise warps hold them in registers (256 arrivals)
+    uint64_t* w_full = s_full + 2;      // W of the tile is written (256 arrivals)
+    uint64_t* w_free = s_full + 3;      // the accumulation has read W
+    uint64_t* acc_done = s_full + 4;
+    uint64_t* drain = s_full + 5;
+    uint32_t* holder = (uint32_t*)(bars + C::NBAR);
+    volatile int* abortf = (volatile int*)(holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int rank, bh;
+    work_item(blockIdx.x, BH, ntq, &rank, &bh);
+    const int qt = ntq - 1 - rank;  // longest query tiles first
+    const int q0 = qt * C::BM;
+    const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
+    const Watchdog wd{status, abortf, (unsigned)KID_TC_PASS2, wait_limit(status)};
+
+    if (threadIdx.x == 0) {
+        *abortf = 0;
+        mbar_init(a_full, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(sx_free, 256);
+        mbar_init(w_full, 256);
+        mbar_init(w_free, 1);
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t tS = tmem, tX = tmem + 128, tW = tmem + 256, tAcc = tmem + 320;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_a1);
+            prefetch_tmap(&tm_a2);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(a_full, 2 * C::AB);
+#pragma unroll
+            for (int r = 0; r < D / 64; r++) {
+                tma_load_3d(sA1 + r * C::BM * 128, &tm_a1, r * 64, q0, bh, a_full);
+                tma_load_3d(sA2 + r * C::BM * 128, &tm_a2, r * 64, q0, bh, a_full);
+            }
+            int kiss = 0, viss = 0;
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&k_full[s], C::KB);
+#pragma unroll
+                for (int r = 0; r < D / 64; r++)
+                    tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
+                kiss = j + 1;
+                if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
+                mbar_expect_tx(&v_full[s], C::KB);
+#pragma unroll
+                for (int r = 0; r < D / 64; r++)
+                    tma_load_3d(sV + s * C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &v_full[s]);
+                viss = j + 1;
+            }
+            mbar_wait_drain(a_full, 0);
+            for (int j = kiss > NS ? kiss - NS : 0; j < kiss; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
+            for (int j = viss > NS ? viss - NS : 0; j < viss; j++) mbar_wait_drain(&v_full[j % NS], (j / NS) & 1);
+        }
+    } else if (warp == 1) {
+        // The whole warp runs the loop, so the descriptors stay warp-uniform;
+        // the elected lane (lane 0 of the converged warp) issues every tcgen05
+        // instruction, so one thread issues all MMAs, in order.
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        const uint32_t idA = idesc_mma(128, D, false, true);
+        const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
+        auto scores = [&](int j) {  // S = Q K_j^T, X = U K_j^T
+            const uint32_t kaddr = smem_u32(sK + (j % NS) * C::KB);
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                mma_commit(s_full);
+                mma_commit(&k_empty[j % NS]);  // K(j) has no other reader
+            }
+            __syncwarp();
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2)) &&
+                  __all_sync(0xffffffffu, mbar_wait(&k_full[0], 0, wd, 3));
+        if (ok) scores(0);
+        for (int j = 0; ok && j < nkt; j++) {
+            const int s = j % NS;
+            if (j + 1 < nkt) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
+                // tile j's S and X are in registers: tile j + 1's may overwrite them
+                if (!__all_sync(0xffffffffu, mbar_wait(sx_free, j & 1, wd, 9))) break;
+                scores(j + 1);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / NS) & 1, wd, 4))) break;
+            tc_fence_after();
+            const uint32_t vaddr = smem_u32(sV + s * C::KB);
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; kk++)
+                    mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
+                mma_commit(w_free);
+                mma_commit(&v_empty[s]);
+            }
+            __syncwarp();
+        }
+        if (elect_one()) mma_commit(drain);
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
+    } else {
+        const int wg = (warp - 2) >> 2;  // keys [64 wg, 64 wg + 64) of every tile
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int t = q0 + row;
+        const uint32_t lrow = (uint32_t)(qd * 32) << 16;
+        const bool valid = t < T;
+        const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
+        const float g1 = valid ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
+        const uint64_t SL2 = f2(scale_log2, scale_log2), NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            ok = mbar_wait(s_full, j & 1, wd, 6);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = j * C::BN;
+            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+            const bool need_mask = lim < C::BN;
+            // W of one 32-key chunk c: w = p (x + 1 - gbar), p = exp2(c s - L)
+            auto weights = [&](int c, const uint32_t(&vs)[32], const uint32_t(&vx)[32], uint32_t(&pk)[16]) {
+#pragma unroll
+                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
+                    const int cc = c * 32 + 2 * i;
+                    const float2 xs =
+                        uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NL2));
+                    float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
+                    if (need_mask) {
+                        if (cc > lim) p0 = 0.f;
+                        if (cc + 1 > lim) p1 = 0.f;
+                    }
+                    const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
+                    const float2 w = uf2(fmul2(f2(p0, p1), fadd2(xv, G1)));
+                    pk[i] = pack_f16(w.x, w.y);
+                }
+            };
+            const int c0 = 2 * wg, c1 = 2 * wg + 1;
+            uint32_t pk0[16], pk1[16];
+            {
+                uint32_t vs[32], vx[32];
+                tmem_ld32(tS + lrow + c0 * 32, vs);
+                tmem_ld32(tX + lrow + c0 * 32, vx);
+                tmem_wait_ld();
+                weights(c0, vs, vx, pk0);
+            }
+            {
+                uint32_t vs[32], vx[32];
+                tmem_ld32(tS + lrow + c1 * 32, vs);
+                tmem_ld32(tX + lrow + c1 * 32, vx);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(sx_free);  // S and X of the tile this thread needs are in registers
+                weights(c1, vs, vx, pk1);
+            }
+            if (j > 0) ok = mbar_wait(w_free, (j - 1) & 1, wd, 10);  // the previous accumulation read W
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st16(tW + lrow + c0 * 16, pk0);
+            tmem_st16(tW + lrow + c1 * 16, pk1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(w_full);
+        }
+        if (ok) ok = mbar_wait(acc_done, 0, wd, 8);
+        // each warpgroup stores 64 output columns through its half of the freed Q slot
+        ok = named_bar_and(1 + wg, 128, ok);
+        if (ok) {
+            tc_fence_after();
+            uint8_t* slot = sA1 + wg * (C::BM * 128);
+#pragma unroll 1
+            for (int c = 0; c < 2; c++) {
+                uint32_t v[32];
+                tmem_ld32(tAcc + lrow + 64 * wg + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    *(uint4*)(slot + sw_off(row, c * 32 + 8 * i, C::BM)) =
+                        make_uint4(pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                                   pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                   pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                   pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + wg, 128);
+            if (qd == 0 && lane == 0) {
+                tma_store_3d(&tm_out, 64 * wg, q0, bh, slot);
+                bulk_commit();
+                bulk_wait_all();  // the slot stays valid until the store has read it
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
 // ================================================================= host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -3014,13 +3282,13 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cud
         PLX_TRY(cudaGetLastError());
     }
     if (after_pass1) PLX_TRY(after_pass1());
-    if constexpr (D == 128) {  // pass 2: two query tiles per CTA sharing the K|V stages
-        using C = DualPP<D>;
-        const int npairs = ((a.T + C::BM - 1) / C::BM + 1) / 2;
-        PLX_TRY(cudaFuncSetAttribute(tc_dual_pp<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    if constexpr (D == 128) {  // pass 2: 128-key tiles, S, X, W and Acc in TMEM columns of their own
+        using C = DualW;
+        const int ntq = (a.T + C::BM - 1) / C::BM;
+        PLX_TRY(cudaFuncSetAttribute(tc_dual_w, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual_pp<D, 0><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, mout, a.lse, w.gbar,
-                                                                     nullptr, a.T, BH, npairs, scale_log2, a.status);
+        tc_dual_w<<<ntq * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk16_128, mv16_128, mout, a.lse, w.gbar,
+                                                          a.T, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // pass 2
