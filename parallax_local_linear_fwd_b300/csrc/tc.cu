@@ -2859,18 +2859,19 @@ __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src
 // N = 128 MMAs (the full tensor rate) and Acc += W V is one N = 128 chain of
 // eight.  One 128-row query tile per CTA; TMEM holds S [0,128), X [128,256),
 // the f16 weights W [256,320) and Acc [320,448) in columns of their own, so
-// the MMA thread issues the next key tile's S and X as soon as the
-// elementwise warps hold this tile's (before they have formed W), and the
-// accumulation after them.  Two elementwise warpgroups split each tile's keys
+// the MMA thread issues the next key tile's S as soon as the elementwise warps
+// hold this tile's S in registers, its X once they hold X, and the
+// accumulation after them: the scores of tile j + 1 run while tile j's
+// weights are formed.  Two elementwise warpgroups split each tile's keys
 // (64 each).  K and V have rings of their own: K(j) is free once S(j), X(j)
 // have run, V(j) once Acc += W(j) V(j) has, so each is refilled as early as
 // its last reader allows.
 struct DualW {
-    static constexpr int D = 128, BM = 128, BN = 128, NT = 320;
+    static constexpr int D = 128, BM = 128, BN = 128, NT = 352;  // TMA, S|X MMA, 8 elementwise, Acc MMA
     static constexpr int AB = BM * D * 2;  // one A tile (Q or U): 32 KB
     static constexpr int KB = BN * D * 2;  // one K or V tile: 32 KB
     static constexpr int NS = 2;           // K stages, and V stages
-    static constexpr int NBAR = 1 + 4 * NS + 6;
+    static constexpr int NBAR = 1 + 4 * NS + 7;
     static constexpr int SMEM = 1024 + 2 * AB + 2 * NS * KB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 512;  // S [0,128), X [128,256), W [256,320), Acc [320,448)
     static_assert(SMEM <= 232448, "one CTA per SM must fit");
@@ -2896,11 +2897,12 @@ __global__ void __launch_bounds__(DualW::NT, 1)
     uint64_t* v_full = k_empty + NS;
     uint64_t* v_empty = v_full + NS;
     uint64_t* s_full = v_empty + NS;    // S and X of the tile are in TMEM
-    uint64_t* sx_free = s_full + 1;     // the elementwise warps hold them in registers (256 arrivals)
-    uint64_t* w_full = s_full + 2;      // W of the tile is written (256 arrivals)
-    uint64_t* w_free = s_full + 3;      // the accumulation has read W
-    uint64_t* acc_done = s_full + 4;
-    uint64_t* drain = s_full + 5;
+    uint64_t* s_free = s_full + 1;      // the elementwise warps hold S in registers (256 arrivals)
+    uint64_t* x_free = s_full + 2;      // ... and X (256 arrivals)
+    uint64_t* w_full = s_full + 3;      // W of the tile is written (256 arrivals)
+    uint64_t* w_free = s_full + 4;      // the accumulation has read W
+    uint64_t* acc_done = s_full + 5;
+    uint64_t* drain = s_full + 6;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
 
@@ -2922,11 +2924,12 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             mbar_init(&v_empty[s], 1);
         }
         mbar_init(s_full, 1);
-        mbar_init(sx_free, 256);
+        mbar_init(s_free, 256);
+        mbar_init(x_free, 256);
         mbar_init(w_full, 256);
         mbar_init(w_free, 1);
         mbar_init(acc_done, 1);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(holder, C::TMEM_COLS);
@@ -2968,54 +2971,59 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             for (int j = kiss > NS ? kiss - NS : 0; j < kiss; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
             for (int j = viss > NS ? viss - NS : 0; j < viss; j++) mbar_wait_drain(&v_full[j % NS], (j / NS) & 1);
         }
-    } else if (warp == 1) {
-        // The whole warp runs the loop, so the descriptors stay warp-uniform;
-        // the elected lane (lane 0 of the converged warp) issues every tcgen05
-        // instruction, so one thread issues all MMAs, in order.
-        const uint32_t idS = idesc_mma(128, C::BN, false, false);
-        const uint32_t idA = idesc_mma(128, D, false, true);
-        const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
-        auto scores = [&](int j) {  // S = Q K_j^T, X = U K_j^T
-            const uint32_t kaddr = smem_u32(sK + (j % NS) * C::KB);
-            tc_fence_after();
-            if (elect_one()) {
+    } else if (warp == 1 || warp == C::NT / 32 - 1) {
+        // Two issuing warps: warp 1 issues S and X, the last warp the
+        // accumulation, so one warp's barrier waits overlap the other's MMAs.
+        // They share no TMEM or shared memory a later MMA of the other
+        // overwrites (K(j) and V(j) have rings of their own).  In each warp
+        // the elected lane (lane 0 of the converged warp) issues all of its
+        // tcgen05 instructions, in order.
+        if (warp == 1) {
+            const uint32_t idS = idesc_mma(128, C::BN, false, false);
+            const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
+            auto product = [&](int j, uint32_t acc_col, uint32_t a, bool last) {  // S = Q K_j^T or X = U K_j^T
+                const uint32_t kaddr = smem_u32(sK + (j % NS) * C::KB);
+                tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(acc_col, desc_kmajor(a, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                    if (last) {
+                        mma_commit(s_full);
+                        mma_commit(&k_empty[j % NS]);  // K(j) has no other reader
+                    }
+                }
+                __syncwarp();
+            };
+            bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2));
+            for (int j = 0; ok && j < nkt; j++) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[j % NS], (j / NS) & 1, wd, 3))) break;
+                // tile j - 1's S is in registers: tile j's may overwrite it; then X likewise
+                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(s_free, (j - 1) & 1, wd, 9))) break;
+                product(j, tS, a1, false);
+                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(x_free, (j - 1) & 1, wd, 11))) break;
+                product(j, tX, a2, true);
+            }
+        } else {
+            const uint32_t idA = idesc_mma(128, D, false, true);
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / NS) & 1, wd, 4))) break;
+                tc_fence_after();
+                const uint32_t vaddr = smem_u32(sV + s * C::KB);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
-                mma_commit(s_full);
-                mma_commit(&k_empty[j % NS]);  // K(j) has no other reader
+                    for (int kk = 0; kk < C::BN / 16; kk++)
+                        mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
+                    mma_commit(w_free);
+                    mma_commit(&v_empty[s]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2)) &&
-                  __all_sync(0xffffffffu, mbar_wait(&k_full[0], 0, wd, 3));
-        if (ok) scores(0);
-        for (int j = 0; ok && j < nkt; j++) {
-            const int s = j % NS;
-            if (j + 1 < nkt) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
-                // tile j's S and X are in registers: tile j + 1's may overwrite them
-                if (!__all_sync(0xffffffffu, mbar_wait(sx_free, j & 1, wd, 9))) break;
-                scores(j + 1);
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
-            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / NS) & 1, wd, 4))) break;
-            tc_fence_after();
-            const uint32_t vaddr = smem_u32(sV + s * C::KB);
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; kk++)
-                    mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
-                mma_commit(w_free);
-                mma_commit(&v_empty[s]);
-            }
-            __syncwarp();
         }
-        if (elect_one()) mma_commit(drain);
+        if (elect_one()) mma_commit(drain);  // one arrival per issuing warp
         __syncwarp();
         mbar_wait_drain(drain, 0);
     } else {
@@ -3058,21 +3066,25 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             };
             const int c0 = 2 * wg, c1 = 2 * wg + 1;
             uint32_t pk0[16], pk1[16];
+            uint32_t vs0[32], vs1[32];
+            tmem_ld32(tS + lrow + c0 * 32, vs0);
+            tmem_ld32(tS + lrow + c1 * 32, vs1);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(s_free);  // S of the tile this thread needs is in registers
             {
-                uint32_t vs[32], vx[32];
-                tmem_ld32(tS + lrow + c0 * 32, vs);
+                uint32_t vx[32];
                 tmem_ld32(tX + lrow + c0 * 32, vx);
                 tmem_wait_ld();
-                weights(c0, vs, vx, pk0);
+                weights(c0, vs0, vx, pk0);
             }
             {
-                uint32_t vs[32], vx[32];
-                tmem_ld32(tS + lrow + c1 * 32, vs);
+                uint32_t vx[32];
                 tmem_ld32(tX + lrow + c1 * 32, vx);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(sx_free);  // S and X of the tile this thread needs are in registers
-                weights(c1, vs, vx, pk1);
+                mbar_arrive(x_free);  // ... and X
+                weights(c1, vs1, vx, pk1);
             }
             if (j > 0) ok = mbar_wait(w_free, (j - 1) & 1, wd, 10);  // the previous accumulation read W
             if (!__all_sync(0xffffffffu, ok)) {
