@@ -748,12 +748,13 @@ struct DualCfg {
     static constexpr int AB = BM * D * 2;       // one A tile (Q, U or dO)
     static constexpr int KB = BN * D * 2;       // one K or V tile
     static constexpr int NBAR = 1 + 2 * NS + 4 + 2;  // + sx_free, w_free
+    static constexpr int NT = 224;  // TMA warp, S|X MMA warp, 4 elementwise warps, accumulation MMA warp
     static constexpr int SMEM = 1024 + 2 * AB + NS * 2 * KB + NBAR * 8 + 16;
     static constexpr unsigned TMEM_COLS = 256;  // S [0,64), X [64,128), W [128,160), Acc [160,160+D)
 };
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(DualCfg<D>::NT, 2)
     tc_dual(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
             const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
@@ -793,12 +794,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mbar_init(a_full, 1);
         for (int s = 0; s < NS; s++) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&kv_empty[s], 2);  // a commit from each issuing warp
         }
         mbar_init(s_full, 1);
         mbar_init(w_full, 128);
         mbar_init(acc_done, 1);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         mbar_init(sx_free, 128);
         mbar_init(w_free, 1);
         fence_barrier_init();
@@ -838,54 +839,58 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             mbar_wait_drain(a_full, 0);
             for (int j = issued > NS ? issued - NS : 0; j < issued; j++) mbar_wait_drain(&kv_full[j % NS], (j / NS) & 1);
         }
-    } else if (warp == 1) {
-        // The whole warp runs the issue loop, so the descriptors stay
-        // warp-uniform; the elected lane (lane 0 of the converged warp) issues
-        // every tcgen05 instruction, so one thread issues all MMAs, in order.
-        const uint32_t idS = idesc_mma(128, C::BN, false, false);
-        const uint32_t idA = idesc_mma(128, D, false, true);
+    } else if (warp == 1 || warp == C::NT / 32 - 1) {
+        // Two issuing warps: warp 1 issues S and X, the last warp the
+        // accumulation, so one warp's barrier waits overlap the other's MMAs.
+        // Neither overwrites what the other's MMAs read: S and X are released
+        // by the elementwise warps (sx_free), W by the accumulation (w_free),
+        // a K|V stage once both warps have committed their last read of it.
+        // In each warp the elected lane (lane 0 of the converged warp) issues
+        // all of its tcgen05 instructions, in order.
         const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
-        auto scores = [&](int j) {  // S = A1 K_j^T, X = A2 (K or V)_j^T
-            const uint32_t kaddr = smem_u32(sKV + (j % NS) * 2 * C::KB);
-            const uint32_t xb = MODE == 0 ? kaddr : kaddr + C::KB;  // B of the second score product
-            tc_fence_after();
-            if (elect_one()) {
+        if (warp == 1) {
+            const uint32_t idS = idesc_mma(128, C::BN, false, false);
+            bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2));
+            for (int j = 0; ok && j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[s], (j / NS) & 1, wd, 3))) break;
+                // tile j - 1's S and X are in registers: tile j's may overwrite them
+                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(sx_free, (j - 1) & 1, wd, 9))) break;
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
+                const uint32_t xb = MODE == 0 ? kaddr : kaddr + C::KB;  // B of the second score product
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++)
-                    mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
-                mma_commit(s_full);
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(xb, C::BN, kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    mma_commit(&kv_empty[s]);  // this warp's last read of the stage
+                }
+                __syncwarp();
             }
-            __syncwarp();
-        };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2)) &&
-                  __all_sync(0xffffffffu, mbar_wait(&kv_full[0], 0, wd, 3));
-        if (ok) scores(0);
-        for (int j = 0; ok && j < nkt; j++) {
-            const int s = j % NS;
-            if (j + 1 < nkt) {
-                // tile j's S and X have been read: tile j + 1's may overwrite them
-                if (!__all_sync(0xffffffffu, mbar_wait(sx_free, j & 1, wd, 9))) break;
-                if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[(j + 1) % NS], ((j + 1) / NS) & 1, wd, 3))) break;
-                scores(j + 1);
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
-            tc_fence_after();
-            const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
-            const uint32_t ab = MODE == 0 ? kaddr + C::KB : kaddr;  // B of the accumulation
-            if (elect_one()) {
+        } else {
+            const uint32_t idA = idesc_mma(128, D, false, true);
+            for (int j = 0; j < nkt; j++) {
+                const int s = j % NS;
+                if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sKV + s * 2 * C::KB);
+                const uint32_t ab = MODE == 0 ? kaddr + C::KB : kaddr;  // B of the accumulation
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; kk++)
-                    mma_ts(tAcc, tW + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
-                mma_commit(w_free);
-                mma_commit(&kv_empty[s]);
+                    for (int kk = 0; kk < C::BN / 16; kk++)
+                        mma_ts(tAcc, tW + kk * 8, desc_mnmajor(ab, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
+                    mma_commit(w_free);
+                    mma_commit(&kv_empty[s]);  // this warp's last read of the stage
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
-        if (elect_one()) mma_commit(drain);
+        if (elect_one()) mma_commit(drain);  // one arrival per issuing warp
         __syncwarp();
         mbar_wait_drain(drain, 0);
     } else {
@@ -3308,7 +3313,7 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cud
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual<D, 0><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, mout, a.lse, w.gbar,
+        tc_dual<D, 0><<<ntq * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk64, mv64, mout, a.lse, w.gbar,
                                                                   nullptr, a.T, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
@@ -3358,7 +3363,7 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready, int parts = 3) {
         const int ntq = (a.T + C::BM - 1) / C::BM;
         PLX_TRY(cudaFuncSetAttribute(tc_dual<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_bwd_b1");
-        tc_dual<D, 1><<<ntq * BH, NTHREADS, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, mR, a.lse, nullptr,
+        tc_dual<D, 1><<<ntq * BH, C::NT, C::SMEM, a.stream>>>(mq128, mdo128, mk64, mv64, mR, a.lse, nullptr,
                                                                   w.ebar, a.T, BH, ntq, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
