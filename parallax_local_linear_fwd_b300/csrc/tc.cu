@@ -10,18 +10,19 @@
 //   pass 1 (tc_pass1_pp): S = c Q K^T on a key tile, online softmax,
 //                       Mu += P~ K; emits lse and mu_k = Mu / l; then the
 //   projection        : u = P_h (q - mu_k) rounded to f16, gbar = mu_k . u.
-//   pass 2 (tc_dual)  : S = c Q K^T and G = U K^T on the SAME key tile in
-//                       shared memory (both branches read one KV stream);
-//                       weights p (1 + g - gbar) with p from the stored lse;
-//                       O += W V.
-//   backward B1 (tc_dual, second mode): S = c Q K^T and E = dO V^T;
-//                       weights p e; R += W K and ebar = sum p e.
+//   pass 2 (tc_dual at d = 64, tc_dual_w at d = 128): S = c Q K^T and
+//                       G = U K^T on the SAME key tile in shared memory (both
+//                       branches read one KV stream); weights p (1 + g - gbar)
+//                       with p from the stored lse; O += W V.
+//   backward B1 (tc_dual / tc_dual_pp, second mode): S = c Q K^T and
+//                       E = dO V^T; weights p e; R += W K and ebar = sum p e.
+//   backward B2 (tc_b2, tc_rows): the row math, the dP_h partials.
+//   backward B3 (tc_bwd_b3_q64 at d = 64, tc_bwd_b3 at d = 128): dK, dV, dQ.
 //
 // Warp roles in the tensor-core kernels: warp 0 issues TMA loads, warp 1 owns
-// TMEM and issues the MMAs (one thread), and warpgroups of four warps move
-// scores between TMEM and registers (thread = query row) and write results:
-// one warpgroup per CTA in the one-tile kernels (192 threads), one per query
-// tile in the two-tile kernels (tc_pass1_pp, tc_dual_pp; 320 threads).
+// TMEM and issues MMAs (one elected thread; some kernels give a second warp
+// the accumulation MMAs), and warpgroups of four warps move scores between
+// TMEM and registers (one TMEM lane = one row) and write results.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,7 +43,6 @@ using namespace tc;
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
-constexpr int NTHREADS = 192;
 // Online-softmax rescale threshold (log2 units): the running max is only
 // moved when a row max exceeds it by more than this, so p~ <= 2^8.
 constexpr float RESCALE_TH = 8.f;
@@ -979,7 +979,8 @@ __global__ void __launch_bounds__(DualCfg<D>::NT, 2)
 }
 
 // ============================================ dual-score pass, two query tiles
-// The d = 128 form of tc_dual.  Two 128-row A tiles (Q and U, or Q and dO)
+// The d = 128 form of tc_dual, used for B1 (the second mode); pass 2 at
+// d = 128 runs tc_dual_w below.  Two 128-row A tiles (Q and U, or Q and dO)
 // take 64 KB of shared memory per query tile, so two independent CTAs per SM
 // leave room for one K|V stage each, and every key tile's load latency is
 // exposed.  Here one CTA per SM holds two adjacent query tiles, a = 2m and
