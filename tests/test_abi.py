@@ -70,3 +70,14 @@ def test_host_argument_checks_need_no_gpu(L):
     assert L.parallax_bwd_workspace_bytes(-1, 1, 16, 64, 1) == 0
     # 2^31 elements overflow the supported index range
     assert L.parallax_fwd(p, p, p, p, p, p, p, 1 << 10, 1 << 10, 1 << 10, 64, 1, None) == plx.PLX_ERR_INVALID_ARG
+
+
+def test_decode_probe_workspace_holds_a_partial_per_cta_and_head(L):
+    # the given-probe decode splits the tiles of all heads over at most 1024
+    # CTAs and writes one partial {m, l, sum p r, pad, sum p v [d], sum p r v [d]}
+    # per (CTA, head) pair that overlaps, in slot cta + head
+    for B, H, Lmax, d in ((1, 1, 1, 64), (8, 16, 4096, 64), (4, 16, 4096, 128), (128, 16, 32, 64)):
+        need = (1024 + B * H) * (4 + 2 * d) * 4
+        got = L.parallax_decode_probe_workspace_bytes(B, H, Lmax, d, plx.PLX_BF16)
+        assert got >= need and got % 256 == 0, (B, H, Lmax, d, got, need)
+    assert L.parallax_decode_probe_workspace_bytes(1, 1, 16, 64, plx.PLX_FP32) == 0

@@ -92,3 +92,25 @@ def test_decode_probe_zero_probe_is_softmax_attention():
     out0, lse0 = plx.parallax_decode(q, k, v, P0, lens=lens_t)
     assert rel_err(go, to_host64(out0).reshape(-1, d), "bf16") < TOL_BF16
     assert np.abs(gl - to_host64(lse0).reshape(-1)).max() < 1e-4
+
+
+def test_decode_probe_ctas_span_several_heads():
+    # short caches and many heads: the tiles of all heads split over the CTAs
+    # put several heads in one CTA's range, so partials start and end inside a
+    # CTA, some heads' ranges hold tiles past their length (empty partials),
+    # and a head's partials come from CTAs that also serve other heads
+    B, H, L = 128, 16, 32
+    lens = [1 + (13 * b) % L for b in range(B)]
+    go, gl, ro, rl, *_ = _case(B, H, L, 64, lens, seed=211)
+    _check(go, gl, ro, rl)
+    B, H, L = 32, 16, 100  # two tiles per head: a CTA range may end between them
+    lens = [(1, 64, 65, 100)[b % 4] for b in range(B)]
+    go, gl, ro, rl, *_ = _case(B, H, L, 64, lens, seed=212)
+    _check(go, gl, ro, rl)
+
+
+def test_decode_probe_one_key_one_head():
+    go, gl, ro, rl, *_ = _case(1, 1, 1, 64, None, seed=213)
+    _check(go, gl, ro, rl)
+    go, gl, ro, rl, *_ = _case(1, 1, 1, 128, None, seed=214)
+    _check(go, gl, ro, rl)
