@@ -83,6 +83,7 @@ struct Dec1 {
     static constexpr int QS = 34;            // stride of q's 32-feature parts in shared memory (even: float2)
     static constexpr int SMEM = 1024 + NS * 2 * TB + ZB + NBAR * 8 + 16 + 8 * 4 + TPK * QS * 4 + 16;
     static_assert(KT * TPK == NW * 32, "one thread per (key, feature part)");
+    static_assert(2 * NW <= 8, "the two tile-parity copies of the warp maxima fit their slot");
     static_assert(MIN_CTAS * (SMEM + 1024) <= 233472, "MIN_CTAS CTAs fit an SM's shared memory");
     static constexpr unsigned TMEM_COLS = D;
     // partial of one chunk: {m, l, pad[2]}, sum p k [D], sum p v [D], M [D][D]
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
     uint64_t* drain = mma_done + 1;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
-    float* wmax = (float*)(holder + 4);      // [NW] tile maxima per worker warp
+    float* wmax = (float*)(holder + 4);      // [2][NW] tile maxima per worker warp, by tile parity
     float* sq = wmax + 8;                    // [D] the query, fp32
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,16 +257,19 @@ __global__ void __launch_bounds__(Dec1<D>::NT, Dec1<D>::MIN_CTAS) dec1_chunk(con
             float tmax = sc;
 #pragma unroll
             for (int o = 1; o < KW; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-            if (lane == 0) wmax[warp] = tmax;
+            // two copies by tile parity: a warp that runs ahead writes the next
+            // tile's maximum while a slower one may still read this tile's
+            float* wm = wmax + (j & 1) * NW;
+            if (lane == 0) wm[warp] = tmax;
             // the abort decision rides on the same barrier
             if (!workers_and(ok, NW * 32)) {
                 ok = false;
                 break;
             }
             if (warp == 0 && j >= 1) issue_mma(j - 1);
-            float tm = wmax[0];
+            float tm = wm[0];
 #pragma unroll
-            for (int w = 1; w < NW; w++) tm = fmaxf(tm, wmax[w]);
+            for (int w = 1; w < NW; w++) tm = fmaxf(tm, wm[w]);
             const float m_new = fmaxf(m_run, tm);
             float alpha = 1.f;
             if (m_new > m_run + RESCALE_TH) {  // uniform across the CTA
@@ -429,7 +433,7 @@ constexpr int kMergeThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16* __restrict__ q,
                                                             const int* __restrict__ lens, const float* __restrict__ P,
-                                                            const float* __restrict__ part, int H, int Lmax,
+                                                            const float* part, int H, int Lmax,
                                                             int chunk, int nchunk, float* __restrict__ lse,
                                                             __nv_bfloat16* __restrict__ out) {
     using C = Dec1<D>;
@@ -457,6 +461,8 @@ __global__ void __launch_bounds__(kMergeThreads) dec1_merge(const __nv_bfloat16*
             pv[ps][i] = a < D ? ((const float4*)(P + ((size_t)h * D + a) * D + qr * CQ))[i] : make_float4(0, 0, 0, 0);
     }
     const float qv = tid < D ? __bfloat162float(q[(size_t)bh * D + tid]) : 0.f;
+    // the partials are read only past this wait: `part` is not declared
+    // __restrict__, so the compiler may not move their loads above it
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll
     for (int ps = 0; ps < NPASS; ps++) {
@@ -837,9 +843,11 @@ __global__ void __launch_bounds__(DecP<D>::NT, DecP<D>::MIN_CTAS)
 // feature.  The partials of head h are those of CTAs c(h ntile) .. c(h ntile +
 // ntile - 1), where c(g) = ((g + 1) N - 1) / G is the CTA whose range holds tile g.
 template <int D>
-__global__ void __launch_bounds__(D) decp_merge(const float* __restrict__ part, int ntile, long long G, int N,
+__global__ void __launch_bounds__(D) decp_merge(const float* part, int ntile, long long G, int N,
                                                 float* __restrict__ lse, __nv_bfloat16* __restrict__ out) {
     using C = DecP<D>;
+    // the partials are read only past this wait: `part` is not declared
+    // __restrict__, so the compiler may not move their loads above it
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bh = blockIdx.x, e = threadIdx.x;
     const long long ga = (long long)bh * ntile, gb = ga + ntile - 1;

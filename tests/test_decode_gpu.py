@@ -134,3 +134,23 @@ def test_decode_nan_rows_past_the_lengths_are_ignored():
     go = to_host64(out).reshape(-1, d)
     assert np.isfinite(go).all()
     assert rel_err(go, ro, "bf16") < TOL_BF16
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_ctas_span_several_heads(d):
+    # short caches and many heads: the tiles of all heads split over one wave
+    # of CTAs put several heads in one CTA's range, so a CTA ends one head's
+    # partial (M read out of TMEM, M started afresh) and begins the next inside
+    # its range; ragged lengths leave some heads' tiles in a range empty
+    B, H, L = 64, 16, 64 if d == 64 else 32
+    lens = [1 + (11 * b) % L for b in range(B)]
+    go, gl, ro, rl = _case(B, H, L, d, "bf16", lens, seed=230 + d)
+    assert np.isfinite(go).all()
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
+    # two tiles per head: a CTA's range may end between a head's tiles
+    B, H, L = 24, 16, 128 if d == 64 else 64
+    lens = [(1, L // 2, L // 2 + 1, L)[b % 4] for b in range(B)]
+    go, gl, ro, rl = _case(B, H, L, d, "bf16", lens, seed=240 + d)
+    assert rel_err(go, ro, "bf16") < TOL_BF16
+    assert np.abs(gl - rl).max() < TOL_BF16 * max(1.0, float(np.sqrt(np.mean(rl * rl))))
