@@ -145,7 +145,9 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
                 const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_q16,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v16,
                 const float* __restrict__ P, float* __restrict__ lse, float* __restrict__ gbar,
-                int T, int H, int BH, int npairs, float scale_log2, unsigned* status) {
+                int T, int H, int BH, int npairs, float scale_log2, int* item_ctr, unsigned* status) {
+    // (item_ctr, when given: the work counter of the persistent pass 2 that
+    // follows on the same stream, set to zero here)
     using C = P1PP<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     const int nk = nktb > nkta ? nktb : nkta;
     const int ntiles = nktb > 0 ? 2 : 1;
     const Watchdog wd{status, abortf, KID_TC_PASS1, wait_limit(status)};
+    if (item_ctr && blockIdx.x == 0 && threadIdx.x == 0) *item_ctr = 0;
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -2863,61 +2866,87 @@ __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src
 // ============================================ pass 2 at d = 128, 128-key tiles
 // Forward pass 2 with key tiles of 128, so S = c Q K^T and G = U K^T are
 // N = 128 MMAs (the full tensor rate) and Acc += W V is one N = 128 chain of
-// eight.  One 128-row query tile per CTA; TMEM holds S [0,128), X [128,256),
-// the f16 weights W [256,320) and Acc [320,448) in columns of their own, so
-// the MMA thread issues the next key tile's S as soon as the elementwise warps
-// hold this tile's S in registers, its X once they hold X, and the
-// accumulation after them: the scores of tile j + 1 run while tile j's
-// weights are formed.  Two elementwise warpgroups split each tile's keys
-// (64 each).  K and V have rings of their own: K(j) is free once S(j), X(j)
-// have run, V(j) once Acc += W(j) V(j) has, so each is refilled as early as
-// its last reader allows.
+// eight.  TMEM holds S [0,128), X [128,256), the f16 weights W [256,320) and
+// Acc [320,448) in columns of their own, so the MMA thread issues the next key
+// tile's S as soon as the elementwise warps hold this tile's S in registers,
+// its X once they hold X, and the accumulation after them: the scores of tile
+// j + 1 run while tile j's weights are formed.  Two elementwise warpgroups
+// split each tile's keys (64 each).
+// The CTAs are persistent, one per SM, and take (128-row query tile, head)
+// items in work_item's order (longest tiles first within a head group) from a
+// counter, so that one item's start overlaps the previous item's end:
+//   - four 32 KB slots hold item l's Q and U tiles in one pair (2 (l & 1) and
+//     the next) and its two-stage K ring in the other pair; the pairs swap
+//     roles from item to item, so once every S and X product of item l has
+//     run, item l + 1's Q, U and first K tiles load while item l's last
+//     weights, accumulation and output store run;
+//   - V has a ring of its own, and the output tile a staging slot of its own,
+//     so Acc is read out while the next item's scores run;
+//   - the MMA warp that issues S and X writes a record {item, key tile} per
+//     tile, released with the tile's s_full; the elementwise warps and the
+//     accumulation warp read it there (a ring of NINFO records), and an item
+//     number of -1 ends every role's loop.
 struct DualW {
     static constexpr int D = 128, BM = 128, BN = 128, NT = 352;  // TMA, S|X MMA, 8 elementwise, Acc MMA
-    static constexpr int AB = BM * D * 2;  // one A tile (Q or U): 32 KB
-    static constexpr int KB = BN * D * 2;  // one K or V tile: 32 KB
-    static constexpr int NS = 2;           // K stages, and V stages
-    static constexpr int NBAR = 1 + 4 * NS + 7;
-    static constexpr int SMEM = 1024 + 2 * AB + 2 * NS * KB + NBAR * 8 + 16;
+    static constexpr int AB = BM * D * 2;  // one 32 KB slot: a Q, U, K, V or output tile
+    static constexpr int KB = BN * D * 2;
+    static constexpr int NS = 2;           // K stages per item, V stages
+    static constexpr int NINFO = 4;        // tile records in flight
+    // a_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full, s_free, x_free, w_full, w_free,
+    // acc_done, acc_free, sx_done, item_full, drain
+    static constexpr int NBAR = 1 + 4 * NS + 10;
+    static constexpr int SMEM = 1024 + 4 * AB + NS * KB + AB + NBAR * 8 + 16 + 8 * NINFO;
     static constexpr unsigned TMEM_COLS = 512;  // S [0,128), X [128,256), W [256,320), Acc [320,448)
     static_assert(SMEM <= 232448, "one CTA per SM must fit");
 };
+
+// The item (query tile qt = ntq - 1 - rank, head bh) of work-list position
+// `item`, its first row and its number of 128-key tiles.
+__device__ __forceinline__ void dualw_item(int item, int BH, int ntq, int T, int* bh, int* q0, int* nkt) {
+    int rank;
+    work_item(item, BH, ntq, &rank, bh);
+    *q0 = (ntq - 1 - rank) * DualW::BM;
+    *nkt = min(*q0 + DualW::BM - 1, T - 1) / DualW::BN + 1;
+}
 
 __global__ void __launch_bounds__(DualW::NT, 1)
     tc_dual_w(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
-              const float* __restrict__ gbar, int T, int BH, int ntq, float scale_log2, unsigned* status) {
+              const float* __restrict__ gbar, int T, int BH, int ntq, int* next_item, float scale_log2,
+              unsigned* status) {
+    // (next_item: a device counter, zero at launch; items gridDim.x onwards
+    // are handed out from it)
     using C = DualW;
     constexpr int NS = C::NS, D = C::D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    uint8_t* sA1 = sm;
-    uint8_t* sA2 = sA1 + C::AB;
-    uint8_t* sK = sA2 + C::AB;          // K stage s at s KB
-    uint8_t* sV = sK + NS * C::KB;      // V stage s at s KB
-    uint64_t* bars = (uint64_t*)(sV + NS * C::KB);
+    uint8_t* sSlot = sm;              // four 32 KB slots: Q, U and the K ring, by item parity
+    uint8_t* sV = sSlot + 4 * C::AB;  // V stage s at s KB
+    uint8_t* sOut = sV + NS * C::KB;  // the output tile, staged for its tensor store
+    uint64_t* bars = (uint64_t*)(sOut + C::AB);
     uint64_t* a_full = bars;
     uint64_t* k_full = bars + 1;
     uint64_t* k_empty = k_full + NS;
     uint64_t* v_full = k_empty + NS;
     uint64_t* v_empty = v_full + NS;
-    uint64_t* s_full = v_empty + NS;    // S and X of the tile are in TMEM
+    uint64_t* s_full = v_empty + NS;    // S and X of the tile are in TMEM and its record is written
     uint64_t* s_free = s_full + 1;      // the elementwise warps hold S in registers (256 arrivals)
     uint64_t* x_free = s_full + 2;      // ... and X (256 arrivals)
     uint64_t* w_full = s_full + 3;      // W of the tile is written (256 arrivals)
     uint64_t* w_free = s_full + 4;      // the accumulation has read W
-    uint64_t* acc_done = s_full + 5;
-    uint64_t* drain = s_full + 6;
+    uint64_t* acc_done = s_full + 5;    // an item's last accumulation has run
+    uint64_t* acc_free = s_full + 6;    // the elementwise warps hold an item's Acc in registers (256)
+    uint64_t* sx_done = s_full + 7;     // every S and X product of an item has run
+    uint64_t* item_full = s_full + 8;   // the next item number is in item_slot
+    uint64_t* drain = s_full + 9;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
+    volatile int* item_slot = (volatile int*)(holder + 2);  // [2] by item parity
+    volatile int* info = (volatile int*)(holder + 4);       // [NINFO][2] {item, key tile} by tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int rank, bh;
-    work_item(blockIdx.x, BH, ntq, &rank, &bh);
-    const int qt = ntq - 1 - rank;  // longest query tiles first
-    const int q0 = qt * C::BM;
-    const int nkt = min(q0 + C::BM - 1, T - 1) / C::BN + 1;
+    const int n_items = ntq * BH;
     const Watchdog wd{status, abortf, (unsigned)KID_TC_PASS2, wait_limit(status)};
 
     if (threadIdx.x == 0) {
@@ -2929,12 +2958,15 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        mbar_init(s_full, 1);
+        mbar_init(s_full, 2);  // the products' commit and the record's arrival
         mbar_init(s_free, 256);
         mbar_init(x_free, 256);
         mbar_init(w_full, 256);
         mbar_init(w_free, 1);
         mbar_init(acc_done, 1);
+        mbar_init(acc_free, 256);
+        mbar_init(sx_done, 1);
+        mbar_init(item_full, 1);
         mbar_init(drain, 2);
         fence_barrier_init();
     }
@@ -2951,186 +2983,270 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             prefetch_tmap(&tm_a2);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_expect_tx(a_full, 2 * C::AB);
+            int kiss = 0, viss = 0, aiss = 0;  // K tiles, V tiles and Q|U pairs issued
+            int g0 = 0;                        // the item's first key tile, counted over this CTA's items
+            int next = blockIdx.x;             // this CTA's first item; the later ones come from the counter
+            bool ok = true;
+            for (int l = 0;; l++) {
+                // every S and X product of item l - 1 has run: all four slots are free
+                if (l > 0 && ok) ok = mbar_wait(sx_done, (l - 1) & 1, wd, 12);
+                const int item = ok ? next : n_items;
+                item_slot[l & 1] = item < n_items ? item : -1;
+                mbar_arrive(item_full);
+                if (item >= n_items) break;
+                next = (int)gridDim.x + atomicAdd(next_item, 1);  // claimed now: its latency overlaps this item
+                int bh, q0, nkt;
+                dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+                uint8_t* sA = sSlot + (l & 1) * 2 * C::AB;
+                uint8_t* sK = sSlot + ((l & 1) ^ 1) * 2 * C::AB;
+                mbar_expect_tx(a_full, 2 * C::AB);
 #pragma unroll
-            for (int r = 0; r < D / 64; r++) {
-                tma_load_3d(sA1 + r * C::BM * 128, &tm_a1, r * 64, q0, bh, a_full);
-                tma_load_3d(sA2 + r * C::BM * 128, &tm_a2, r * 64, q0, bh, a_full);
+                for (int r = 0; r < D / 64; r++) {
+                    tma_load_3d(sA + r * C::BM * 128, &tm_a1, r * 64, q0, bh, a_full);
+                    tma_load_3d(sA + C::AB + r * C::BM * 128, &tm_a2, r * 64, q0, bh, a_full);
+                }
+                aiss++;
+                for (int j = 0; j < nkt; j++) {
+                    const int g = g0 + j, s = g % NS;
+                    // the K stage's earlier reader in this item is tile g - NS (sx_done
+                    // covered the earlier items); V's ring runs across items
+                    if (j >= NS && !(ok = mbar_wait(&k_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
+                    mbar_expect_tx(&k_full[s], C::KB);
+#pragma unroll
+                    for (int r = 0; r < D / 64; r++)
+                        tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
+                    kiss = g + 1;
+                    if (g >= NS && !(ok = mbar_wait(&v_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
+                    mbar_expect_tx(&v_full[s], C::KB);
+#pragma unroll
+                    for (int r = 0; r < D / 64; r++)
+                        tma_load_3d(sV + s * C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &v_full[s]);
+                    viss = g + 1;
+                }
+                g0 += nkt;
             }
-            int kiss = 0, viss = 0;
-            for (int j = 0; j < nkt; j++) {
-                const int s = j % NS;
-                if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
-                mbar_expect_tx(&k_full[s], C::KB);
-#pragma unroll
-                for (int r = 0; r < D / 64; r++)
-                    tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
-                kiss = j + 1;
-                if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, wd, 1)) break;
-                mbar_expect_tx(&v_full[s], C::KB);
-#pragma unroll
-                for (int r = 0; r < D / 64; r++)
-                    tma_load_3d(sV + s * C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &v_full[s]);
-                viss = j + 1;
-            }
-            mbar_wait_drain(a_full, 0);
-            for (int j = kiss > NS ? kiss - NS : 0; j < kiss; j++) mbar_wait_drain(&k_full[j % NS], (j / NS) & 1);
-            for (int j = viss > NS ? viss - NS : 0; j < viss; j++) mbar_wait_drain(&v_full[j % NS], (j / NS) & 1);
+            // every load issued lands before the CTA exits
+            if (aiss > 0) mbar_wait_drain(a_full, (aiss - 1) & 1);
+            for (int g = kiss > NS ? kiss - NS : 0; g < kiss; g++) mbar_wait_drain(&k_full[g % NS], (g / NS) & 1);
+            for (int g = viss > NS ? viss - NS : 0; g < viss; g++) mbar_wait_drain(&v_full[g % NS], (g / NS) & 1);
         }
-    } else if (warp == 1 || warp == C::NT / 32 - 1) {
-        // Two issuing warps: warp 1 issues S and X, the last warp the
-        // accumulation, so one warp's barrier waits overlap the other's MMAs.
-        // They share no TMEM or shared memory a later MMA of the other
-        // overwrites (K(j) and V(j) have rings of their own).  In each warp
-        // the elected lane (lane 0 of the converged warp) issues all of its
-        // tcgen05 instructions, in order.
-        if (warp == 1) {
-            const uint32_t idS = idesc_mma(128, C::BN, false, false);
-            const uint32_t a1 = smem_u32(sA1), a2 = smem_u32(sA2);
-            auto product = [&](int j, uint32_t acc_col, uint32_t a, bool last) {  // S = Q K_j^T or X = U K_j^T
-                const uint32_t kaddr = smem_u32(sK + (j % NS) * C::KB);
+    } else if (warp == 1) {
+        // S and X: the whole warp runs the loop, the elected lane issues
+        const uint32_t idS = idesc_mma(128, C::BN, false, false);
+        int g0 = 0;
+        for (int l = 0;; l++) {
+            if (!__all_sync(0xffffffffu, mbar_wait(item_full, l & 1, wd, 13))) break;
+            const int item = item_slot[l & 1];
+            if (item < 0) {
+                // the end, passed on in the next record once the last tile's
+                // S and X have landed (its s_full phase is complete)
+                if (g0 > 0 && !__all_sync(0xffffffffu, mbar_wait(s_full, (g0 - 1) & 1, wd, 15))) break;
+                if (elect_one()) {
+                    info[2 * (g0 % C::NINFO)] = -1;
+                    mbar_arrive(s_full);
+                    mbar_arrive(s_full);
+                }
+                __syncwarp();
+                break;
+            }
+            int bh, q0, nkt;
+            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+            const uint32_t a1 = smem_u32(sSlot + (l & 1) * 2 * C::AB), a2 = a1 + C::AB;
+            uint8_t* sK = sSlot + ((l & 1) ^ 1) * 2 * C::AB;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, l & 1, wd, 2));
+            for (int j = 0; ok && j < nkt; j++) {
+                const int g = g0 + j, s = g % NS;
+                const uint32_t kaddr = smem_u32(sK + s * C::KB);
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&k_full[s], (g / NS) & 1, wd, 3)))) break;
+                // tile g - 1's S is in registers: tile g's may overwrite it; then X likewise
+                if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(s_free, (g - 1) & 1, wd, 9)))) break;
+                tc_fence_after();
+                if (elect_one()) {
+                    info[2 * (g % C::NINFO)] = item;
+                    info[2 * (g % C::NINFO) + 1] = j;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                }
+                __syncwarp();
+                if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(x_free, (g - 1) & 1, wd, 11)))) break;
                 tc_fence_after();
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
-                        mma_ss(acc_col, desc_kmajor(a, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
-                    if (last) {
-                        mma_commit(s_full);
-                        mma_commit(&k_empty[j % NS]);  // K(j) has no other reader
-                    }
-                }
-                __syncwarp();
-            };
-            bool ok = __all_sync(0xffffffffu, mbar_wait(a_full, 0, wd, 2));
-            for (int j = 0; ok && j < nkt; j++) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&k_full[j % NS], (j / NS) & 1, wd, 3))) break;
-                // tile j - 1's S is in registers: tile j's may overwrite it; then X likewise
-                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(s_free, (j - 1) & 1, wd, 9))) break;
-                product(j, tS, a1, false);
-                if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(x_free, (j - 1) & 1, wd, 11))) break;
-                product(j, tX, a2, true);
-            }
-        } else {
-            const uint32_t idA = idesc_mma(128, D, false, true);
-            for (int j = 0; j < nkt; j++) {
-                const int s = j % NS;
-                if (!__all_sync(0xffffffffu, mbar_wait(w_full, j & 1, wd, 5))) break;
-                if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / NS) & 1, wd, 4))) break;
-                tc_fence_after();
-                const uint32_t vaddr = smem_u32(sV + s * C::KB);
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; kk++)
-                        mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                    if (j == nkt - 1) mma_commit(acc_done);  // one phase: the epilogue's only wait
-                    mma_commit(w_free);
-                    mma_commit(&v_empty[s]);
+                        mma_ss(tX, desc_kmajor(a2, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
+                    mma_commit(s_full);
+                    mma_commit(&k_empty[s]);             // K(g) has no other reader
+                    if (j == nkt - 1) mma_commit(sx_done);  // the item's slots may be reloaded
+                    mbar_arrive(s_full);                 // the record above is written
                 }
                 __syncwarp();
             }
+            if (!ok) break;
+            g0 += nkt;
         }
         if (elect_one()) mma_commit(drain);  // one arrival per issuing warp
+        __syncwarp();
+        mbar_wait_drain(drain, 0);
+    } else if (warp == C::NT / 32 - 1) {
+        // the accumulation Acc += W V, item after item
+        const uint32_t idA = idesc_mma(128, D, false, true);
+        int l = 0;  // items whose last accumulation is issued
+        for (int g = 0;; g++) {
+            if (!__all_sync(0xffffffffu, mbar_wait(w_full, g & 1, wd, 5))) break;
+            const int item = info[2 * (g % C::NINFO)];
+            if (item < 0) break;
+            const int j = info[2 * (g % C::NINFO) + 1], s = g % NS;
+            int bh, q0, nkt;
+            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+            // the elementwise warps have read the previous item's Acc
+            if (j == 0 && l > 0 && !__all_sync(0xffffffffu, mbar_wait(acc_free, (l - 1) & 1, wd, 14))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (g / NS) & 1, wd, 4))) break;
+            tc_fence_after();
+            const uint32_t vaddr = smem_u32(sV + s * C::KB);
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; kk++)
+                    mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == nkt - 1) mma_commit(acc_done);  // one phase per item: the epilogue's wait
+                mma_commit(w_free);
+                mma_commit(&v_empty[s]);
+            }
+            __syncwarp();
+            if (j == nkt - 1) l++;
+        }
+        if (elect_one()) mma_commit(drain);
         __syncwarp();
         mbar_wait_drain(drain, 0);
     } else {
         const int wg = (warp - 2) >> 2;  // keys [64 wg, 64 wg + 64) of every tile
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
-        const int t = q0 + row;
         const uint32_t lrow = (uint32_t)(qd * 32) << 16;
-        const bool valid = t < T;
-        const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
-        const float g1 = valid ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
-        const uint64_t SL2 = f2(scale_log2, scale_log2), NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+        const bool leader = qd == 0 && lane == 0;  // issues the warpgroup's output stores
+        const uint64_t SL2 = f2(scale_log2, scale_log2);
+        uint8_t* slot = sOut + wg * (C::BM * 128);  // this warpgroup's 64 output columns
+        // The four warps of a warpgroup leave the item loop together, only
+        // right after a warpgroup-wide AND, so that none of them waits at a
+        // named barrier the others never reach.
         bool ok = true;
-        for (int j = 0; j < nkt; j++) {
-            ok = mbar_wait(s_full, j & 1, wd, 6);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+        int g = 0;
+        for (int l = 0;; l++) {
+            // the next item's first record
+            int item = -1;
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd, 6));
+                if (ok) item = info[2 * (g % C::NINFO)];
+                if (ok && item < 0) mbar_arrive(w_full);  // the end, for the accumulation warp
             }
-            tc_fence_after();
-            const int k0 = j * C::BN;
-            const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
-            const bool need_mask = lim < C::BN;
-            // W of one 32-key chunk c: w = p (x + 1 - gbar), p = exp2(c s - L)
-            auto weights = [&](int c, const uint32_t(&vs)[32], const uint32_t(&vx)[32], uint32_t(&pk)[16]) {
-#pragma unroll
-                for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
-                    const int cc = c * 32 + 2 * i;
-                    const float2 xs =
-                        uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NL2));
-                    float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
-                    if (need_mask) {
-                        if (cc > lim) p0 = 0.f;
-                        if (cc + 1 > lim) p1 = 0.f;
+            if (!named_bar_and(1 + wg, 128, ok && item >= 0)) break;
+            int bh, q0, nkt;
+            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+            const int t = q0 + row;
+            const bool valid = t < T;
+            const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
+            const float g1 = valid ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
+            const uint64_t NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+            for (int j = 0; j < nkt; j++, g++) {
+                if (j > 0) {
+                    ok = mbar_wait(s_full, g & 1, wd, 6);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
                     }
-                    const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
-                    const float2 w = uf2(fmul2(f2(p0, p1), fadd2(xv, G1)));
-                    pk[i] = pack_f16(w.x, w.y);
                 }
-            };
-            const int c0 = 2 * wg, c1 = 2 * wg + 1;
-            uint32_t pk0[16], pk1[16];
-            uint32_t vs0[32], vs1[32];
-            tmem_ld32(tS + lrow + c0 * 32, vs0);
-            tmem_ld32(tS + lrow + c1 * 32, vs1);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(s_free);  // S of the tile this thread needs is in registers
-            {
-                uint32_t vx[32];
-                tmem_ld32(tX + lrow + c0 * 32, vx);
-                tmem_wait_ld();
-                weights(c0, vs0, vx, pk0);
-            }
-            {
-                uint32_t vx[32];
-                tmem_ld32(tX + lrow + c1 * 32, vx);
+                tc_fence_after();
+                const int k0 = j * C::BN;
+                const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+                const bool need_mask = lim < C::BN;
+                // W of one 32-key chunk c: w = p (x + 1 - gbar), p = exp2(c s - L)
+                auto weights = [&](int c, const uint32_t(&vs)[32], const uint32_t(&vx)[32], uint32_t(&pk)[16]) {
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
+                        const int cc = c * 32 + 2 * i;
+                        const float2 xs =
+                            uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NL2));
+                        float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
+                        if (need_mask) {
+                            if (cc > lim) p0 = 0.f;
+                            if (cc + 1 > lim) p1 = 0.f;
+                        }
+                        const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
+                        const float2 w = uf2(fmul2(f2(p0, p1), fadd2(xv, G1)));
+                        pk[i] = pack_f16(w.x, w.y);
+                    }
+                };
+                const int c0 = 2 * wg, c1 = 2 * wg + 1;
+                uint32_t pk0[16], pk1[16];
+                uint32_t vs0[32], vs1[32];
+                tmem_ld32(tS + lrow + c0 * 32, vs0);
+                tmem_ld32(tS + lrow + c1 * 32, vs1);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(x_free);  // ... and X
-                weights(c1, vs1, vx, pk1);
+                mbar_arrive(s_free);  // S of the tile this thread needs is in registers
+                {
+                    uint32_t vx[32];
+                    tmem_ld32(tX + lrow + c0 * 32, vx);
+                    tmem_wait_ld();
+                    weights(c0, vs0, vx, pk0);
+                }
+                {
+                    uint32_t vx[32];
+                    tmem_ld32(tX + lrow + c1 * 32, vx);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(x_free);  // ... and X
+                    weights(c1, vs1, vx, pk1);
+                }
+                if (g > 0) ok = mbar_wait(w_free, (g - 1) & 1, wd, 10);  // the previous accumulation read W
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st16(tW + lrow + c0 * 16, pk0);
+                tmem_st16(tW + lrow + c1 * 16, pk1);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(w_full);
             }
-            if (j > 0) ok = mbar_wait(w_free, (j - 1) & 1, wd, 10);  // the previous accumulation read W
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            // the item's output: Acc to registers (then the next item's
+            // accumulation may overwrite it), bf16 into this warpgroup's half
+            // of the staging slot once its previous store has read it, one
+            // tensor store per warpgroup
+            if (ok) ok = mbar_wait(acc_done, l & 1, wd, 8);
+            ok = named_bar_and(1 + wg, 128, ok);
+            if (!ok) break;
             tc_fence_after();
-            tmem_st16(tW + lrow + c0 * 16, pk0);
-            tmem_st16(tW + lrow + c1 * 16, pk1);
-            tmem_wait_st();
+            uint32_t va[32], vb[32];
+            tmem_ld32(tAcc + lrow + 64 * wg, va);
+            tmem_ld32(tAcc + lrow + 64 * wg + 32, vb);
+            tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(w_full);
-        }
-        if (ok) ok = mbar_wait(acc_done, 0, wd, 8);
-        // each warpgroup stores 64 output columns through its half of the freed Q slot
-        ok = named_bar_and(1 + wg, 128, ok);
-        if (ok) {
-            tc_fence_after();
-            uint8_t* slot = sA1 + wg * (C::BM * 128);
-#pragma unroll 1
-            for (int c = 0; c < 2; c++) {
-                uint32_t v[32];
-                tmem_ld32(tAcc + lrow + 64 * wg + 32 * c, v);
-                tmem_wait_ld();
+            mbar_arrive(acc_free);
+            if (leader) bulk_wait_read_all();
+            named_bar_sync(1 + wg, 128);
 #pragma unroll
-                for (int i = 0; i < 4; i++)
-                    *(uint4*)(slot + sw_off(row, c * 32 + 8 * i, C::BM)) =
-                        make_uint4(pack_bf16(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                                   pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                   pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                   pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+            for (int i = 0; i < 4; i++) {
+                *(uint4*)(slot + sw_off(row, 8 * i, C::BM)) =
+                    make_uint4(pack_bf16(__uint_as_float(va[8 * i]), __uint_as_float(va[8 * i + 1])),
+                               pack_bf16(__uint_as_float(va[8 * i + 2]), __uint_as_float(va[8 * i + 3])),
+                               pack_bf16(__uint_as_float(va[8 * i + 4]), __uint_as_float(va[8 * i + 5])),
+                               pack_bf16(__uint_as_float(va[8 * i + 6]), __uint_as_float(va[8 * i + 7])));
+                *(uint4*)(slot + sw_off(row, 32 + 8 * i, C::BM)) =
+                    make_uint4(pack_bf16(__uint_as_float(vb[8 * i]), __uint_as_float(vb[8 * i + 1])),
+                               pack_bf16(__uint_as_float(vb[8 * i + 2]), __uint_as_float(vb[8 * i + 3])),
+                               pack_bf16(__uint_as_float(vb[8 * i + 4]), __uint_as_float(vb[8 * i + 5])),
+                               pack_bf16(__uint_as_float(vb[8 * i + 6]), __uint_as_float(vb[8 * i + 7])));
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + wg, 128);
-            if (qd == 0 && lane == 0) {
+            if (leader) {
                 tma_store_3d(&tm_out, 64 * wg, q0, bh, slot);
                 bulk_commit();
-                bulk_wait_all();  // the slot stays valid until the store has read it
             }
         }
+        if (leader) bulk_wait_all();  // the slot stays valid until the last store has read it
     }
     tc_fence_before();
     __syncthreads();
@@ -3180,11 +3296,12 @@ bool make_map(CUtensorMap* m, const void* base, int D, int T, int BH, int rows) 
     } while (0)
 
 
-// Workspace of the tensor-core forward: f16 copies of q, k, v, then U (f16)
-// and gbar (fp32).
+// Workspace of the tensor-core forward: f16 copies of q, k, v, then U (f16),
+// gbar (fp32) and the work counter of the persistent pass 2.
 struct TcFwdWs {
     __half *q16, *k16, *v16, *U;
     float* gbar;
+    int* item_ctr;
 };
 TcFwdWs tc_fwd_ws(void* ws, int B, int H, int T, int d) {
     const size_t n = (size_t)B * H * T, nd2 = align256(n * d * 2);
@@ -3195,6 +3312,7 @@ TcFwdWs tc_fwd_ws(void* ws, int B, int H, int T, int d) {
     w.v16 = (__half*)(p + 2 * nd2);
     w.U = (__half*)(p + 3 * nd2);
     w.gbar = (float*)(p + 4 * nd2);
+    w.item_ctr = (int*)(p + 4 * nd2 + align256(n * 4));
     return w;
 }
 
@@ -3295,18 +3413,22 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cud
         timing_begin(a.stream, "tc_pass1");
         tc_pass1_pp<D><<<npairs * BH, C::NT, C::SMEM, a.stream>>>(
             mq_in, mk_in, mk16_128, mmu, mu128, mq128, mv_in, mv16_128, a.P, a.lse, w.gbar, a.T,
-            a.H, BH, npairs, scale_log2, a.status);
+            a.H, BH, npairs, scale_log2, D == 128 ? w.item_ctr : nullptr, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     }
     if (after_pass1) PLX_TRY(after_pass1());
-    if constexpr (D == 128) {  // pass 2: 128-key tiles, S, X, W and Acc in TMEM columns of their own
+    if constexpr (D == 128) {  // pass 2: 128-key tiles, persistent CTAs, one per SM
         using C = DualW;
         const int ntq = (a.T + C::BM - 1) / C::BM;
+        int dev = 0, sms = 0;
+        PLX_TRY(cudaGetDevice(&dev));
+        PLX_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        const int grid = std::min(sms, ntq * BH);
         PLX_TRY(cudaFuncSetAttribute(tc_dual_w, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual_w<<<ntq * BH, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk16_128, mv16_128, mout, a.lse, w.gbar,
-                                                          a.T, BH, ntq, scale_log2, a.status);
+        tc_dual_w<<<grid, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk16_128, mv16_128, mout, a.lse, w.gbar,
+                                                      a.T, BH, ntq, w.item_ctr, scale_log2, a.status);
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // pass 2
@@ -3471,7 +3593,7 @@ bool tc_make_map(void* map, const void* base, int D, int T, int BH, int rows) {
 
 size_t tc_fwd_ws_bytes(int B, int H, int T, int d) {
     const size_t n = (size_t)B * H * T;
-    return 4 * align256(n * d * 2) + align256(n * 4);
+    return 4 * align256(n * d * 2) + align256(n * 4) + 256;
 }
 
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d) { return tc_bwd_bytes(B, H, T, d); }
@@ -3519,6 +3641,7 @@ cudaError_t fwd_bwd_impl(const FwdArgs& f, const BwdArgs& b) {
     fw.v16 = w.v16;
     fw.U = w.U;
     fw.gbar = w.dq_acc;
+    fw.item_ctr = (int*)w.rows;  // B2 writes the rows only after pass 2
     SideStream* ss = nullptr;
     std::unique_lock<std::mutex> lock;
     PLX_TRY(side_stream(&ss, &lock));
