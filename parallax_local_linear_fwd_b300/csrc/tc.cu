@@ -2885,7 +2885,11 @@ __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src
 //   - the MMA warp that issues S and X writes a record {item, key tile} per
 //     tile, released with the tile's s_full; the elementwise warps and the
 //     accumulation warp read it there (a ring of NINFO records), and an item
-//     number of -1 ends every role's loop.
+//     number of -1 ends every role's loop;
+//   - the elementwise warps read an item's output out of Acc after they have
+//     formed the next item's first weights (so the last accumulation's
+//     latency is hidden), and load each item's per-row lse and gbar one item
+//     ahead (the loader claims items two ahead and publishes the next one).
 struct DualW {
     static constexpr int D = 128, BM = 128, BN = 128, NT = 352;  // TMA, S|X MMA, 8 elementwise, Acc MMA
     static constexpr int AB = BM * D * 2;  // one 32 KB slot: a Q, U, K, V or output tile
@@ -2895,7 +2899,7 @@ struct DualW {
     // a_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full, s_free, x_free, w_full, w_free,
     // acc_done, acc_free, sx_done, item_full, drain
     static constexpr int NBAR = 1 + 4 * NS + 10;
-    static constexpr int SMEM = 1024 + 4 * AB + NS * KB + AB + NBAR * 8 + 16 + 8 * NINFO;
+    static constexpr int SMEM = 1024 + 4 * AB + NS * KB + AB + NBAR * 8 + 24 + 8 * NINFO;
     static constexpr unsigned TMEM_COLS = 512;  // S [0,128), X [128,256), W [256,320), Acc [320,448)
     static_assert(SMEM <= 232448, "one CTA per SM must fit");
 };
@@ -2942,8 +2946,8 @@ __global__ void __launch_bounds__(DualW::NT, 1)
     uint64_t* drain = s_full + 9;
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
-    volatile int* item_slot = (volatile int*)(holder + 2);  // [2] by item parity
-    volatile int* info = (volatile int*)(holder + 4);       // [NINFO][2] {item, key tile} by tile
+    volatile int* item_slot = (volatile int*)(holder + 2);  // [2][2] by item parity: {item, next item}
+    volatile int* info = (volatile int*)(holder + 6);       // [NINFO][2] {item, key tile} by tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = ntq * BH;
@@ -2985,18 +2989,21 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             prefetch_tmap(&tm_v);
             int kiss = 0, viss = 0, aiss = 0;  // K tiles, V tiles and Q|U pairs issued
             int g0 = 0;                        // the item's first key tile, counted over this CTA's items
-            int next = blockIdx.x;             // this CTA's first item; the later ones come from the counter
+            // items l and l + 1: this CTA's first item, then the counter's, each
+            // claimed an item ahead of its use so that the atomic's latency is hidden
+            int cur = blockIdx.x;
+            int nxt = (int)gridDim.x + atomicAdd(next_item, 1);
             bool ok = true;
             for (int l = 0;; l++) {
                 // every S and X product of item l - 1 has run: all four slots are free
                 if (l > 0 && ok) ok = mbar_wait(sx_done, (l - 1) & 1, wd, 12);
-                const int item = ok ? next : n_items;
-                item_slot[l & 1] = item < n_items ? item : -1;
-                mbar_arrive(item_full);
-                if (item >= n_items) break;
-                next = (int)gridDim.x + atomicAdd(next_item, 1);  // claimed now: its latency overlaps this item
+                if (!ok || cur >= n_items) {
+                    item_slot[2 * (l & 1)] = -1;
+                    mbar_arrive(item_full);
+                    break;
+                }
                 int bh, q0, nkt;
-                dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+                dualw_item(cur, BH, ntq, T, &bh, &q0, &nkt);
                 uint8_t* sA = sSlot + (l & 1) * 2 * C::AB;
                 uint8_t* sK = sSlot + ((l & 1) ^ 1) * 2 * C::AB;
                 mbar_expect_tx(a_full, 2 * C::AB);
@@ -3006,6 +3013,12 @@ __global__ void __launch_bounds__(DualW::NT, 1)
                     tma_load_3d(sA + C::AB + r * C::BM * 128, &tm_a2, r * 64, q0, bh, a_full);
                 }
                 aiss++;
+                item_slot[2 * (l & 1)] = cur;
+                item_slot[2 * (l & 1) + 1] = nxt < n_items ? nxt : -1;
+                mbar_arrive(item_full);
+                const int nn = nxt < n_items ? (int)gridDim.x + atomicAdd(next_item, 1) : n_items;
+                cur = nxt;
+                nxt = nn;
                 for (int j = 0; j < nkt; j++) {
                     const int g = g0 + j, s = g % NS;
                     // the K stage's earlier reader in this item is tile g - NS (sx_done
@@ -3036,11 +3049,13 @@ __global__ void __launch_bounds__(DualW::NT, 1)
         int g0 = 0;
         for (int l = 0;; l++) {
             if (!__all_sync(0xffffffffu, mbar_wait(item_full, l & 1, wd, 13))) break;
-            const int item = item_slot[l & 1];
+            const int item = item_slot[2 * (l & 1)];
             if (item < 0) {
-                // the end, passed on in the next record once the last tile's
-                // S and X have landed (its s_full phase is complete)
-                if (g0 > 0 && !__all_sync(0xffffffffu, mbar_wait(s_full, (g0 - 1) & 1, wd, 15))) break;
+                // the end, passed on in the next record once both elementwise
+                // warpgroups have taken the last tile's S (s_free): they have
+                // then waited on its s_full phase, which the end's arrivals
+                // must not complete in their place
+                if (g0 > 0 && !__all_sync(0xffffffffu, mbar_wait(s_free, (g0 - 1) & 1, wd, 15))) break;
                 if (elect_one()) {
                     info[2 * (g0 % C::NINFO)] = -1;
                     mbar_arrive(s_full);
@@ -3126,97 +3141,24 @@ __global__ void __launch_bounds__(DualW::NT, 1)
         const bool leader = qd == 0 && lane == 0;  // issues the warpgroup's output stores
         const uint64_t SL2 = f2(scale_log2, scale_log2);
         uint8_t* slot = sOut + wg * (C::BM * 128);  // this warpgroup's 64 output columns
-        // The four warps of a warpgroup leave the item loop together, only
-        // right after a warpgroup-wide AND, so that none of them waits at a
-        // named barrier the others never reach.
+        // Every named-barrier step below is reached by all four warps of the
+        // warpgroup (a wait that fails skips work, not the step), and the
+        // warps leave the item loop together, right after a warpgroup-wide
+        // AND, so that none of them waits at a named barrier the others never
+        // reach.
         bool ok = true;
         int g = 0;
-        for (int l = 0;; l++) {
-            // the next item's first record
-            int item = -1;
-            if (ok) {
-                ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd, 6));
-                if (ok) item = info[2 * (g % C::NINFO)];
-                if (ok && item < 0) mbar_arrive(w_full);  // the end, for the accumulation warp
-            }
-            if (!named_bar_and(1 + wg, 128, ok && item >= 0)) break;
-            int bh, q0, nkt;
-            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
-            const int t = q0 + row;
-            const bool valid = t < T;
-            const float L2 = valid ? lse[(size_t)bh * T + t] * LOG2E : 0.f;
-            const float g1 = valid ? 1.f - gbar[(size_t)bh * T + t] : 0.f;
-            const uint64_t NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
-            for (int j = 0; j < nkt; j++, g++) {
-                if (j > 0) {
-                    ok = mbar_wait(s_full, g & 1, wd, 6);
-                    if (!__all_sync(0xffffffffu, ok)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                tc_fence_after();
-                const int k0 = j * C::BN;
-                const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
-                const bool need_mask = lim < C::BN;
-                // W of one 32-key chunk c: w = p (x + 1 - gbar), p = exp2(c s - L)
-                auto weights = [&](int c, const uint32_t(&vs)[32], const uint32_t(&vx)[32], uint32_t(&pk)[16]) {
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
-                        const int cc = c * 32 + 2 * i;
-                        const float2 xs =
-                            uf2(ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NL2));
-                        float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
-                        if (need_mask) {
-                            if (cc > lim) p0 = 0.f;
-                            if (cc + 1 > lim) p1 = 0.f;
-                        }
-                        const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
-                        const float2 w = uf2(fmul2(f2(p0, p1), fadd2(xv, G1)));
-                        pk[i] = pack_f16(w.x, w.y);
-                    }
-                };
-                const int c0 = 2 * wg, c1 = 2 * wg + 1;
-                uint32_t pk0[16], pk1[16];
-                uint32_t vs0[32], vs1[32];
-                tmem_ld32(tS + lrow + c0 * 32, vs0);
-                tmem_ld32(tS + lrow + c1 * 32, vs1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(s_free);  // S of the tile this thread needs is in registers
-                {
-                    uint32_t vx[32];
-                    tmem_ld32(tX + lrow + c0 * 32, vx);
-                    tmem_wait_ld();
-                    weights(c0, vs0, vx, pk0);
-                }
-                {
-                    uint32_t vx[32];
-                    tmem_ld32(tX + lrow + c1 * 32, vx);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(x_free);  // ... and X
-                    weights(c1, vs1, vx, pk1);
-                }
-                if (g > 0) ok = mbar_wait(w_free, (g - 1) & 1, wd, 10);  // the previous accumulation read W
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_st16(tW + lrow + c0 * 16, pk0);
-                tmem_st16(tW + lrow + c1 * 16, pk1);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(w_full);
-            }
-            // the item's output: Acc to registers (then the next item's
-            // accumulation may overwrite it), bf16 into this warpgroup's half
-            // of the staging slot once its previous store has read it, one
-            // tensor store per warpgroup
-            if (ok) ok = mbar_wait(acc_done, l & 1, wd, 8);
+        int pbh = 0, pq0 = 0;                          // the item whose output is still in Acc
+        int pf_item = -1;                              // the next item, and its row's lse and gbar
+        float pf_lse = 0.f, pf_gbar = 0.f;
+        // item lp's output: Acc to registers (then the next item's
+        // accumulation may overwrite it), bf16 into this warpgroup's half of
+        // the staging slot once its previous store has read it, one tensor
+        // store per warpgroup
+        auto epilogue = [&](int lp) {
+            if (ok) ok = mbar_wait(acc_done, lp & 1, wd, 8);
             ok = named_bar_and(1 + wg, 128, ok);
-            if (!ok) break;
+            if (!ok) return;
             tc_fence_after();
             uint32_t va[32], vb[32];
             tmem_ld32(tAcc + lrow + 64 * wg, va);
@@ -3242,9 +3184,109 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             fence_proxy_async_smem();
             named_bar_sync(1 + wg, 128);
             if (leader) {
-                tma_store_3d(&tm_out, 64 * wg, q0, bh, slot);
+                tma_store_3d(&tm_out, 64 * wg, pq0, pbh, slot);
                 bulk_commit();
             }
+        };
+        for (int l = 0;; l++) {
+            // the next item's first record
+            int item = -1;
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd, 6));
+                if (ok) item = info[2 * (g % C::NINFO)];
+            }
+            if (!named_bar_and(1 + wg, 128, ok && item >= 0)) {
+                if (l > 0) epilogue(l - 1);
+                // the end, for the accumulation warp: after the last output is
+                // read (its acc_done wait follows every arrival on the last
+                // tile's w_full phase, which this arrival must not join)
+                if (ok && item < 0) mbar_arrive(w_full);
+                break;
+            }
+            int bh, q0, nkt;
+            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+            const int t = q0 + row;
+            const bool valid = t < T;
+            if (item != pf_item) {
+                const int tc = min(t, T - 1);
+                pf_lse = lse[(size_t)bh * T + tc];
+                pf_gbar = gbar[(size_t)bh * T + tc];
+            }
+            const float L2 = valid ? pf_lse * LOG2E : 0.f;
+            const float g1 = valid ? 1.f - pf_gbar : 0.f;
+            const uint64_t NL2 = f2(-L2, -L2), G1 = f2(g1, g1);
+            // the next item's, one item ahead (used only at its start)
+            pf_item = item_slot[2 * (l & 1) + 1];
+            if (pf_item >= 0) {
+                int nbh, nq0, nnkt;
+                dualw_item(pf_item, BH, ntq, T, &nbh, &nq0, &nnkt);
+                const int tc = min(nq0 + row, T - 1);
+                pf_lse = lse[(size_t)nbh * T + tc];
+                pf_gbar = gbar[(size_t)nbh * T + tc];
+            }
+            for (int j = 0; j < nkt; j++, g++) {
+                if (ok && j > 0) ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, wd, 6));
+                if (ok) {
+                    tc_fence_after();
+                    const int k0 = j * C::BN;
+                    const int lim = (k0 + C::BN - 1 > q0) ? t - k0 : C::BN;
+                    const bool need_mask = lim < C::BN;
+                    // W of one 32-key chunk c: w = p (x + 1 - gbar), p = exp2(c s - L)
+                    auto weights = [&](int c, const uint32_t(&vs)[32], const uint32_t(&vx)[32],
+                                       uint32_t(&pk)[16]) {
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {  // keys 2i, 2i + 1 of the chunk, one f32x2 op each
+                            const int cc = c * 32 + 2 * i;
+                            const float2 xs = uf2(
+                                ffma2(f2(__uint_as_float(vs[2 * i]), __uint_as_float(vs[2 * i + 1])), SL2, NL2));
+                            float p0 = fast_exp2(xs.x), p1 = fast_exp2(xs.y);
+                            if (need_mask) {
+                                if (cc > lim) p0 = 0.f;
+                                if (cc + 1 > lim) p1 = 0.f;
+                            }
+                            const uint64_t xv = f2(__uint_as_float(vx[2 * i]), __uint_as_float(vx[2 * i + 1]));
+                            const float2 w = uf2(fmul2(f2(p0, p1), fadd2(xv, G1)));
+                            pk[i] = pack_f16(w.x, w.y);
+                        }
+                    };
+                    const int c0 = 2 * wg, c1 = 2 * wg + 1;
+                    uint32_t pk0[16], pk1[16];
+                    uint32_t vs0[32], vs1[32];
+                    tmem_ld32(tS + lrow + c0 * 32, vs0);
+                    tmem_ld32(tS + lrow + c1 * 32, vs1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(s_free);  // S of the tile this thread needs is in registers
+                    {
+                        uint32_t vx[32];
+                        tmem_ld32(tX + lrow + c0 * 32, vx);
+                        tmem_wait_ld();
+                        weights(c0, vs0, vx, pk0);
+                    }
+                    {
+                        uint32_t vx[32];
+                        tmem_ld32(tX + lrow + c1 * 32, vx);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        mbar_arrive(x_free);  // ... and X
+                        weights(c1, vs1, vx, pk1);
+                    }
+                    if (g > 0) ok = mbar_wait(w_free, (g - 1) & 1, wd, 10);  // the previous accumulation read W
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_st16(tW + lrow + c0 * 16, pk0);
+                        tmem_st16(tW + lrow + c1 * 16, pk1);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(w_full);
+                    }
+                }
+                // the previous item's output, once this item's first weights are out
+                if (j == 0 && l > 0) epilogue(l - 1);
+            }
+            pbh = bh;
+            pq0 = q0;
         }
         if (leader) bulk_wait_all();  // the slot stays valid until the last store has read it
     }
