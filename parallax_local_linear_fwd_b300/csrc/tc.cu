@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(P1PP<D>::NT, 1)
     const int ntiles = nktb > 0 ? 2 : 1;
     const Watchdog wd{status, abortf, KID_TC_PASS1, wait_limit(status)};
     if (item_ctr && blockIdx.x == 0 && threadIdx.x == 0) *item_ctr = 0;
+    // pass 2, launched as a programmatic dependent, may be scheduled once
+    // every CTA of this grid has started (it waits for this grid's completion
+    // before it reads anything written here)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         *abortf = 0;
@@ -2916,11 +2920,12 @@ __device__ __forceinline__ void dualw_item(int item, int BH, int ntq, int T, int
 __global__ void __launch_bounds__(DualW::NT, 1)
     tc_dual_w(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
-              const float* __restrict__ gbar, int T, int BH, int ntq, int* next_item, float scale_log2,
-              unsigned* status) {
+              const __grid_constant__ CUtensorMap tm_out, const float* lse, const float* gbar, int T, int BH,
+              int ntq, int* next_item, float scale_log2, unsigned* status) {
     // (next_item: a device counter, zero at launch; items gridDim.x onwards
-    // are handed out from it)
+    // are handed out from it.  lse, gbar and the counter are written by pass
+    // 1 and read only past the griddepcontrol.wait below: lse and gbar are not
+    // __restrict__, so the compiler may not move their loads above it.)
     using C = DualW;
     constexpr int NS = C::NS, D = C::D;
     extern __shared__ uint8_t smem_raw[];
@@ -2980,6 +2985,9 @@ __global__ void __launch_bounds__(DualW::NT, 1)
     tc_fence_after();
     const uint32_t tmem = *holder;
     const uint32_t tS = tmem, tX = tmem + 128, tW = tmem + 256, tAcc = tmem + 320;
+    // launched as a programmatic dependent of pass 1: its outputs (the f16
+    // copies, U, lse, gbar and the zeroed counter) are complete past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         if (lane == 0) {
@@ -3469,8 +3477,20 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cud
         const int grid = std::min(sms, ntq * BH);
         PLX_TRY(cudaFuncSetAttribute(tc_dual_w, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
-        tc_dual_w<<<grid, C::NT, C::SMEM, a.stream>>>(mq128, mu128, mk16_128, mv16_128, mout, a.lse, w.gbar,
-                                                      a.T, BH, ntq, w.item_ctr, scale_log2, a.status);
+        {  // a programmatic dependent of pass 1: its CTAs set up on the SMs pass 1's last CTAs free
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid);
+            cfg.blockDim = dim3(C::NT);
+            cfg.dynamicSmemBytes = C::SMEM;
+            cfg.stream = a.stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            PLX_TRY(cudaLaunchKernelEx(&cfg, tc_dual_w, mq128, mu128, mk16_128, mv16_128, mout, (const float*)a.lse,
+                                       (const float*)w.gbar, a.T, BH, ntq, w.item_ctr, scale_log2, a.status));
+        }
         timing_end(a.stream);
         PLX_TRY(cudaGetLastError());
     } else {  // pass 2
