@@ -311,6 +311,17 @@ PLX_API int parallax_set_wait_limit(long long cycles);
  * previous setting, or -1 if `path` is not a PLX_PATH_* value. */
 PLX_API int parallax_set_path(int path);
 
+/* Caps the number of CTAs the persistent kernels launch for later calls in
+ * this process: pass 2 of the tensor-core forward at d = 128 (one CTA per SM
+ * by default) and B2 of the tensor-core backward at d = 64 (two per SM).  0
+ * restores the default.  Each CTA of those kernels takes work items from a
+ * counter until none are left, so a small cap makes every CTA run many items
+ * of mixed lengths: a test hook for their item changes on small problems.
+ * Results do not depend on the cap (the items' arithmetic is the same; only
+ * which CTA runs an item changes).  Returns the previous cap, or -1 if
+ * `ctas` is negative. */
+PLX_API int parallax_set_persistent_ctas(int ctas);
+
 /*
  * Launch accounting and per-kernel device timing (tracing).
  * Every kernel launch the library makes is counted.  While timing is enabled,

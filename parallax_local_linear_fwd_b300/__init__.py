@@ -28,6 +28,7 @@ __all__ = [
     "parallax_decode", "parallax_decode_workspace_bytes", "parallax_decode_probe",
     "parallax_decode_probe_workspace_bytes",
     "parallax_fwd_probe", "parallax_fwd_probe_workspace_bytes", "parallax_set_wait_limit",
+    "parallax_set_persistent_ctas",
 ]
 
 PLX_OK, PLX_ERR_INVALID_ARG, PLX_ERR_UNSUPPORTED, PLX_ERR_CUDA, PLX_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -50,6 +51,7 @@ _SIGNATURES = {
     "parallax_bwd": (_i, [_vp] * 12 + [_i, _i, _i, _i, _i, _vp]),
     "parallax_last_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "parallax_set_path": (_i, [_i]),
+    "parallax_set_persistent_ctas": (_i, [_i]),
     "parallax_set_wait_limit": (_i, [ctypes.c_longlong]),
     "parallax_strerror": (ctypes.c_char_p, [_i]),
     "parallax_launch_count": (ctypes.c_ulonglong, []),
@@ -452,6 +454,15 @@ def parallax_last_device_error(stream=None):
 
 def parallax_set_path(path: int) -> int:
     return int(lib().parallax_set_path(path))
+
+
+def parallax_set_persistent_ctas(ctas: int) -> int:
+    """Cap on the CTAs of the persistent kernels (0: the default); returns the
+    previous cap.  A test hook: a small cap makes each CTA run many items."""
+    prev = int(lib().parallax_set_persistent_ctas(int(ctas)))
+    if prev < 0:
+        raise ValueError(f"parallax_set_persistent_ctas: ctas must be >= 0, got {ctas}")
+    return prev
 
 
 def parallax_set_wait_limit(cycles: int) -> None:

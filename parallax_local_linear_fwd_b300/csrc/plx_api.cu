@@ -19,6 +19,7 @@ std::mutex g_mu;
 unsigned* g_status[kMaxDevices] = {};  // per-device watchdog word (4 x u32)
 int g_arch_ok[kMaxDevices] = {};        // 0 unknown, 1 sm_103, -1 other
 std::atomic<int> g_path{PLX_PATH_AUTO};
+std::atomic<int> g_persist_cap{0};
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -188,6 +189,7 @@ void timing_end(cudaStream_t s) {
     }
     t_kid = -1;
 }
+int persistent_cta_cap() { return g_persist_cap.load(); }
 }  // namespace plx
 
 extern "C" {
@@ -585,6 +587,11 @@ int parallax_set_wait_limit(long long cycles) {
 int parallax_set_path(int path) {
     if (path != PLX_PATH_AUTO && path != PLX_PATH_SIMT && path != PLX_PATH_TC) return -1;
     return g_path.exchange(path);
+}
+
+int parallax_set_persistent_ctas(int ctas) {
+    if (ctas < 0) return -1;
+    return g_persist_cap.exchange(ctas);
 }
 
 const char* parallax_strerror(int code) {

@@ -118,6 +118,10 @@ size_t decode_probe_ws_bytes(int B, int H, int Lmax, int d);
 cudaError_t decode_probe(const DecodeArgs& a);
 size_t tc_fwd_ws_bytes(int B, int H, int T, int d);
 size_t tc_bwd_ws_bytes(int B, int H, int T, int d);
+// CTAs the persistent kernels (pass 2 at d = 128, B2 at d = 64) launch at
+// most: their own count per SM when 0 (parallax_set_persistent_ctas).
+int persistent_cta_cap();
+
 cudaError_t tc_fwd(const FwdArgs& a);
 cudaError_t tc_bwd(const BwdArgs& a);
 cudaError_t tc_fwd_bwd(const FwdArgs& f, const BwdArgs& b);

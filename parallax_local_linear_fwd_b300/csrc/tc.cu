@@ -3474,7 +3474,8 @@ cudaError_t fwd_impl(const FwdArgs& a, const TcFwdWs& w, const std::function<cud
         int dev = 0, sms = 0;
         PLX_TRY(cudaGetDevice(&dev));
         PLX_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const int grid = std::min(sms, ntq * BH);
+        const int cap = persistent_cta_cap();
+        const int grid = std::min(cap > 0 ? std::min(cap, sms) : sms, ntq * BH);
         PLX_TRY(cudaFuncSetAttribute(tc_dual_w, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         timing_begin(a.stream, "tc_pass2");
         {  // a programmatic dependent of pass 1: its CTAs set up on the SMs pass 1's last CTAs free
@@ -3562,7 +3563,8 @@ cudaError_t bwd_impl(const BwdArgs& a, bool copies_ready, int parts = 3) {
             int dev = 0, sms = 0;
             PLX_TRY(cudaGetDevice(&dev));
             PLX_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-            const int grid = std::min(2 * sms, nchunks * a.H);  // persistent: two CTAs per SM
+            const int cap = persistent_cta_cap();  // persistent: two CTAs per SM
+            const int grid = std::min(cap > 0 ? std::min(cap, 2 * sms) : 2 * sms, nchunks * a.H);
             timing_begin(a.stream, "tc_bwd_b2");
             tc_b2<<<grid, B2T::NT, B2T::SMEM, a.stream>>>(w.q16, a.mu_k, a.P, a.lse, w.R, w.ebar, w.U, w.dmu,
                                                           w.dq_acc, w.rows, w.partial, a.B, a.H, a.T, nchunks,

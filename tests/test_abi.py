@@ -52,6 +52,14 @@ def test_strerror_and_path(L):
     assert plx.parallax_set_path(7) == -1
 
 
+def test_persistent_ctas_cap_needs_no_gpu(L):
+    assert L.parallax_set_persistent_ctas(-1) == -1
+    with pytest.raises(ValueError):
+        plx.parallax_set_persistent_ctas(-1)
+    prev = plx.parallax_set_persistent_ctas(5)
+    assert plx.parallax_set_persistent_ctas(prev) == 5
+
+
 def test_host_argument_checks_need_no_gpu(L):
     p = ctypes.c_void_p(256)  # never dereferenced: the checks fail first
     assert L.parallax_fwd(p, p, p, p, p, p, p, 1, 1, 16, 96, 1, None) == plx.PLX_ERR_UNSUPPORTED
