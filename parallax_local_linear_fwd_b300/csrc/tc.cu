@@ -2886,7 +2886,7 @@ __global__ void __launch_bounds__(256) tc_cast_dq(const float4* __restrict__ src
 //     weights, accumulation and output store run;
 //   - V has a ring of its own, and the output tile a staging slot of its own,
 //     so Acc is read out while the next item's scores run;
-//   - the MMA warp that issues S and X writes a record {item, key tile} per
+//   - the MMA warp that issues S and X writes a record {item, key tile | last} per
 //     tile, released with the tile's s_full; the elementwise warps and the
 //     accumulation warp read it there (a ring of NINFO records), and an item
 //     number of -1 ends every role's loop;
@@ -2952,7 +2952,7 @@ __global__ void __launch_bounds__(DualW::NT, 1)
     uint32_t* holder = (uint32_t*)(bars + C::NBAR);
     volatile int* abortf = (volatile int*)(holder + 1);
     volatile int* item_slot = (volatile int*)(holder + 2);  // [2][2] by item parity: {item, next item}
-    volatile int* info = (volatile int*)(holder + 6);       // [NINFO][2] {item, key tile} by tile
+    volatile int* info = (volatile int*)(holder + 6);       // [NINFO][2] {item, key tile | last << 16} by tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = ntq * BH;
@@ -3003,6 +3003,9 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             int nxt = (int)gridDim.x + atomicAdd(next_item, 1);
             bool ok = true;
             for (int l = 0;; l++) {
+                // item l decoded before the wait, so that only the loads follow it
+                int bh = 0, q0 = 0, nkt = 0;
+                if (cur < n_items) dualw_item(cur, BH, ntq, T, &bh, &q0, &nkt);
                 // every S and X product of item l - 1 has run: all four slots are free
                 if (l > 0 && ok) ok = mbar_wait(sx_done, (l - 1) & 1, wd, 12);
                 if (!ok || cur >= n_items) {
@@ -3010,8 +3013,6 @@ __global__ void __launch_bounds__(DualW::NT, 1)
                     mbar_arrive(item_full);
                     break;
                 }
-                int bh, q0, nkt;
-                dualw_item(cur, BH, ntq, T, &bh, &q0, &nkt);
                 uint8_t* sA = sSlot + (l & 1) * 2 * C::AB;
                 uint8_t* sK = sSlot + ((l & 1) ^ 1) * 2 * C::AB;
                 mbar_expect_tx(a_full, 2 * C::AB);
@@ -3086,7 +3087,7 @@ __global__ void __launch_bounds__(DualW::NT, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     info[2 * (g % C::NINFO)] = item;
-                    info[2 * (g % C::NINFO) + 1] = j;
+                    info[2 * (g % C::NINFO) + 1] = j | (j == nkt - 1 ? 1 << 16 : 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++)
                         mma_ss(tS, desc_kmajor(a1, C::BM, kk), desc_kmajor(kaddr, C::BN, kk), idS, kk > 0);
@@ -3119,9 +3120,8 @@ __global__ void __launch_bounds__(DualW::NT, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(w_full, g & 1, wd, 5))) break;
             const int item = info[2 * (g % C::NINFO)];
             if (item < 0) break;
-            const int j = info[2 * (g % C::NINFO) + 1], s = g % NS;
-            int bh, q0, nkt;
-            dualw_item(item, BH, ntq, T, &bh, &q0, &nkt);
+            const int jl = info[2 * (g % C::NINFO) + 1], j = jl & 0xFFFF, s = g % NS;
+            const bool last = (jl >> 16) != 0;  // the item's last key tile
             // the elementwise warps have read the previous item's Acc
             if (j == 0 && l > 0 && !__all_sync(0xffffffffu, mbar_wait(acc_free, (l - 1) & 1, wd, 14))) break;
             if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (g / NS) & 1, wd, 4))) break;
@@ -3131,12 +3131,12 @@ __global__ void __launch_bounds__(DualW::NT, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; kk++)
                     mma_ts(tAcc, tW + kk * 8, desc_mnmajor(vaddr, C::BN, kk), idA, (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == nkt - 1) mma_commit(acc_done);  // one phase per item: the epilogue's wait
+                if (last) mma_commit(acc_done);  // one phase per item: the epilogue's wait
                 mma_commit(w_free);
                 mma_commit(&v_empty[s]);
             }
             __syncwarp();
-            if (j == nkt - 1) l++;
+            if (last) l++;
         }
         if (elect_one()) mma_commit(drain);
         __syncwarp();
