@@ -3028,22 +3028,31 @@ __global__ void __launch_bounds__(DualW::NT, 1)
                 const int nn = nxt < n_items ? (int)gridDim.x + atomicAdd(next_item, 1) : n_items;
                 cur = nxt;
                 nxt = nn;
-                for (int j = 0; j < nkt; j++) {
-                    const int g = g0 + j, s = g % NS;
-                    // the K stage's earlier reader in this item is tile g - NS (sx_done
-                    // covered the earlier items); V's ring runs across items
-                    if (j >= NS && !(ok = mbar_wait(&k_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
-                    mbar_expect_tx(&k_full[s], C::KB);
+                // K(j), then V(j - 1): V lags K by one tile, so that K(j), which needs
+                // only X(j - 2) to have run, is not held behind V(j - 1)'s wait for the
+                // accumulation of tile j - 3 (which completes later)
+                for (int j = 0; j <= nkt; j++) {
+                    if (j < nkt) {
+                        const int g = g0 + j, s = g % NS;
+                        // the K stage's earlier reader in this item is tile g - NS
+                        // (sx_done covered the earlier items)
+                        if (j >= NS && !(ok = mbar_wait(&k_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
+                        mbar_expect_tx(&k_full[s], C::KB);
 #pragma unroll
-                    for (int r = 0; r < D / 64; r++)
-                        tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
-                    kiss = g + 1;
-                    if (g >= NS && !(ok = mbar_wait(&v_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
-                    mbar_expect_tx(&v_full[s], C::KB);
+                        for (int r = 0; r < D / 64; r++)
+                            tma_load_3d(sK + s * C::KB + r * C::BN * 128, &tm_k, r * 64, j * C::BN, bh, &k_full[s]);
+                        kiss = g + 1;
+                    }
+                    if (j >= 1) {  // V(j - 1); V's ring runs across items
+                        const int g = g0 + j - 1, s = g % NS;
+                        if (g >= NS && !(ok = mbar_wait(&v_empty[s], ((g / NS) - 1) & 1, wd, 1))) break;
+                        mbar_expect_tx(&v_full[s], C::KB);
 #pragma unroll
-                    for (int r = 0; r < D / 64; r++)
-                        tma_load_3d(sV + s * C::KB + r * C::BN * 128, &tm_v, r * 64, j * C::BN, bh, &v_full[s]);
-                    viss = g + 1;
+                        for (int r = 0; r < D / 64; r++)
+                            tma_load_3d(sV + s * C::KB + r * C::BN * 128, &tm_v, r * 64, (j - 1) * C::BN, bh,
+                                        &v_full[s]);
+                        viss = g + 1;
+                    }
                 }
                 g0 += nkt;
             }
